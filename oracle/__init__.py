@@ -1,0 +1,146 @@
+"""CPU oracle for D = alpha*A*B + beta*C (fp64 accumulation, one final rounding).
+
+TEST INFRASTRUCTURE ONLY. The test suite, the package smoke check and the
+benchmark's CPU-baseline leg may load this module; the product path never does.
+It shares no code with the CUDA library: the arithmetic lives in ``oracle.c``
+(plain C, fp64), and this file only marshals arguments through ctypes.
+
+The definition it follows, and every reading of the pages it rests on, is in
+the header comment of ``oracle.c``. Parity of each function here is pinned by
+``tests/test_oracle_pins.py`` against closed forms, brute force and the IEEE-754
+rounding definition.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+import torch
+
+OUT_BF16 = 0
+OUT_F32 = 1
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile oracle.c into liboracle.so (plain gcc, no contraction, no fast-math)."""
+    with _lock:
+        stale = (not os.path.exists(_LIB)) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC)
+        if force or stale:
+            tmp = _LIB + f".tmp{os.getpid()}"
+            cmd = ["gcc", "-O2", "-ffp-contract=off", "-fno-fast-math", "-fPIC", "-shared",
+                   "-pthread", "-std=c11", "-Wall", "-o", tmp, _SRC, "-lm"]
+            subprocess.run(cmd, check=True)
+            os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        build()
+        lib = ctypes.CDLL(_LIB)
+        i64, dbl, vp = ctypes.c_int64, ctypes.c_double, ctypes.c_void_p
+        lib.oracle_gemm_rows.restype = ctypes.c_int
+        lib.oracle_gemm_rows.argtypes = [i64, i64, i64, vp, i64, vp, i64, vp, i64, dbl, dbl,
+                                         ctypes.c_int, vp, i64, vp, i64, vp, i64, ctypes.c_int]
+        lib.oracle_round_bf16.restype = ctypes.c_uint16
+        lib.oracle_round_bf16.argtypes = [dbl]
+        lib.oracle_round_f32.restype = ctypes.c_float
+        lib.oracle_round_f32.argtypes = [dbl]
+        lib.oracle_round_bf16_from_f32_bits.restype = None
+        lib.oracle_round_bf16_from_f32_bits.argtypes = [vp, vp, i64]
+        lib.oracle_round_bf16_array.restype = None
+        lib.oracle_round_bf16_array.argtypes = [vp, vp, i64]
+        _lib = lib
+    return _lib
+
+
+def library_path() -> str:
+    _load()
+    return _LIB
+
+
+def _bits_view(t: torch.Tensor, name: str):
+    """(pointer, row stride in elements) of a 2-D CPU tensor with unit column stride."""
+    if t.device.type != "cpu" or t.dim() != 2:
+        raise ValueError(f"{name}: need a 2-D CPU tensor")
+    if t.numel() and t.stride(1) != 1:
+        raise ValueError(f"{name}: need unit column stride")
+    return t.data_ptr(), (t.stride(0) if t.numel() else max(t.shape[1], 1))
+
+
+def gemm_rows(A: torch.Tensor, B: torch.Tensor, C: torch.Tensor | None, alpha: float,
+              beta: float, out_dtype: int, rows=None, want_pre: bool = False,
+              nthreads: int | None = None):
+    """Rows `rows` (default: all) of D = alpha*A*B + beta*C, computed on the CPU.
+
+    A [M,K] and B [K,N] are bf16 CPU tensors (row-major, any row stride); C is
+    [M,N] of the output dtype or None when beta == 0. alpha and beta are taken
+    as fp32 values (the boundary's parameter type) and widened to fp64.
+    Returns (D, pre): D is numpy uint16 (bf16 bits) or float32, shape
+    [len(rows), N]; pre is the fp64 value before rounding (or None).
+    """
+    lib = _load()
+    if A.dtype != torch.bfloat16 or B.dtype != torch.bfloat16:
+        raise TypeError("A and B must be bf16")
+    M, K = A.shape
+    K2, N = B.shape
+    if K2 != K:
+        raise ValueError("inner dimensions differ")
+    alpha = float(np.float32(alpha))
+    beta = float(np.float32(beta))
+    if rows is None:
+        rows = np.arange(M, dtype=np.int64)
+    rows = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+    a_ptr, lda = _bits_view(A, "A")
+    b_ptr, ldb = _bits_view(B, "B")
+    c_ptr, ldc = 0, max(N, 1)
+    if beta != 0.0:
+        want = torch.bfloat16 if out_dtype == OUT_BF16 else torch.float32
+        if C is None or C.dtype != want or tuple(C.shape) != (M, N):
+            raise ValueError("C must be [M,N] of the output dtype when beta != 0")
+        c_ptr, ldc = _bits_view(C, "C")
+    out_np = np.uint16 if out_dtype == OUT_BF16 else np.float32
+    D = np.zeros((len(rows), N), dtype=out_np)
+    pre = np.zeros((len(rows), N), dtype=np.float64) if want_pre else None
+    if nthreads is None:
+        nthreads = len(os.sched_getaffinity(0))
+    rc = lib.oracle_gemm_rows(M, N, K, a_ptr, lda, b_ptr, ldb, c_ptr, ldc, alpha, beta,
+                              out_dtype, rows.ctypes.data, len(rows), D.ctypes.data, max(N, 1),
+                              pre.ctypes.data if pre is not None else None, max(N, 1),
+                              int(nthreads))
+    if rc != 0:
+        raise RuntimeError("oracle_gemm_rows rejected its arguments")
+    return D, pre
+
+
+def round_bf16(x: float) -> int:
+    """fp64 -> bf16 bits, round to nearest even, one rounding."""
+    return int(_load().oracle_round_bf16(float(x)))
+
+
+def round_bf16_array(x: np.ndarray) -> np.ndarray:
+    x = np.ascontiguousarray(x, dtype=np.float64)
+    out = np.empty(x.shape, dtype=np.uint16)
+    _load().oracle_round_bf16_array(x.ctypes.data, out.ctypes.data, x.size)
+    return out
+
+
+def round_bf16_from_f32_bits(u: np.ndarray) -> np.ndarray:
+    u = np.ascontiguousarray(u, dtype=np.uint32)
+    out = np.empty(u.shape, dtype=np.uint16)
+    _load().oracle_round_bf16_from_f32_bits(u.ctypes.data, out.ctypes.data, u.size)
+    return out
+
+
+def round_f32(x: float) -> float:
+    return float(_load().oracle_round_f32(float(x)))
