@@ -1,0 +1,179 @@
+/*
+ * tpgemm.h - C ABI of the tile-partitioned dense GEMM library for GB300 (sm_103a)
+ *
+ *     D = alpha * A * B + beta * C
+ *
+ * A is bf16 [M, K], B is bf16 [K, N], C and D are [M, N] of the output dtype
+ * (bf16 or fp32); all row-major with explicit row strides. Products are
+ * accumulated in fp32 on the tensor cores; the epilogue applies alpha and beta
+ * in fp32 and rounds once (round-to-nearest-even) to the output dtype.
+ *
+ * Sources for the operation and its conventions:
+ *  - "TorchInductor ganha suporte a GEMMs de alta performance com CuteDSL":
+ *    GEMMs in attention projections and fully-connected layers dominate a
+ *    transformer forward pass (the paragraph on where GPU cycles go); tile
+ *    sizes matched to the tensor-core pipeline, explicit shared-memory stages,
+ *    warp specialisation and TMA are the design levers (same paragraph and the
+ *    one on GEMM design decisions); the epilogue may load an auxiliary tensor
+ *    and add it element-wise (the roadmap paragraph on epilogue fusion), which
+ *    is beta * C here.
+ *  - "cuTile Rust explained", "Ownership crosses the launch boundary" and "The
+ *    useful boundary": the mutable output is split into disjoint tiles, each
+ *    owned by exactly one tile program; inputs are shared and read-only. Here
+ *    every D tile is written by exactly one CTA, with no atomics and no
+ *    split-K accumulation in global memory.
+ *  - Same page, "Why scoped graph capture helps borrowing": only operations
+ *    that allocate nothing are safe to capture and replay. gemm_run allocates
+ *    nothing and never synchronises.
+ *  - "Implementing Tensor Parallelism Communication Overlays ...", "Preventing
+ *    Rust Lifetime Pitfalls in Async GPU Operations": work is asynchronous on
+ *    the caller's stream, so the caller keeps every buffer alive until the
+ *    stream has passed the call.
+ *  - Goldy "Rust Compute Kernels", "Shape contracts" and "Fusing invocations":
+ *    shapes are checked before anything runs and failures are named; a written
+ *    argument that overlaps another argument is rejected.
+ *
+ * Ownership: the caller owns A, B, C and D (device memory of the handle's
+ * device). The library reads A, B, C and writes exactly the M x N elements of
+ * D; bytes in the row-stride padding of D are never touched.
+ *
+ * Errors: every function returns a tpgemm_status. Argument errors are detected
+ * on the host before anything is enqueued. A device-side timeout (a pipeline
+ * wait that exceeded its limit) is recorded in the handle's status word and
+ * reported by gemm_sync_status. No function aborts, exits or traps.
+ */
+#ifndef TPGEMM_H
+#define TPGEMM_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct tpgemm_handle tpgemm_handle; /* opaque */
+
+/* Output (and C) element type. */
+enum tpgemm_out_dtype { TPGEMM_OUT_BF16 = 0, TPGEMM_OUT_F32 = 1 };
+
+enum tpgemm_status {
+    TPGEMM_OK = 0,
+    TPGEMM_ERR_INVALID_ARG = -1,        /* null pointer, negative size, ld < extent, bad dtype */
+    TPGEMM_ERR_ALIGNMENT = -2,          /* pointer or row stride in bytes not a multiple of 16 */
+    TPGEMM_ERR_OVERLAP = -3,            /* D overlaps A or B, or partially overlaps C */
+    TPGEMM_ERR_UNSUPPORTED_DEVICE = -4, /* device is not compute capability 10.3 */
+    TPGEMM_ERR_CUDA = -5,               /* a CUDA runtime/driver call failed */
+    TPGEMM_ERR_TIMEOUT = -6,            /* a device-side pipeline wait ran out (see gemm_sync_status) */
+    TPGEMM_ERR_TOO_LARGE = -7           /* a dimension exceeds 2^31 - 1 */
+};
+
+/* Kernel variants, for gemm_force_variant and gemm_query_plan. */
+enum tpgemm_variant {
+    TPGEMM_VARIANT_AUTO = 0,   /* M <= 64: weight-streaming; otherwise tiled */
+    TPGEMM_VARIANT_TILED = 1,  /* persistent warp-specialised tcgen05 kernel, 128x256 tiles */
+    TPGEMM_VARIANT_STREAM = 2, /* small-M weight-streaming kernel (swapped operands) */
+    TPGEMM_VARIANT_EPILOGUE_ONLY = 3 /* K == 0: D = beta * C */
+};
+
+/*
+ * Creates a handle for CUDA device `device`. Checks that the device is
+ * compute capability 10.3, reads its SM count, resolves the driver's
+ * tensor-map encoder, sets the kernels' shared-memory limits and allocates
+ * the 8-byte device status word (the only allocation the library makes).
+ * *out is set to NULL on failure. Not called on a hot path.
+ */
+int gemm_create(tpgemm_handle **out, int device);
+
+/*
+ * Enqueues D = alpha*A*B + beta*C on `stream` (a cudaStream_t; NULL is the
+ * legacy default stream) and returns without synchronising.
+ *   M, N, K     >= 0, each <= 2^31 - 1.
+ *   A, lda      bf16, row-major [M, K], lda >= K (elements).
+ *   B, ldb      bf16, row-major [K, N], ldb >= N.
+ *   C, ldc      out_dtype, row-major [M, N], ldc >= N. Not read when beta == 0,
+ *               and may then be NULL.
+ *   D, ldd      out_dtype, row-major [M, N], ldd >= N.
+ *   out_dtype   TPGEMM_OUT_BF16 or TPGEMM_OUT_F32.
+ * All non-NULL pointers must be 16-byte aligned and every row stride times
+ * the element size a multiple of 16 bytes (TMA requirements); a stride of a
+ * matrix with one row is not checked. M == 0 or N == 0 enqueues nothing;
+ * K == 0 gives D = beta*C (zeros when beta == 0).
+ * D == C with ldd == ldc (in place) is allowed; any other overlap of D with
+ * A, B or C is TPGEMM_ERR_OVERLAP. Argument errors enqueue nothing. Launch
+ * failures return TPGEMM_ERR_CUDA. Allocates nothing, so it may be captured
+ * into a CUDA graph. Calls on different streams may run concurrently.
+ */
+int gemm_run(tpgemm_handle *h, int64_t M, int64_t N, int64_t K, const void *A, int64_t lda,
+             const void *B, int64_t ldb, const void *C, int64_t ldc, void *D, int64_t ldd,
+             float alpha, float beta, int out_dtype, void *stream);
+
+/*
+ * Synchronises `stream`, then reads and clears the handle's device status
+ * word. Returns TPGEMM_OK, TPGEMM_ERR_TIMEOUT if any kernel since the last
+ * call gave up on a pipeline wait (its output is then incomplete), or
+ * TPGEMM_ERR_CUDA if the synchronisation failed.
+ */
+int gemm_sync_status(tpgemm_handle *h, void *stream);
+
+/*
+ * The argument checks of gemm_run on their own: returns the status gemm_run
+ * would return for these arguments before launching anything (TPGEMM_OK when
+ * they are acceptable). Needs no handle, no GPU and no valid memory: the
+ * pointers are only compared and tested for alignment, never dereferenced.
+ */
+int gemm_check_args(int64_t M, int64_t N, int64_t K, const void *A, int64_t lda, const void *B,
+                    int64_t ldb, const void *C, int64_t ldc, const void *D, int64_t ldd, float beta,
+                    int out_dtype);
+
+/* Frees the handle and its status word. NULL is accepted. */
+int gemm_destroy(tpgemm_handle *h);
+
+/* Static, human-readable name of a tpgemm_status value. */
+const char *gemm_status_string(int status);
+
+/*
+ * Forces a kernel variant for later gemm_run calls on this handle
+ * (TPGEMM_VARIANT_AUTO restores the default choice). TILED and STREAM are
+ * accepted for any K >= 1; STREAM additionally requires M <= 64. Not
+ * thread-safe with concurrent gemm_run calls on the same handle.
+ */
+int gemm_force_variant(tpgemm_handle *h, int variant);
+
+/*
+ * Reports what gemm_run would launch for this problem, without launching:
+ * the variant, the output tile (rows x cols of D), the number of tiles, the
+ * grid size in CTAs, the cluster size, the dynamic shared memory per CTA and
+ * the number of kernel launches. Any output pointer may be NULL.
+ */
+int gemm_query_plan(tpgemm_handle *h, int64_t M, int64_t N, int64_t K, int out_dtype,
+                    int *variant, int *tile_m, int *tile_n, int64_t *num_tiles, int *grid,
+                    int *cluster, int *smem_bytes, int *launches);
+
+/*
+ * Host copy of the persistent tile scheduler: for a grid of `grid` CTAs over
+ * an mt x nt grid of output tiles with grouped raster `group_m`, writes the
+ * (m_tile, n_tile) pair of the i-th tile visited by CTA `cta` into
+ * out[2*i], out[2*i+1] for i < cap, and returns the number of tiles that CTA
+ * owns (or a negative status). The kernels run the same function, so this is
+ * what the partition tests check. No GPU is needed.
+ */
+int64_t gemm_schedule_tiles(int64_t mt, int64_t nt, int group_m, int grid, int cta, int32_t *out,
+                            int64_t cap);
+
+/*
+ * Watchdog self-test: launches one CTA that waits on a barrier no thread will
+ * ever arrive at, with a limit of `timeout_ns` nanoseconds (1 us .. 1 s), then
+ * synchronises `stream`. Returns TPGEMM_ERR_TIMEOUT when the wait ran out as
+ * designed and the context is still usable, TPGEMM_OK if it (wrongly) did not
+ * run out, or TPGEMM_ERR_CUDA. Leaves the handle's status word clear.
+ */
+int gemm_watchdog_selftest(tpgemm_handle *h, uint64_t timeout_ns, void *stream);
+
+/* Number of SMs the handle schedules over, or a negative status. */
+int gemm_num_sms(tpgemm_handle *h);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TPGEMM_H */

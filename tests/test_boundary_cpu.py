@@ -1,0 +1,190 @@
+"""Host-only tests of the C-ABI library: it loads without a GPU, exports every
+function include/tpgemm.h declares, rejects bad arguments with the documented
+status before anything is launched, and its tile scheduler partitions the
+output exactly (each tile owned by one CTA: "cuTile Rust explained",
+"Ownership crosses the launch boundary")."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+import tile_partitioned_dense_gb300 as tpd
+from tile_partitioned_dense_gb300 import build_ext
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "tpgemm.h")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    build_ext.build()
+    tpd.load_library()
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(gemm_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = _declared_functions()
+    for required in ["gemm_create", "gemm_run", "gemm_destroy", "gemm_sync_status", "gemm_status_string"]:
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol():
+    lib = ctypes.CDLL(tpd.LIB_PATH)
+    missing = [n for n in _declared_functions() if not hasattr(lib, n)]
+    assert not missing, missing
+    out = subprocess.run(["nm", "-D", "--defined-only", tpd.LIB_PATH], capture_output=True, text=True)
+    if out.returncode == 0:
+        exported = set(re.findall(r"\sT\s(\w+)", out.stdout))
+        for n in _declared_functions():
+            assert n in exported, n
+
+
+def test_status_strings():
+    for code, name in [(0, "TPGEMM_OK"), (-1, "TPGEMM_ERR_INVALID_ARG"), (-2, "TPGEMM_ERR_ALIGNMENT"),
+                       (-3, "TPGEMM_ERR_OVERLAP"), (-4, "TPGEMM_ERR_UNSUPPORTED_DEVICE"),
+                       (-5, "TPGEMM_ERR_CUDA"), (-6, "TPGEMM_ERR_TIMEOUT"), (-7, "TPGEMM_ERR_TOO_LARGE")]:
+        assert tpd.gemm_status_string(code) == name
+    assert tpd.gemm_status_string(123) == "TPGEMM_ERR_UNKNOWN"
+
+
+def test_null_handle_is_rejected_without_gpu():
+    assert tpd.gemm_run(None, 8, 8, 8, 0x1000, 8, 0x2000, 8, None, 8, 0x3000, 8, 1.0, 0.0, 0, None) == tpd.ERR_INVALID_ARG
+    assert tpd.gemm_sync_status(None, None) == tpd.ERR_INVALID_ARG
+    assert tpd.gemm_destroy(None) == tpd.OK
+    assert tpd.gemm_force_variant(None, 0) == tpd.ERR_INVALID_ARG
+    assert tpd.gemm_watchdog_selftest(None, 10000, None) == tpd.ERR_INVALID_ARG
+    assert tpd.gemm_num_sms(None) == tpd.ERR_INVALID_ARG
+
+
+# Fake, well-separated, 16-byte aligned device addresses: gemm_check_args only
+# compares and aligns pointers.
+A0, B0, C0, D0 = 0x10000000, 0x20000000, 0x30000000, 0x40000000
+
+
+def chk(M=64, N=64, K=64, A=A0, lda=None, B=B0, ldb=None, C=None, ldc=None, D=D0, ldd=None, beta=0.0,
+        out=tpd.OUT_BF16):
+    lda = K if lda is None else lda
+    ldb = N if ldb is None else ldb
+    ldc = N if ldc is None else ldc
+    ldd = N if ldd is None else ldd
+    return tpd.gemm_check_args(M, N, K, A, lda, B, ldb, C, ldc, D, ldd, beta, out)
+
+
+def test_check_args_accepts_valid():
+    assert chk() == tpd.OK
+    assert chk(C=C0, beta=1.0) == tpd.OK
+    assert chk(M=4096, N=4096, K=4096) == tpd.OK
+    assert chk(out=tpd.OUT_F32, C=C0, beta=-2.0) == tpd.OK
+    assert chk(M=1, K=7, lda=7) == tpd.OK  # one row: its stride is never used
+
+
+def test_check_args_invalid():
+    assert chk(out=2) == tpd.ERR_INVALID_ARG
+    assert chk(M=-1) == tpd.ERR_INVALID_ARG
+    assert chk(K=-3) == tpd.ERR_INVALID_ARG
+    assert chk(D=None) == tpd.ERR_INVALID_ARG
+    assert chk(A=None) == tpd.ERR_INVALID_ARG
+    assert chk(B=None) == tpd.ERR_INVALID_ARG
+    assert chk(beta=1.0, C=None) == tpd.ERR_INVALID_ARG
+    assert chk(lda=56) == tpd.ERR_INVALID_ARG
+    assert chk(ldb=56) == tpd.ERR_INVALID_ARG
+    assert chk(ldd=56) == tpd.ERR_INVALID_ARG
+    assert chk(C=C0, ldc=56, beta=1.0) == tpd.ERR_INVALID_ARG
+
+
+def test_check_args_too_large():
+    assert chk(M=2 ** 31) == tpd.ERR_TOO_LARGE
+    assert chk(K=2 ** 31, lda=2 ** 31) == tpd.ERR_TOO_LARGE
+
+
+def test_check_args_alignment():
+    assert chk(A=A0 + 8) == tpd.ERR_ALIGNMENT
+    assert chk(B=B0 + 2) == tpd.ERR_ALIGNMENT
+    assert chk(D=D0 + 4) == tpd.ERR_ALIGNMENT
+    assert chk(C=C0 + 8, beta=1.0) == tpd.ERR_ALIGNMENT
+    assert chk(K=60, lda=60) == tpd.ERR_ALIGNMENT    # 120-byte rows
+    assert chk(N=60, ldb=60, ldd=64) == tpd.ERR_ALIGNMENT
+    assert chk(N=60, ldb=64, ldd=60) == tpd.ERR_ALIGNMENT
+    assert chk(N=60, ldb=64, ldd=60, out=tpd.OUT_F32) == tpd.OK  # 240 bytes is a 16-byte multiple
+    assert chk(K=60, lda=64) == tpd.OK
+
+
+def test_check_args_overlap():
+    # D inside A
+    assert chk(D=A0 + 64 * 16) == tpd.ERR_OVERLAP
+    # D overlapping B's last row
+    assert chk(D=B0 + 63 * 64 * 2) == tpd.ERR_OVERLAP
+    # in place D == C, same stride: allowed
+    assert chk(C=D0, beta=1.0) == tpd.OK
+    # D == C with a different stride, or a shifted C: rejected
+    assert chk(C=D0, ldc=72, beta=1.0) == tpd.ERR_OVERLAP
+    assert chk(C=D0 + 16, beta=1.0) == tpd.ERR_OVERLAP
+    # C may alias D freely when it is not read (beta == 0)
+    assert chk(C=D0 + 16, beta=0.0) == tpd.OK
+    # A and B may overlap each other (both read-only)
+    assert chk(B=A0) == tpd.OK
+    # adjacent, not overlapping
+    assert chk(D=A0 + 64 * 64 * 2) == tpd.OK
+
+
+def test_check_args_degenerate():
+    assert chk(M=0, A=None, B=None, D=None) == tpd.OK
+    assert chk(N=0, A=None, B=None, D=None) == tpd.OK
+    assert chk(K=0, A=None, B=None) == tpd.OK
+    assert chk(K=0, A=None, B=None, C=C0, beta=2.0) == tpd.OK
+
+
+def test_create_without_gpu_fails_cleanly():
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    h = ctypes.c_void_p()
+    st = tpd.load_library().gemm_create(ctypes.byref(h), 0)
+    assert st in (tpd.ERR_CUDA, tpd.ERR_INVALID_ARG)
+    assert not h.value
+
+
+def _tile_grid(M, N, bm=128, bn=256):
+    return (M + bm - 1) // bm, (N + bn - 1) // bn
+
+
+@pytest.mark.parametrize("mt,nt", [_tile_grid(256, 256), _tile_grid(4096, 4096), _tile_grid(8192, 6144),
+                                   _tile_grid(8192, 4096), (1, 1), (3, 7), (17, 5), (64, 1), (1, 224)])
+@pytest.mark.parametrize("grid", [1, 7, 148, 152, 160, 1000])
+@pytest.mark.parametrize("group_m", [1, 8, 16])
+def test_schedule_is_an_exact_partition(mt, nt, grid, group_m):
+    grid = min(grid, mt * nt) if mt * nt else 1
+    seen = {}
+    for cta in range(grid):
+        tiles = tpd.gemm_schedule_tiles(mt, nt, group_m, grid, cta)
+        for (m, n) in tiles:
+            assert 0 <= m < mt and 0 <= n < nt
+            assert (m, n) not in seen, f"tile {(m, n)} owned by CTAs {seen[(m, n)]} and {cta}"
+            seen[(m, n)] = cta
+        # balanced: every CTA owns floor or ceil of tiles/grid
+        assert len(tiles) in (mt * nt // grid, -(-mt * nt // grid))
+    assert len(seen) == mt * nt
+
+
+def test_schedule_grouped_raster_order():
+    # the first tiles of a band walk down the band before moving right
+    order = [tpd.gemm_schedule_tiles(40, 8, 16, 1, 0)[i] for i in range(20)]
+    assert order[:16] == [(m, 0) for m in range(16)]
+    assert order[16:20] == [(m, 1) for m in range(4)]
+    # the last band has 40 - 32 = 8 rows
+    tail = tpd.gemm_schedule_tiles(40, 8, 16, 1, 0)[32 * 8:32 * 8 + 9]
+    assert tail[:8] == [(32 + m, 0) for m in range(8)] and tail[8] == (32, 1)
+
+
+def test_schedule_rejects_bad_arguments():
+    lib = tpd.load_library()
+    assert lib.gemm_schedule_tiles(4, 4, 0, 1, 0, None, 0) == tpd.ERR_INVALID_ARG
+    assert lib.gemm_schedule_tiles(4, 4, 8, 2, 2, None, 0) == tpd.ERR_INVALID_ARG
+    assert lib.gemm_schedule_tiles(4, 4, 8, 2, 0, None, 3) == tpd.ERR_INVALID_ARG

@@ -1,0 +1,198 @@
+"""Python binding of the tile-partitioned dense GEMM library (libtpgemm.so).
+
+Argument marshalling only: every step of D = alpha*A*B + beta*C runs in the
+CUDA kernels behind the C ABI of include/tpgemm.h. The functions below carry
+the same names and arguments as that header; ``matmul`` is a convenience that
+takes torch tensors, passes their pointers, strides and the current stream,
+and allocates D with torch when none is given. There is no CPU fallback: if
+the extension is not built, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "libtpgemm.so")
+
+OUT_BF16 = 0
+OUT_F32 = 1
+VARIANT_AUTO = 0
+VARIANT_TILED = 1
+VARIANT_STREAM = 2
+VARIANT_EPILOGUE_ONLY = 3
+
+OK = 0
+ERR_INVALID_ARG = -1
+ERR_ALIGNMENT = -2
+ERR_OVERLAP = -3
+ERR_UNSUPPORTED_DEVICE = -4
+ERR_CUDA = -5
+ERR_TIMEOUT = -6
+ERR_TOO_LARGE = -7
+
+_lib = None
+
+
+class TpgemmError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        super().__init__(f"{what}: {gemm_status_string(status)} ({status})")
+        self.status = status
+
+
+def load_library() -> ctypes.CDLL:
+    """Load libtpgemm.so from the package directory (raises if it is missing)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(
+                f"{LIB_PATH} is not built; run `python -c 'import __graft_entry__ as g; g.build()'`")
+        lib = ctypes.CDLL(LIB_PATH)
+        i64, i32, vp, f32 = ctypes.c_int64, ctypes.c_int, ctypes.c_void_p, ctypes.c_float
+        pi32, pi64 = ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_int64)
+        sig = {
+            "gemm_create": (i32, [ctypes.POINTER(vp), i32]),
+            "gemm_run": (i32, [vp, i64, i64, i64, vp, i64, vp, i64, vp, i64, vp, i64, f32, f32, i32, vp]),
+            "gemm_sync_status": (i32, [vp, vp]),
+            "gemm_check_args": (i32, [i64, i64, i64, vp, i64, vp, i64, vp, i64, vp, i64, f32, i32]),
+            "gemm_destroy": (i32, [vp]),
+            "gemm_status_string": (ctypes.c_char_p, [i32]),
+            "gemm_force_variant": (i32, [vp, i32]),
+            "gemm_query_plan": (i32, [vp, i64, i64, i64, i32, pi32, pi32, pi32, pi64, pi32, pi32, pi32, pi32]),
+            "gemm_schedule_tiles": (i64, [i64, i64, i32, i32, i32, ctypes.POINTER(ctypes.c_int32), i64]),
+            "gemm_watchdog_selftest": (i32, [vp, ctypes.c_uint64, vp]),
+            "gemm_num_sms": (i32, [vp]),
+        }
+        for name, (res, args) in sig.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = lib
+    return _lib
+
+
+# ------------------------------------------------------------------ C ABI, same names
+
+def gemm_create(device: int = 0) -> ctypes.c_void_p:
+    h = ctypes.c_void_p()
+    st = load_library().gemm_create(ctypes.byref(h), int(device))
+    if st != OK:
+        raise TpgemmError(st, "gemm_create")
+    return h
+
+
+def gemm_run(h, M, N, K, A, lda, B, ldb, C, ldc, D, ldd, alpha, beta, out_dtype, stream) -> int:
+    return load_library().gemm_run(h, M, N, K, A, lda, B, ldb, C, ldc, D, ldd, alpha, beta,
+                                   out_dtype, stream)
+
+
+def gemm_sync_status(h, stream=None) -> int:
+    return load_library().gemm_sync_status(h, stream)
+
+
+def gemm_check_args(M, N, K, A, lda, B, ldb, C, ldc, D, ldd, beta, out_dtype) -> int:
+    return load_library().gemm_check_args(M, N, K, A, lda, B, ldb, C, ldc, D, ldd, beta, out_dtype)
+
+
+def gemm_destroy(h) -> int:
+    return load_library().gemm_destroy(h)
+
+
+def gemm_status_string(status: int) -> str:
+    return load_library().gemm_status_string(int(status)).decode()
+
+
+def gemm_force_variant(h, variant: int) -> int:
+    return load_library().gemm_force_variant(h, int(variant))
+
+
+def gemm_query_plan(h, M, N, K, out_dtype) -> dict:
+    v, tm, tn, g, cl, sm, la = (ctypes.c_int() for _ in range(7))
+    nt = ctypes.c_int64()
+    st = load_library().gemm_query_plan(h, M, N, K, out_dtype, ctypes.byref(v), ctypes.byref(tm),
+                                        ctypes.byref(tn), ctypes.byref(nt), ctypes.byref(g),
+                                        ctypes.byref(cl), ctypes.byref(sm), ctypes.byref(la))
+    if st != OK:
+        raise TpgemmError(st, "gemm_query_plan")
+    return dict(variant=v.value, tile_m=tm.value, tile_n=tn.value, num_tiles=nt.value, grid=g.value,
+                cluster=cl.value, smem_bytes=sm.value, launches=la.value)
+
+
+def gemm_schedule_tiles(mt: int, nt: int, group_m: int, grid: int, cta: int):
+    """List of (m_tile, n_tile) visited by CTA `cta` (the kernels' own schedule)."""
+    lib = load_library()
+    n = lib.gemm_schedule_tiles(mt, nt, group_m, grid, cta, None, 0)
+    if n < 0:
+        raise TpgemmError(int(n), "gemm_schedule_tiles")
+    buf = (ctypes.c_int32 * max(2 * n, 1))()
+    lib.gemm_schedule_tiles(mt, nt, group_m, grid, cta, buf, n)
+    return [(buf[2 * i], buf[2 * i + 1]) for i in range(n)]
+
+
+def gemm_watchdog_selftest(h, timeout_ns: int, stream=None) -> int:
+    return load_library().gemm_watchdog_selftest(h, int(timeout_ns), stream)
+
+
+def gemm_num_sms(h) -> int:
+    return load_library().gemm_num_sms(h)
+
+
+# ------------------------------------------------------------------ torch convenience
+
+class Gemm:
+    """Owns one handle; ``__call__`` runs D = alpha*A*B + beta*C on torch tensors."""
+
+    def __init__(self, device: int = 0):
+        self.device = int(device)
+        self.handle = gemm_create(self.device)
+
+    def close(self):
+        if self.handle is not None:
+            gemm_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def __call__(self, A, B, C=None, alpha=1.0, beta=0.0, out_dtype=None, out=None, stream=None):
+        import torch
+        if out_dtype is None:
+            out_dtype = out.dtype if out is not None else torch.bfloat16
+        odt = {torch.bfloat16: OUT_BF16, torch.float32: OUT_F32}[out_dtype]
+        M, K = A.shape
+        N = B.shape[1]
+        if out is None:
+            out = torch.empty((M, N), dtype=out_dtype, device=A.device)
+        if stream is None:
+            stream = torch.cuda.current_stream(A.device).cuda_stream
+
+        def ptr_ld(t, cols):
+            if t is None:
+                return None, max(cols, 1)
+            if t.dim() != 2 or (t.numel() and t.stride(1) != 1):
+                raise ValueError("2-D tensors with unit column stride are required")
+            return t.data_ptr(), (t.stride(0) if t.shape[0] > 1 else max(t.stride(0), cols, 1))
+
+        a, lda = ptr_ld(A, K)
+        b, ldb = ptr_ld(B, N)
+        c, ldc = ptr_ld(C, N)
+        d, ldd = ptr_ld(out, N)
+        st = gemm_run(self.handle, M, N, K, a, lda, b, ldb, c, ldc, d, ldd, float(alpha), float(beta),
+                      odt, stream)
+        if st != OK:
+            raise TpgemmError(st, "gemm_run")
+        return out
+
+
+_default = {}
+
+
+def matmul(A, B, C=None, alpha=1.0, beta=0.0, out_dtype=None, out=None, stream=None):
+    """D = alpha*A*B + beta*C on the GPU through the C ABI (one handle per device)."""
+    dev = A.device.index if A.device.index is not None else 0
+    if dev not in _default:
+        _default[dev] = Gemm(dev)
+    return _default[dev](A, B, C, alpha, beta, out_dtype, out, stream)

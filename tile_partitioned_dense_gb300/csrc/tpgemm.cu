@@ -1,0 +1,479 @@
+// Host side of the C ABI declared in include/tpgemm.h: argument checks, kernel
+// selection, TMA tensor-map encoding and launch. Nothing here allocates or
+// synchronises on the gemm_run path; the only device allocation is the 8-byte
+// status word made by gemm_create.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstdlib>
+#include <cstring>
+#include <new>
+
+#include "tpgemm.h"
+
+#include "aux_kernels.cuh"
+#include "gemm_stream.cuh"
+#include "gemm_tiled.cuh"
+#include "schedule.cuh"
+
+namespace {
+
+constexpr int64_t kMaxDim = 2147483647; // 2^31 - 1
+constexpr int kGroupM = 16;             // grouped-raster band height, in tiles
+constexpr int kStreamMaxM = 64;
+
+struct Plan {
+    int variant = TPGEMM_VARIANT_AUTO;
+    int tile_m = 0, tile_n = 0;
+    int64_t num_tiles = 0;
+    int grid = 0;
+    int cluster = 1;
+    int smem = 0;
+    int launches = 0;
+    int mt_pad = 0, stages = 0, split = 1;
+};
+
+} // namespace
+
+struct tpgemm_handle {
+    int device = -1;
+    int num_sms = 0;
+    uint32_t *status = nullptr;
+    PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+    int forced = TPGEMM_VARIANT_AUTO;
+    uint64_t timeout_ns = 2000000000ull;
+    // co-resident 2-CTA clusters of the streaming kernel, per [out f32][mt/16 - 1]
+    int stream_clusters[2][4] = {{0, 0, 0, 0}, {0, 0, 0, 0}};
+};
+
+namespace {
+
+struct DeviceGuard {
+    int prev = -1;
+    bool switched = false;
+    explicit DeviceGuard(int dev) {
+        if (cudaGetDevice(&prev) == cudaSuccess && prev != dev) {
+            switched = cudaSetDevice(dev) == cudaSuccess;
+        }
+    }
+    ~DeviceGuard() {
+        if (switched) cudaSetDevice(prev);
+    }
+};
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Byte range [lo, hi) touched by a row-major rows x cols matrix with row stride ld.
+struct Range {
+    uintptr_t lo, hi;
+};
+Range byte_range(const void *p, int64_t rows, int64_t cols, int64_t ld, int64_t elt) {
+    const uintptr_t lo = reinterpret_cast<uintptr_t>(p);
+    if (rows <= 0 || cols <= 0) return {lo, lo};
+    return {lo, lo + static_cast<uintptr_t>(((rows - 1) * ld + cols) * elt)};
+}
+bool overlaps(Range a, Range b) { return a.lo < b.hi && b.lo < a.hi && a.lo != a.hi && b.lo != b.hi; }
+
+// Row stride in bytes given to the tensor map: the caller's, except for a
+// single-row matrix whose stride is never used (any 16-byte multiple works).
+uint64_t tma_stride(int64_t rows, int64_t cols, int64_t ld, int64_t elt) {
+    if (rows <= 1) return static_cast<uint64_t>(((cols * elt) + 15) / 16 * 16);
+    return static_cast<uint64_t>(ld * elt);
+}
+
+int encode_2d(tpgemm_handle *h, CUtensorMap *map, CUtensorMapDataType dt, const void *ptr,
+              uint64_t inner, uint64_t outer, uint64_t stride_bytes, uint32_t box_inner,
+              uint32_t box_outer) {
+    cuuint64_t dims[2] = {inner, outer};
+    cuuint64_t strides[1] = {stride_bytes};
+    cuuint32_t box[2] = {box_inner, box_outer};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = h->encode(map, dt, 2, const_cast<void *>(ptr), dims, strides, box, estr,
+                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? TPGEMM_OK : TPGEMM_ERR_CUDA;
+}
+
+int stream_clusters_for(tpgemm_handle *h, bool f32, int mt, int stages) {
+    int &slot = h->stream_clusters[f32 ? 1 : 0][mt / 16 - 1];
+    if (slot > 0) return slot;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * (h->num_sms / 2), 1, 1);
+    cfg.blockDim = dim3(tpg::stream::THREADS, 1, 1);
+    cfg.dynamicSmemBytes = tpg::stream::smem_bytes(mt, stages, 2);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    cudaError_t e = f32 ? cudaOccupancyMaxActiveClusters(&n, tpg::stream::gemm_stream_kernel<true, 2>, &cfg)
+                        : cudaOccupancyMaxActiveClusters(&n, tpg::stream::gemm_stream_kernel<false, 2>, &cfg);
+    if (e != cudaSuccess || n <= 0) {
+        (void)cudaGetLastError();
+        n = h->num_sms / 2;
+    }
+    slot = n;
+    return n;
+}
+
+Plan make_plan(tpgemm_handle *h, int64_t M, int64_t N, int64_t K, int out_dtype) {
+    Plan pl;
+    if (M == 0 || N == 0) return pl;
+    if (K == 0) {
+        pl.variant = TPGEMM_VARIANT_EPILOGUE_ONLY;
+        const int64_t total = M * N;
+        int64_t blocks = (total + 1023) / 1024;
+        if (blocks > 8LL * h->num_sms) blocks = 8LL * h->num_sms;
+        pl.grid = static_cast<int>(blocks < 1 ? 1 : blocks);
+        pl.launches = 1;
+        return pl;
+    }
+    int variant = h->forced;
+    if (variant == TPGEMM_VARIANT_AUTO) variant = M <= kStreamMaxM ? TPGEMM_VARIANT_STREAM : TPGEMM_VARIANT_TILED;
+    if (variant == TPGEMM_VARIANT_STREAM && M > kStreamMaxM) variant = TPGEMM_VARIANT_TILED;
+    pl.variant = variant;
+    pl.launches = 1;
+    if (variant == TPGEMM_VARIANT_TILED) {
+        const int64_t mt = (M + tpg::tiled::BM - 1) / tpg::tiled::BM;
+        const int64_t nt = (N + tpg::tiled::BN - 1) / tpg::tiled::BN;
+        pl.tile_m = tpg::tiled::BM;
+        pl.tile_n = tpg::tiled::BN;
+        pl.num_tiles = mt * nt;
+        pl.grid = static_cast<int>(pl.num_tiles < h->num_sms ? pl.num_tiles : h->num_sms);
+        pl.smem = static_cast<int>(tpg::tiled::SMEM_BYTES);
+        return pl;
+    }
+    // weight-streaming variant
+    const int mt_pad = static_cast<int>((M + 15) / 16 * 16);
+    const int64_t kb = (K + tpg::stream::BK - 1) / tpg::stream::BK;
+    const int64_t nt = (N + tpg::stream::BN - 1) / tpg::stream::BN;
+    pl.tile_m = static_cast<int>(M);
+    pl.tile_n = tpg::stream::BN;
+    pl.num_tiles = nt;
+    pl.mt_pad = mt_pad;
+    // Split K across a CTA pair when one CTA per panel would leave SMs idle.
+    pl.split = (kb >= 2 && nt < 2LL * h->num_sms) ? 2 : 1;
+    pl.stages = tpg::stream::max_stages(mt_pad, pl.split);
+    pl.smem = static_cast<int>(tpg::stream::smem_bytes(mt_pad, pl.stages, pl.split));
+    if (pl.split == 2) {
+        const int clusters = stream_clusters_for(h, out_dtype == TPGEMM_OUT_F32, mt_pad, pl.stages);
+        const int64_t c = nt < clusters ? nt : clusters;
+        pl.grid = static_cast<int>(2 * c);
+        pl.cluster = 2;
+    } else {
+        pl.grid = static_cast<int>(nt < h->num_sms ? nt : h->num_sms);
+    }
+    return pl;
+}
+
+template <typename Kernel, typename... Args>
+int launch(Kernel kernel, int grid, int block, int smem, int cluster, cudaStream_t stream,
+           Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+    cfg.blockDim = dim3(static_cast<unsigned>(block), 1, 1);
+    cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    if (cluster > 1) {
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = static_cast<unsigned>(cluster);
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    }
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, args...);
+    return e == cudaSuccess ? TPGEMM_OK : TPGEMM_ERR_CUDA;
+}
+
+} // namespace
+
+extern "C" {
+
+const char *gemm_status_string(int status) {
+    switch (status) {
+    case TPGEMM_OK: return "TPGEMM_OK";
+    case TPGEMM_ERR_INVALID_ARG: return "TPGEMM_ERR_INVALID_ARG";
+    case TPGEMM_ERR_ALIGNMENT: return "TPGEMM_ERR_ALIGNMENT";
+    case TPGEMM_ERR_OVERLAP: return "TPGEMM_ERR_OVERLAP";
+    case TPGEMM_ERR_UNSUPPORTED_DEVICE: return "TPGEMM_ERR_UNSUPPORTED_DEVICE";
+    case TPGEMM_ERR_CUDA: return "TPGEMM_ERR_CUDA";
+    case TPGEMM_ERR_TIMEOUT: return "TPGEMM_ERR_TIMEOUT";
+    case TPGEMM_ERR_TOO_LARGE: return "TPGEMM_ERR_TOO_LARGE";
+    default: return "TPGEMM_ERR_UNKNOWN";
+    }
+}
+
+int gemm_create(tpgemm_handle **out, int device) {
+    if (!out) return TPGEMM_ERR_INVALID_ARG;
+    *out = nullptr;
+    int count = 0;
+    if (cudaGetDeviceCount(&count) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return TPGEMM_ERR_CUDA;
+    }
+    if (device < 0 || device >= count) return TPGEMM_ERR_INVALID_ARG;
+    cudaDeviceProp prop;
+    if (cudaGetDeviceProperties(&prop, device) != cudaSuccess) return TPGEMM_ERR_CUDA;
+    if (prop.major != 10 || prop.minor != 3) return TPGEMM_ERR_UNSUPPORTED_DEVICE;
+
+    tpgemm_handle *h = new (std::nothrow) tpgemm_handle();
+    if (!h) return TPGEMM_ERR_CUDA;
+    h->device = device;
+    h->num_sms = prop.multiProcessorCount;
+    if (const char *env = std::getenv("TPGEMM_WATCHDOG_NS")) {
+        const unsigned long long v = std::strtoull(env, nullptr, 10);
+        if (v >= 1000ull && v <= 60000000000ull) h->timeout_ns = v;
+    }
+    DeviceGuard guard(device);
+    void *fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || !fn) {
+        delete h;
+        return TPGEMM_ERR_CUDA;
+    }
+    h->encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    bool ok = true;
+    ok &= cudaFuncSetAttribute(tpg::tiled::gemm_tiled_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(tpg::tiled::SMEM_BYTES)) == cudaSuccess;
+    ok &= cudaFuncSetAttribute(tpg::tiled::gemm_tiled_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(tpg::tiled::SMEM_BYTES)) == cudaSuccess;
+    const int stream_smem = static_cast<int>(tpg::stream::SMEM_LIMIT);
+    ok &= cudaFuncSetAttribute(tpg::stream::gemm_stream_kernel<false, 1>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, stream_smem) == cudaSuccess;
+    ok &= cudaFuncSetAttribute(tpg::stream::gemm_stream_kernel<true, 1>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, stream_smem) == cudaSuccess;
+    ok &= cudaFuncSetAttribute(tpg::stream::gemm_stream_kernel<false, 2>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, stream_smem) == cudaSuccess;
+    ok &= cudaFuncSetAttribute(tpg::stream::gemm_stream_kernel<true, 2>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, stream_smem) == cudaSuccess;
+    if (!ok || cudaMalloc(&h->status, sizeof(uint64_t)) != cudaSuccess ||
+        cudaMemset(h->status, 0, sizeof(uint64_t)) != cudaSuccess) {
+        (void)cudaGetLastError();
+        if (h->status) cudaFree(h->status);
+        delete h;
+        return TPGEMM_ERR_CUDA;
+    }
+    *out = h;
+    return TPGEMM_OK;
+}
+
+int gemm_destroy(tpgemm_handle *h) {
+    if (!h) return TPGEMM_OK;
+    int rc = TPGEMM_OK;
+    {
+        DeviceGuard guard(h->device);
+        if (h->status && cudaFree(h->status) != cudaSuccess) rc = TPGEMM_ERR_CUDA;
+    }
+    delete h;
+    return rc;
+}
+
+int gemm_num_sms(tpgemm_handle *h) { return h ? h->num_sms : TPGEMM_ERR_INVALID_ARG; }
+
+int gemm_force_variant(tpgemm_handle *h, int variant) {
+    if (!h) return TPGEMM_ERR_INVALID_ARG;
+    if (variant != TPGEMM_VARIANT_AUTO && variant != TPGEMM_VARIANT_TILED && variant != TPGEMM_VARIANT_STREAM)
+        return TPGEMM_ERR_INVALID_ARG;
+    h->forced = variant;
+    return TPGEMM_OK;
+}
+
+int gemm_query_plan(tpgemm_handle *h, int64_t M, int64_t N, int64_t K, int out_dtype, int *variant,
+                    int *tile_m, int *tile_n, int64_t *num_tiles, int *grid, int *cluster, int *smem_bytes,
+                    int *launches) {
+    if (!h || M < 0 || N < 0 || K < 0) return TPGEMM_ERR_INVALID_ARG;
+    if (out_dtype != TPGEMM_OUT_BF16 && out_dtype != TPGEMM_OUT_F32) return TPGEMM_ERR_INVALID_ARG;
+    if (M > kMaxDim || N > kMaxDim || K > kMaxDim) return TPGEMM_ERR_TOO_LARGE;
+    DeviceGuard guard(h->device);
+    const Plan pl = make_plan(h, M, N, K, out_dtype);
+    if (variant) *variant = pl.variant;
+    if (tile_m) *tile_m = pl.tile_m;
+    if (tile_n) *tile_n = pl.tile_n;
+    if (num_tiles) *num_tiles = pl.num_tiles;
+    if (grid) *grid = pl.grid;
+    if (cluster) *cluster = pl.cluster;
+    if (smem_bytes) *smem_bytes = pl.smem;
+    if (launches) *launches = pl.launches;
+    return TPGEMM_OK;
+}
+
+int64_t gemm_schedule_tiles(int64_t mt, int64_t nt, int group_m, int grid, int cta, int32_t *out, int64_t cap) {
+    if (mt < 0 || nt < 0 || group_m < 1 || grid < 1 || cta < 0 || cta >= grid || cap < 0 || (cap > 0 && !out))
+        return TPGEMM_ERR_INVALID_ARG;
+    const int64_t total = mt * nt;
+    int64_t count = 0;
+    for (int64_t t = cta; t < total; t += grid, ++count) {
+        if (count < cap) {
+            const tpg::TileCoord c = tpg::tile_of_index(t, mt, nt, group_m);
+            out[2 * count] = c.m;
+            out[2 * count + 1] = c.n;
+        }
+    }
+    return count;
+}
+
+int gemm_check_args(int64_t M, int64_t N, int64_t K, const void *A, int64_t lda, const void *B, int64_t ldb,
+                    const void *C, int64_t ldc, const void *D, int64_t ldd, float beta, int out_dtype) {
+    if (out_dtype != TPGEMM_OUT_BF16 && out_dtype != TPGEMM_OUT_F32) return TPGEMM_ERR_INVALID_ARG;
+    if (M < 0 || N < 0 || K < 0) return TPGEMM_ERR_INVALID_ARG;
+    if (M > kMaxDim || N > kMaxDim || K > kMaxDim) return TPGEMM_ERR_TOO_LARGE;
+    if (M == 0 || N == 0) return TPGEMM_OK;
+    const int64_t elt = out_dtype == TPGEMM_OUT_F32 ? 4 : 2;
+    const bool use_c = beta != 0.0f;
+    // shapes and strides
+    if (!D || ldd < N) return TPGEMM_ERR_INVALID_ARG;
+    if (K > 0 && (!A || !B || lda < K || ldb < N)) return TPGEMM_ERR_INVALID_ARG;
+    if (use_c && (!C || ldc < N)) return TPGEMM_ERR_INVALID_ARG;
+    if (ldd > kMaxDim * 8 || (K > 0 && (lda > kMaxDim * 8 || ldb > kMaxDim * 8)) || (use_c && ldc > kMaxDim * 8))
+        return TPGEMM_ERR_TOO_LARGE;
+    // alignment (TMA: 16-byte base addresses and 16-byte multiple row strides)
+    if (!aligned16(D) || (M > 1 && (ldd * elt) % 16 != 0)) return TPGEMM_ERR_ALIGNMENT;
+    if (K > 0) {
+        if (!aligned16(A) || !aligned16(B)) return TPGEMM_ERR_ALIGNMENT;
+        if (M > 1 && (lda * 2) % 16 != 0) return TPGEMM_ERR_ALIGNMENT;
+        if (K > 1 && (ldb * 2) % 16 != 0) return TPGEMM_ERR_ALIGNMENT;
+    }
+    if (use_c && (!aligned16(C) || (M > 1 && (ldc * elt) % 16 != 0))) return TPGEMM_ERR_ALIGNMENT;
+    // overlap: D is written, so it may not share bytes with an input, except
+    // the exact in-place case D == C with the same row stride.
+    const Range rd = byte_range(D, M, N, ldd, elt);
+    if (K > 0 && (overlaps(rd, byte_range(A, M, K, lda, 2)) || overlaps(rd, byte_range(B, K, N, ldb, 2))))
+        return TPGEMM_ERR_OVERLAP;
+    if (use_c && !(C == D && ldc == ldd) && overlaps(rd, byte_range(C, M, N, ldc, elt)))
+        return TPGEMM_ERR_OVERLAP;
+    return TPGEMM_OK;
+}
+
+int gemm_run(tpgemm_handle *h, int64_t M, int64_t N, int64_t K, const void *A, int64_t lda, const void *B,
+             int64_t ldb, const void *C, int64_t ldc, void *D, int64_t ldd, float alpha, float beta,
+             int out_dtype, void *stream_ptr) {
+    if (!h) return TPGEMM_ERR_INVALID_ARG;
+    const int chk = gemm_check_args(M, N, K, A, lda, B, ldb, C, ldc, D, ldd, beta, out_dtype);
+    if (chk != TPGEMM_OK || M == 0 || N == 0) return chk;
+    const int64_t elt = out_dtype == TPGEMM_OUT_F32 ? 4 : 2;
+    const bool use_c = beta != 0.0f;
+
+    DeviceGuard guard(h->device);
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+    const Plan pl = make_plan(h, M, N, K, out_dtype);
+    const bool f32 = out_dtype == TPGEMM_OUT_F32;
+
+    if (pl.variant == TPGEMM_VARIANT_EPILOGUE_ONLY) {
+        const int32_t m = static_cast<int32_t>(M), n = static_cast<int32_t>(N);
+        const void *c = use_c ? C : nullptr;
+        return f32 ? launch(tpg::epilogue_only_kernel<true>, pl.grid, 256, 0, 1, stream, m, n, beta, c, ldc, D, ldd)
+                   : launch(tpg::epilogue_only_kernel<false>, pl.grid, 256, 0, 1, stream, m, n, beta, c, ldc, D,
+                            ldd);
+    }
+
+    const CUtensorMapDataType out_dt = f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    CUtensorMap tmA, tmB;
+    if (pl.variant == TPGEMM_VARIANT_TILED) {
+        CUtensorMap tmC, tmD;
+        const uint32_t chunk = f32 ? 32u : 64u;
+        // C and D maps stop at the last whole 16-byte cell of a row (see TiledParams::n_tma);
+        // with no whole cell the maps are placeholders and every column takes the plain path.
+        const int64_t cell = 16 / elt;
+        const int64_t n_tma = N / cell * cell;
+        const uint64_t map_n = static_cast<uint64_t>(n_tma > 0 ? n_tma : N);
+        if (encode_2d(h, &tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, A, K, M, tma_stride(M, K, lda, 2), 64,
+                      tpg::tiled::BM) ||
+            encode_2d(h, &tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, B, N, K, tma_stride(K, N, ldb, 2), 64, 64) ||
+            encode_2d(h, &tmD, out_dt, D, map_n, M, tma_stride(M, N, ldd, elt), chunk, tpg::tiled::BM) ||
+            encode_2d(h, &tmC, out_dt, use_c ? C : D, map_n, M,
+                      use_c ? tma_stride(M, N, ldc, elt) : tma_stride(M, N, ldd, elt), chunk, tpg::tiled::BM))
+            return TPGEMM_ERR_CUDA;
+        tpg::TiledParams p;
+        p.M = static_cast<int32_t>(M);
+        p.N = static_cast<int32_t>(N);
+        p.K = static_cast<int32_t>(K);
+        p.mt = static_cast<int32_t>((M + tpg::tiled::BM - 1) / tpg::tiled::BM);
+        p.nt = static_cast<int32_t>((N + tpg::tiled::BN - 1) / tpg::tiled::BN);
+        p.kb = static_cast<int32_t>((K + tpg::tiled::BK - 1) / tpg::tiled::BK);
+        p.group_m = kGroupM;
+        p.n_tma = static_cast<int32_t>(n_tma);
+        p.alpha = alpha;
+        p.beta = beta;
+        p.C = use_c ? C : nullptr;
+        p.ldc = ldc;
+        p.D = D;
+        p.ldd = ldd;
+        p.status = h->status;
+        p.timeout_ns = h->timeout_ns;
+        return f32 ? launch(tpg::tiled::gemm_tiled_kernel<true>, pl.grid, tpg::tiled::THREADS, pl.smem, 1, stream,
+                            tmA, tmB, tmC, tmD, p)
+                   : launch(tpg::tiled::gemm_tiled_kernel<false>, pl.grid, tpg::tiled::THREADS, pl.smem, 1, stream,
+                            tmA, tmB, tmC, tmD, p);
+    }
+
+    // weight-streaming variant
+    if (encode_2d(h, &tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, A, K, M, tma_stride(M, K, lda, 2), 64,
+                  static_cast<uint32_t>(pl.mt_pad)) ||
+        encode_2d(h, &tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, B, N, K, tma_stride(K, N, ldb, 2), 64, 64))
+        return TPGEMM_ERR_CUDA;
+    tpg::StreamParams p;
+    p.M = static_cast<int32_t>(M);
+    p.N = static_cast<int32_t>(N);
+    p.K = static_cast<int32_t>(K);
+    p.nt = static_cast<int32_t>(pl.num_tiles);
+    p.kb = static_cast<int32_t>((K + tpg::stream::BK - 1) / tpg::stream::BK);
+    p.mt_pad = pl.mt_pad;
+    p.stages = pl.stages;
+    p.alpha = alpha;
+    p.beta = beta;
+    p.C = use_c ? C : nullptr;
+    p.ldc = ldc;
+    p.D = D;
+    p.ldd = ldd;
+    p.status = h->status;
+    p.timeout_ns = h->timeout_ns;
+    if (pl.split == 2)
+        return f32 ? launch(tpg::stream::gemm_stream_kernel<true, 2>, pl.grid, tpg::stream::THREADS, pl.smem, 2,
+                            stream, tmA, tmB, p)
+                   : launch(tpg::stream::gemm_stream_kernel<false, 2>, pl.grid, tpg::stream::THREADS, pl.smem, 2,
+                            stream, tmA, tmB, p);
+    return f32 ? launch(tpg::stream::gemm_stream_kernel<true, 1>, pl.grid, tpg::stream::THREADS, pl.smem, 1, stream,
+                        tmA, tmB, p)
+               : launch(tpg::stream::gemm_stream_kernel<false, 1>, pl.grid, tpg::stream::THREADS, pl.smem, 1, stream,
+                        tmA, tmB, p);
+}
+
+int gemm_sync_status(tpgemm_handle *h, void *stream) {
+    if (!h) return TPGEMM_ERR_INVALID_ARG;
+    DeviceGuard guard(h->device);
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return TPGEMM_ERR_CUDA;
+    uint32_t word = 0;
+    if (cudaMemcpy(&word, h->status, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess) return TPGEMM_ERR_CUDA;
+    if (word != 0) {
+        if (cudaMemset(h->status, 0, sizeof(uint64_t)) != cudaSuccess) return TPGEMM_ERR_CUDA;
+        return TPGEMM_ERR_TIMEOUT;
+    }
+    return TPGEMM_OK;
+}
+
+int gemm_watchdog_selftest(tpgemm_handle *h, uint64_t timeout_ns, void *stream_ptr) {
+    if (!h || timeout_ns < 1000ull || timeout_ns > 1000000000ull) return TPGEMM_ERR_INVALID_ARG;
+    DeviceGuard guard(h->device);
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+    // Start from a clear word so the result reflects this launch only.
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return TPGEMM_ERR_CUDA;
+    if (cudaMemset(h->status, 0, sizeof(uint64_t)) != cudaSuccess) return TPGEMM_ERR_CUDA;
+    if (launch(tpg::watchdog_selftest_kernel, 1, 32, 0, 1, stream, h->status, timeout_ns) != TPGEMM_OK)
+        return TPGEMM_ERR_CUDA;
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return TPGEMM_ERR_CUDA;
+    uint32_t word = 0;
+    if (cudaMemcpy(&word, h->status, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess) return TPGEMM_ERR_CUDA;
+    if (cudaMemset(h->status, 0, sizeof(uint64_t)) != cudaSuccess) return TPGEMM_ERR_CUDA;
+    return (word & tpg::kStatusSelftest) ? TPGEMM_ERR_TIMEOUT : TPGEMM_OK;
+}
+
+} // extern "C"
