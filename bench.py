@@ -1,0 +1,479 @@
+#!/usr/bin/env python3
+"""Benchmark of the tile-partitioned dense GEMM D = alpha*A*B + beta*C on GB300.
+
+One step = one gemm_run (a single kernel launch: the whole hot path, tile
+schedule + TMA ring + tcgen05 MMA + epilogue) on one batch of synthetic input
+resident in HBM. The default workload is the square 4096^3 bf16 GEMM; the QKV
+projection, the MLP down-projection with residual and the M=16 decode shape are
+measured the same way and reported under "per_config".
+
+L2: every step reads its own copy of the inputs, drawn from rotating device
+buffer sets whose total size exceeds 3x the L2 cache, so no launch finds its
+operands already in L2 (no flush kernel runs inside the timed region).
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+Under torchrun (N > 1) every rank runs its own independent GEMM (weak scaling,
+no data-path collective); rank 0 prints one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "bf16 GEMM TFLOP/s (% of GB300 dense BF16 peak); decode-shape HBM GB/s (% peak)"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+KERNEL_NAMES = {"tiled": "tpg::tiled::gemm_tiled_kernel", "stream": "tpg::stream::gemm_stream_kernel"}
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="square")
+    ap.add_argument("--no-extra", action="store_true", help="skip the per_config measurements")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0, help="budget of the oracle sample")
+    return ap.parse_args()
+
+
+# ----------------------------------------------------------------------------- environment
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return {k: float(p[k]) for k in FALLBACK_PEAKS}, "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_source_sha() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "tile_partitioned_dense_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        if f.endswith((".cu", ".cuh")):
+            with open(os.path.join(csrc, f), "rb") as fh:
+                h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def profile_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary of this kernel on
+    this workload, or None when there is none or the kernel changed since."""
+    path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.md")
+    try:
+        text = open(path).read()
+    except OSError:
+        return None
+    sha = re.search(r"kernel_source_sha:\s*([0-9a-f]+)", text)
+    dram = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    if not sha or not dram or sha.group(1) != kernel_source_sha():
+        return None
+    return float(dram.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi samples (every 100 ms) of SM clock and throttle reasons."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.file = None
+
+    def start(self):
+        try:
+            self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.file, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.file.flush()
+        self.file.seek(0)
+        rows = [r.split(", ") for r in self.file.read().strip().splitlines() if r.strip()]
+        os.unlink(self.file.name)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            try:
+                sm.append(float(r[0]))
+                mx.append(float(r[1]))
+                for name, v in zip(names, r[4:8]):
+                    if v.strip() == "Active":
+                        reasons.add(name)
+            except (ValueError, IndexError):
+                continue
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- our arm
+
+class Workload:
+    """Device copies of one config's inputs, replicated into rotating sets."""
+
+    def __init__(self, cfg, torch, l2_bytes: int, pinned: bool):
+        from workloads import make_inputs
+        self.cfg = cfg
+        A, B, C = make_inputs(cfg)
+        self.host = {"A": A, "B": B, "C": C}
+        out = torch.float32 if cfg.out_dtype == "f32" else torch.bfloat16
+        self.out_dtype = out
+        self.out_code = 1 if out == torch.float32 else 0
+        per_set = A.numel() * 2 + B.numel() * 2 + (cfg.M * cfg.N * (4 if out == torch.float32 else 2)) * (
+            2 if C is not None else 1)
+        self.nsets = max(2, -(-3 * l2_bytes // per_set) + 1)
+        dev = torch.device("cuda")
+        self.sets = []
+        for _ in range(self.nsets):
+            s = {"A": A.to(dev), "B": B.to(dev), "C": C.to(dev) if C is not None else None,
+                 "D": torch.empty((cfg.M, cfg.N), dtype=out, device=dev)}
+            self.sets.append(s)
+        if pinned:
+            self.pin = {k: (v.pin_memory() if v is not None else None) for k, v in self.host.items()}
+            self.pin["D"] = torch.empty((cfg.M, cfg.N), dtype=out).pin_memory()
+        self.bytes_A = A.numel() * 2
+        self.bytes_B = B.numel() * 2
+        self.bytes_C = C.numel() * C.element_size() if C is not None else 0
+        self.bytes_D = cfg.M * cfg.N * (4 if out == torch.float32 else 2)
+
+    def run(self, tpd, h, i, stream):
+        s = self.sets[i % self.nsets]
+        c = self.cfg
+        C = s["C"]
+        return tpd.gemm_run(h, c.M, c.N, c.K, s["A"].data_ptr(), c.K, s["B"].data_ptr(), c.N,
+                            C.data_ptr() if C is not None else None, c.N, s["D"].data_ptr(), c.N,
+                            c.alpha, c.beta, self.out_code, stream)
+
+
+def time_launches(torch, tpd, h, wl, steps, warmup, barrier):
+    """Per-launch CUDA-event durations (ms) of `steps` back-to-back launches on
+    the current stream, bracketed by barrier + synchronize; also the bracket's
+    wall-clock time on the device (first start event to last end event)."""
+    stream = torch.cuda.current_stream()
+    sptr = stream.cuda_stream
+    for i in range(warmup):
+        assert wl.run(tpd, h, i, sptr) == 0
+    torch.cuda.synchronize()
+    barrier()
+    torch.cuda.synchronize()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    for i in range(steps):
+        starts[i].record(stream)
+        st = wl.run(tpd, h, warmup + i, sptr)
+        ends[i].record(stream)
+        if st != 0:
+            raise RuntimeError(tpd.gemm_status_string(st))
+    torch.cuda.synchronize()
+    barrier()
+    torch.cuda.synchronize()
+    per = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    span = starts[0].elapsed_time(ends[-1])
+    st = tpd.gemm_sync_status(h, None)
+    if st != 0:
+        raise RuntimeError("device status: " + tpd.gemm_status_string(st))
+    return per, span
+
+
+def time_e2e(torch, tpd, h, wl, steps):
+    """End to end through the public API: per step, copy A, B (and C) from
+    pinned host memory, run gemm_run, copy D back to pinned host memory."""
+    stream = torch.cuda.current_stream()
+    sptr = stream.cuda_stream
+    s = wl.sets[0]
+    c = wl.cfg
+
+    def step():
+        s["A"].copy_(wl.pin["A"], non_blocking=True)
+        s["B"].copy_(wl.pin["B"], non_blocking=True)
+        if s["C"] is not None:
+            s["C"].copy_(wl.pin["C"], non_blocking=True)
+        st = wl.run(tpd, h, 0, sptr)
+        if st != 0:
+            raise RuntimeError(tpd.gemm_status_string(st))
+        wl.pin["D"].copy_(s["D"], non_blocking=True)
+
+    for _ in range(2):
+        step()
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(steps):
+        step()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    ms = t0.elapsed_time(t1) / steps
+    return ms, wl.bytes_A + wl.bytes_B + wl.bytes_C, wl.bytes_D
+
+
+def roofline_entry(cfg, kernel, avg_ms, peaks, peak_src):
+    if cfg.name == "decode":
+        b_bytes = cfg.K * cfg.N * 2
+        achieved = b_bytes / (avg_ms * 1e-3) / 1e9
+        peak = peaks["hbm_gbs"]
+        unit, bound = "GB/s", "hbm"
+    else:
+        achieved = cfg.flops / (avg_ms * 1e-3) / 1e12
+        peak = peaks["bf16_tflops"]
+        unit, bound = "TFLOP/s", "tensor"
+    return {"bound": bound, "achieved": round(achieved, 2), "peak": peak, "unit": unit,
+            "frac": round(achieved / peak, 4), "peak_source": f"{peak_src} (MEASURED_PEAKS.json burst)"
+            if peak_src == "measured" else "fallback", "traffic": profile_traffic(kernel, cfg.name),
+            "kernel": KERNEL_NAMES[kernel]}
+
+
+def config_entry(cfg, wl, nsets):
+    return {"workload": f"{cfg.name}: {cfg.description}", "M": cfg.M, "N": cfg.N, "K": cfg.K,
+            "alpha": cfg.alpha, "beta": cfg.beta, "out_dtype": cfg.out_dtype,
+            "l2": f"inputs larger than L2: {nsets} rotating device copies of A,B(,C),D",
+            "parallelism": "replicas (independent GEMM per GPU)"}
+
+
+def cpu_baseline(cfg, budget_s):
+    """The oracle as it stands, on a bounded row sample of the same workload."""
+    import oracle
+    from workloads import make_inputs, sample_rows
+    A, B, C = make_inputs(cfg)
+    threads = len(os.sched_getaffinity(0))
+    probe = sample_rows(cfg.M, max(1, min(cfg.M, threads)), seed=7)
+    t0 = time.perf_counter()
+    oracle.gemm_rows(A, B, C, cfg.alpha, cfg.beta, 1 if cfg.out_dtype == "f32" else 0, rows=probe,
+                     nthreads=threads)
+    per_row = (time.perf_counter() - t0) / len(probe)
+    nrows = int(max(len(probe), min(cfg.M, budget_s / max(per_row, 1e-9))))
+    rows = sample_rows(cfg.M, nrows, seed=11)
+    t0 = time.perf_counter()
+    oracle.gemm_rows(A, B, C, cfg.alpha, cfg.beta, 1 if cfg.out_dtype == "f32" else 0, rows=rows,
+                     nthreads=threads)
+    dt = time.perf_counter() - t0
+    flops = 2.0 * len(rows) * cfg.N * cfg.K
+    if cfg.name == "decode":
+        value, unit = len(rows) / cfg.M * cfg.K * cfg.N * 2 / dt / 1e9, "GB/s"
+    else:
+        value, unit = flops / dt / 1e12, "TFLOP/s"
+    return {"value": value, "unit": unit, "cores": threads, "kind": "oracle",
+            "sample": f"{len(rows)} of {cfg.M} rows of {cfg.name} (all N columns, full K), "
+                      f"{dt:.1f} s, fp64 C oracle, {threads} threads"}
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+    import tile_partitioned_dense_gb300 as tpd
+    from workloads import CONFIGS
+
+    world, rank, local = dist_env()
+    if world != args.gpus:
+        if world > 1 or args.gpus > 1:
+            raise SystemExit(f"--gpus {args.gpus} but WORLD_SIZE={world}; launch N>1 with torchrun")
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    peaks, peak_src = load_peaks()
+    props = torch.cuda.get_device_properties(local)
+    l2 = int(getattr(props, "L2_cache_size", 0) or 129 * 2 ** 20)
+    h = tpd.gemm_create(local)
+
+    cfg = CONFIGS[args.workload]
+    wl = Workload(cfg, torch, l2, pinned=not args.no_e2e)
+    plan = tpd.gemm_query_plan(h, cfg.M, cfg.N, cfg.K, wl.out_code)
+    kernel = "stream" if plan["variant"] == tpd.VARIANT_STREAM else "tiled"
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    per, span = time_launches(torch, tpd, h, wl, args.steps, args.warmup, barrier)
+    clocks = sampler.stop()
+
+    total_ms = sum(per)
+    avg_ms = total_ms / len(per)
+    # max over ranks of the timed-region time
+    t = torch.tensor([span, avg_ms], dtype=torch.float64, device="cuda")
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    span_max, avg_max = float(t[0]), float(t[1])
+    if cfg.name == "decode":
+        unit = "GB/s"
+        value = world * args.steps * cfg.K * cfg.N * 2 / (span_max * 1e-3) / 1e9
+    else:
+        unit = "TFLOP/s"
+        value = world * args.steps * cfg.flops / (span_max * 1e-3) / 1e12
+
+    e2e = None
+    if not args.no_e2e:
+        e2e_steps = max(3, min(args.steps, 20))
+        ms, bi, bo = time_e2e(torch, tpd, h, wl, e2e_steps)
+        tt = torch.tensor([ms], dtype=torch.float64, device="cuda")
+        if world > 1:
+            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms = float(tt[0])
+        ev = (world * cfg.K * cfg.N * 2 / (ms * 1e-3) / 1e9) if cfg.name == "decode" else \
+            (world * cfg.flops / (ms * 1e-3) / 1e12)
+        e2e = {"value": round(ev, 3), "unit": unit, "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo,
+               "ms_per_step": round(ms, 4), "steps": e2e_steps,
+               "path": "pinned host -> device copies, gemm_run (C ABI), device -> pinned host copy"}
+
+    per_config = {}
+    launches = args.steps
+    if not args.no_extra:
+        for name in ["qkv", "mlp_down", "decode", "square"]:
+            if name == cfg.name:
+                continue
+            c2 = CONFIGS[name]
+            w2 = Workload(c2, torch, l2, pinned=False)
+            p2 = tpd.gemm_query_plan(h, c2.M, c2.N, c2.K, w2.out_code)
+            k2 = "stream" if p2["variant"] == tpd.VARIANT_STREAM else "tiled"
+            steps2 = max(20, min(400, int(0.4 / (c2.flops / 1.5e15 if name != "decode" else 40e-6))))
+            per2, span2 = time_launches(torch, tpd, h, w2, steps2, 10, barrier)
+            avg2 = sum(per2) / len(per2)
+            if name == "decode":
+                v2 = c2.K * c2.N * 2 / (span2 / steps2 * 1e-3) / 1e9
+                u2 = "GB/s"
+            else:
+                v2 = c2.flops / (span2 / steps2 * 1e-3) / 1e12
+                u2 = "TFLOP/s"
+            per_config[name] = {"value": round(v2, 2), "unit": u2, "ms_per_step": round(span2 / steps2, 5),
+                                "steps": steps2, "roofline": roofline_entry(c2, k2, avg2, peaks, peak_src),
+                                "config": config_entry(c2, w2, w2.nsets), "plan": p2}
+            launches += steps2
+            del w2
+            torch.cuda.empty_cache()
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(cfg, args.cpu_seconds)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC,
+            "value": round(value, 3),
+            "unit": unit,
+            "n_gpus": world,
+            "steps": args.steps,
+            "warmup": args.warmup,
+            "ms_per_step": round(span_max / args.steps, 5),
+            "higher_is_better": True,
+            "scaling": "weak",
+            "vs_baseline": None,
+            "dtype": "bf16",
+            "data": "synthetic (seeded: A,B ~ N(0,1) for square; see workloads.py)",
+            "config": config_entry(cfg, wl, wl.nsets),
+            "impl": "ours",
+            "roofline": roofline_entry(cfg, kernel, avg_max, peaks, peak_src),
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": launches,
+            "clocks": clocks,
+            "plan": plan,
+            "kernel_avg_ms": round(avg_max, 5),
+            "per_config": per_config,
+        }
+        print(json.dumps(line), flush=True)
+    tpd.gemm_destroy(h)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+# ----------------------------------------------------------------------------- reference arm
+
+def run_reference(args):
+    """The oracle (the plain fp64 CPU definition) timed as the reference arm:
+    each step computes a bounded row sample of the same workload."""
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    from workloads import CONFIGS, make_inputs, sample_rows
+    cfg = CONFIGS[args.workload]
+    A, B, C = make_inputs(cfg)
+    threads = len(os.sched_getaffinity(0))
+    out = 1 if cfg.out_dtype == "f32" else 0
+    probe = sample_rows(cfg.M, max(1, min(cfg.M, threads)), seed=7)
+    t0 = time.perf_counter()
+    oracle.gemm_rows(A, B, C, cfg.alpha, cfg.beta, out, rows=probe, nthreads=threads)
+    per_row = (time.perf_counter() - t0) / len(probe)
+    # keep the whole --steps K --warmup W run within about two minutes
+    per_step_s = max(0.2, min(3.0, 120.0 / max(1, args.steps + args.warmup)))
+    nrows = int(max(1, min(cfg.M, per_step_s / max(per_row, 1e-9))))
+    times = []
+    for i in range(args.warmup + args.steps):
+        rows = sample_rows(cfg.M, nrows, seed=100 + i)
+        t0 = time.perf_counter()
+        oracle.gemm_rows(A, B, C, cfg.alpha, cfg.beta, out, rows=rows, nthreads=threads)
+        if i >= args.warmup:
+            times.append(time.perf_counter() - t0)
+    ms = 1e3 * sum(times) / len(times)
+    if cfg.name == "decode":
+        value, unit = nrows / cfg.M * cfg.K * cfg.N * 2 / (ms * 1e-3) / 1e9, "GB/s"
+    else:
+        value, unit = 2.0 * nrows * cfg.N * cfg.K / (ms * 1e-3) / 1e12, "TFLOP/s"
+    sample = (f"{nrows} of {cfg.M} rows of {cfg.name} per step (all N columns, full K), "
+              f"fp64 C oracle, {threads} threads")
+    line = {"metric": METRIC, "value": value, "unit": unit, "n_gpus": args.gpus, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(ms, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded, workloads.py)",
+            "config": {"workload": f"{cfg.name}: {cfg.description}", "M": cfg.M, "N": cfg.N, "K": cfg.K},
+            "impl": "reference",
+            "cpu_baseline": {"value": value, "unit": unit, "cores": threads, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()
