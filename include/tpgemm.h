@@ -172,6 +172,43 @@ int gemm_watchdog_selftest(tpgemm_handle *h, uint64_t timeout_ns, void *stream);
 /* Number of SMs the handle schedules over, or a negative status. */
 int gemm_num_sms(tpgemm_handle *h);
 
+/*
+ * Allocation-free GEMM (no counterpart in the paper; it serves callers that
+ * cannot allocate device memory). Some callers cannot call cudaMalloc: code
+ * whose device memory must all come from a pool or arena owned by an outer
+ * framework, and serving loops that forbid allocation after warm-up, where an
+ * allocation can stall on the driver, fragment the pool or break a stream
+ * capture in progress. gemm_create allocates (the handle's status word), so
+ * such callers use this entry point instead. It needs no handle and runs on the
+ * current device.
+ *
+ * Computes the same D = alpha*A*B + beta*C as gemm_run, with the same
+ * arguments, layouts, alignment, aliasing and error rules, always with the
+ * tiled kernel (K == 0 runs the D = beta*C kernel). The kernel's scratch, its
+ * 4-byte status word, lives in a file-scope device array of 16 bytes (the
+ * stated maximum) that every GPU that loads this library holds until the
+ * process exits; the scratch needed does not grow with M, N or K, and sizes
+ * beyond the library's limit (any dimension above 2^31 - 1) are rejected with
+ * TPGEMM_ERR_TOO_LARGE. The caller still passes and owns A, B, C and D.
+ * Nothing here calls cudaMalloc, cudaFree or any allocating library routine.
+ *
+ * The first call on a device does that device's one-time set-up (it looks up
+ * the array's device address, resolves the tensor-map encoder, sets the
+ * kernel's shared-memory limit and clears the array, synchronously); make
+ * that first call before any stream capture. Every call shares the array and
+ * it keeps the last call's contents: each call clears the status word on
+ * `stream` before its launch, so calls that overlap on the GPU (on different
+ * streams) race on it.
+ *
+ * check_status == 0: enqueue and return (launch errors only).
+ * check_status != 0: also synchronise `stream`, read and clear the status
+ * word, and return TPGEMM_ERR_TIMEOUT if a pipeline wait ran out.
+ */
+int gemm_run_noalloc(int64_t M, int64_t N, int64_t K, const void *A, int64_t lda,
+                     const void *B, int64_t ldb, const void *C, int64_t ldc, void *D,
+                     int64_t ldd, float alpha, float beta, int out_dtype, void *stream,
+                     int check_status);
+
 #ifdef __cplusplus
 }
 #endif

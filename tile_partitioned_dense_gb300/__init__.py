@@ -62,6 +62,8 @@ def load_library() -> ctypes.CDLL:
             "gemm_schedule_tiles": (i64, [i64, i64, i32, i32, i32, ctypes.POINTER(ctypes.c_int32), i64]),
             "gemm_watchdog_selftest": (i32, [vp, ctypes.c_uint64, vp]),
             "gemm_num_sms": (i32, [vp]),
+            "gemm_run_noalloc": (i32, [i64, i64, i64, vp, i64, vp, i64, vp, i64, vp, i64, f32, f32, i32, vp,
+                                       i32]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -135,6 +137,14 @@ def gemm_watchdog_selftest(h, timeout_ns: int, stream=None) -> int:
 
 def gemm_num_sms(h) -> int:
     return load_library().gemm_num_sms(h)
+
+
+def gemm_run_noalloc(M, N, K, A, lda, B, ldb, C, ldc, D, ldd, alpha, beta, out_dtype, stream,
+                     check_status=0) -> int:
+    """gemm_run without a handle and without any device allocation, for callers
+    that cannot call cudaMalloc (see include/tpgemm.h)."""
+    return load_library().gemm_run_noalloc(M, N, K, A, lda, B, ldb, C, ldc, D, ldd, alpha, beta,
+                                           out_dtype, stream, int(check_status))
 
 
 # ------------------------------------------------------------------ torch convenience

@@ -9,6 +9,7 @@
 #include <cstdint>
 #include <cstdlib>
 #include <cstring>
+#include <mutex>
 #include <new>
 
 #include "tpgemm.h"
@@ -477,3 +478,167 @@ int gemm_watchdog_selftest(tpgemm_handle *h, uint64_t timeout_ns, void *stream_p
 }
 
 } // extern "C"
+
+// ---------------------------------------------------------------------------
+// Allocation-free entry point (gemm_run_noalloc).
+//
+// Some callers cannot call cudaMalloc: code that runs while a memory pool or
+// arena owned by an outer framework is the only legal source of device memory,
+// serving loops that forbid allocation after warm-up (an allocation there can
+// stall on the driver, fragment the pool or break a stream capture in
+// progress), and callers that have no place to keep a handle. gemm_create
+// allocates the handle's status word with cudaMalloc, so those callers use this
+// entry point instead: it runs the tiled GEMM kernel with its scratch (the
+// 4-byte status word the kernel's bounded waits report into) taken from the
+// file-scope array below, which every GPU that loads this library holds until
+// the process exits.
+namespace {
+
+constexpr int kNoallocStatusWords = 4;   // maximum scratch: 16 bytes
+constexpr int kNoallocMaxDevices = 64;
+static __device__ __align__(256) uint32_t g_noalloc_scratch[kNoallocStatusWords];
+
+struct NoallocDevice {
+    bool ready = false;
+    uint32_t *status = nullptr; // device address of g_noalloc_scratch on this device
+    int num_sms = 0;
+    PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+};
+NoallocDevice g_noalloc_dev[kNoallocMaxDevices];
+std::mutex g_noalloc_mutex;
+
+// One-time set-up for the current device (which must be the device the
+// pointers live on). In host code the array's name is only a host-side stand-in,
+// so its device address is looked up here, with this device current, and passed
+// to the kernel as a pointer.
+int noalloc_setup(int dev, NoallocDevice **out) {
+    if (dev < 0 || dev >= kNoallocMaxDevices) return TPGEMM_ERR_INVALID_ARG;
+    std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+    NoallocDevice &d = g_noalloc_dev[dev];
+    if (!d.ready) {
+        cudaDeviceProp prop;
+        if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess) return TPGEMM_ERR_CUDA;
+        if (prop.major != 10 || prop.minor != 3) return TPGEMM_ERR_UNSUPPORTED_DEVICE;
+        void *ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || !ptr) {
+            (void)cudaGetLastError();
+            return TPGEMM_ERR_CUDA;
+        }
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess || !fn)
+            return TPGEMM_ERR_CUDA;
+        if (cudaFuncSetAttribute(tpg::tiled::gemm_tiled_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(tpg::tiled::SMEM_BYTES)) != cudaSuccess ||
+            cudaFuncSetAttribute(tpg::tiled::gemm_tiled_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(tpg::tiled::SMEM_BYTES)) != cudaSuccess ||
+            cudaMemset(ptr, 0, sizeof(uint32_t) * kNoallocStatusWords) != cudaSuccess) {
+            (void)cudaGetLastError();
+            return TPGEMM_ERR_CUDA;
+        }
+        d.status = static_cast<uint32_t *>(ptr);
+        d.num_sms = prop.multiProcessorCount;
+        d.encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+        d.ready = true;
+    }
+    *out = &d;
+    return TPGEMM_OK;
+}
+
+int noalloc_encode(PFN_cuTensorMapEncodeTiled_v12000 encode, CUtensorMap *map, CUtensorMapDataType dt,
+                   const void *ptr, uint64_t inner, uint64_t outer, uint64_t stride_bytes, uint32_t box_inner,
+                   uint32_t box_outer) {
+    cuuint64_t dims[2] = {inner, outer};
+    cuuint64_t strides[1] = {stride_bytes};
+    cuuint32_t box[2] = {box_inner, box_outer};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = encode(map, dt, 2, const_cast<void *>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? TPGEMM_OK : TPGEMM_ERR_CUDA;
+}
+
+} // namespace
+
+extern "C" int gemm_run_noalloc(int64_t M, int64_t N, int64_t K, const void *A, int64_t lda, const void *B,
+                                int64_t ldb, const void *C, int64_t ldc, void *D, int64_t ldd, float alpha,
+                                float beta, int out_dtype, void *stream_ptr, int check_status) {
+    const int chk = gemm_check_args(M, N, K, A, lda, B, ldb, C, ldc, D, ldd, beta, out_dtype);
+    if (chk != TPGEMM_OK || M == 0 || N == 0) return chk;
+    // The scratch this kernel needs is one status word whatever M, N and K are,
+    // so the 16-byte array serves every size gemm_check_args accepts.
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) return TPGEMM_ERR_CUDA;
+    NoallocDevice *nd = nullptr;
+    const int st = noalloc_setup(dev, &nd);
+    if (st != TPGEMM_OK) return st;
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+    const bool f32 = out_dtype == TPGEMM_OUT_F32;
+    const int64_t elt = f32 ? 4 : 2;
+    const bool use_c = beta != 0.0f;
+    int rc;
+    if (K == 0) {
+        // D = beta*C: no pipeline, no scratch
+        int64_t blocks = (M * N + 1023) / 1024;
+        if (blocks > 8LL * nd->num_sms) blocks = 8LL * nd->num_sms;
+        const int32_t m = static_cast<int32_t>(M), n = static_cast<int32_t>(N);
+        const void *c = use_c ? C : nullptr;
+        rc = f32 ? launch(tpg::epilogue_only_kernel<true>, static_cast<int>(blocks), 256, 0, 1, stream, m, n, beta, c,
+                          ldc, D, ldd)
+                 : launch(tpg::epilogue_only_kernel<false>, static_cast<int>(blocks), 256, 0, 1, stream, m, n, beta,
+                          c, ldc, D, ldd);
+    } else {
+        // The status word must start at zero: every call shares it.
+        if (cudaMemsetAsync(nd->status, 0, sizeof(uint32_t), stream) != cudaSuccess) return TPGEMM_ERR_CUDA;
+        const CUtensorMapDataType out_dt = f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+        const uint32_t chunk = f32 ? 32u : 64u;
+        const int64_t cell = 16 / elt;
+        const int64_t n_tma = N / cell * cell;
+        const uint64_t map_n = static_cast<uint64_t>(n_tma > 0 ? n_tma : N);
+        CUtensorMap tmA, tmB, tmC, tmD;
+        if (noalloc_encode(nd->encode, &tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, A, K, M, tma_stride(M, K, lda, 2), 64,
+                           tpg::tiled::BM) ||
+            noalloc_encode(nd->encode, &tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, B, N, K, tma_stride(K, N, ldb, 2), 64,
+                           64) ||
+            noalloc_encode(nd->encode, &tmD, out_dt, D, map_n, M, tma_stride(M, N, ldd, elt), chunk,
+                           tpg::tiled::BM) ||
+            noalloc_encode(nd->encode, &tmC, out_dt, use_c ? C : D, map_n, M,
+                           use_c ? tma_stride(M, N, ldc, elt) : tma_stride(M, N, ldd, elt), chunk, tpg::tiled::BM))
+            return TPGEMM_ERR_CUDA;
+        tpg::TiledParams p;
+        p.M = static_cast<int32_t>(M);
+        p.N = static_cast<int32_t>(N);
+        p.K = static_cast<int32_t>(K);
+        p.mt = static_cast<int32_t>((M + tpg::tiled::BM - 1) / tpg::tiled::BM);
+        p.nt = static_cast<int32_t>((N + tpg::tiled::BN - 1) / tpg::tiled::BN);
+        p.kb = static_cast<int32_t>((K + tpg::tiled::BK - 1) / tpg::tiled::BK);
+        p.group_m = kGroupM;
+        p.n_tma = static_cast<int32_t>(n_tma);
+        p.alpha = alpha;
+        p.beta = beta;
+        p.C = use_c ? C : nullptr;
+        p.ldc = ldc;
+        p.D = D;
+        p.ldd = ldd;
+        p.status = nd->status;
+        p.timeout_ns = 2000000000ull;
+        const int64_t tiles = static_cast<int64_t>(p.mt) * p.nt;
+        const int grid = static_cast<int>(tiles < nd->num_sms ? tiles : nd->num_sms);
+        const int smem = static_cast<int>(tpg::tiled::SMEM_BYTES);
+        rc = f32 ? launch(tpg::tiled::gemm_tiled_kernel<true>, grid, tpg::tiled::THREADS, smem, 1, stream, tmA, tmB,
+                          tmC, tmD, p)
+                 : launch(tpg::tiled::gemm_tiled_kernel<false>, grid, tpg::tiled::THREADS, smem, 1, stream, tmA, tmB,
+                          tmC, tmD, p);
+    }
+    if (rc != TPGEMM_OK || !check_status) return rc;
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return TPGEMM_ERR_CUDA;
+    uint32_t word = 0;
+    if (cudaMemcpy(&word, nd->status, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess) return TPGEMM_ERR_CUDA;
+    if (word != 0) {
+        if (cudaMemset(nd->status, 0, sizeof(uint32_t)) != cudaSuccess) return TPGEMM_ERR_CUDA;
+        return TPGEMM_ERR_TIMEOUT;
+    }
+    return TPGEMM_OK;
+}
