@@ -69,10 +69,11 @@ enum tpgemm_status {
 
 /* Kernel variants, for gemm_force_variant and gemm_query_plan. */
 enum tpgemm_variant {
-    TPGEMM_VARIANT_AUTO = 0,   /* M <= 64: weight-streaming; otherwise tiled */
-    TPGEMM_VARIANT_TILED = 1,  /* persistent warp-specialised tcgen05 kernel, 128x256 tiles */
+    TPGEMM_VARIANT_AUTO = 0,   /* M <= 64: streaming; M <= 128: tiled; otherwise tiled pair */
+    TPGEMM_VARIANT_TILED = 1,  /* persistent warp-specialised tcgen05 kernel, 128x256 tiles per CTA */
     TPGEMM_VARIANT_STREAM = 2, /* small-M weight-streaming kernel (swapped operands) */
-    TPGEMM_VARIANT_EPILOGUE_ONLY = 3 /* K == 0: D = beta * C */
+    TPGEMM_VARIANT_EPILOGUE_ONLY = 3, /* K == 0: D = beta * C */
+    TPGEMM_VARIANT_TILED_PAIR = 4 /* the tiled kernel on CTA pairs: 256x256 tiles, cta_group::2 MMA */
 };
 
 /*
@@ -133,9 +134,10 @@ const char *gemm_status_string(int status);
 
 /*
  * Forces a kernel variant for later gemm_run calls on this handle
- * (TPGEMM_VARIANT_AUTO restores the default choice). TILED and STREAM are
- * accepted for any K >= 1; STREAM additionally requires M <= 64. Not
- * thread-safe with concurrent gemm_run calls on the same handle.
+ * (TPGEMM_VARIANT_AUTO restores the default choice). TILED, TILED_PAIR and
+ * STREAM are accepted for any K >= 1; STREAM is used only when M <= 64 (larger
+ * M falls back to TILED). Not thread-safe with concurrent gemm_run calls on
+ * the same handle.
  */
 int gemm_force_variant(tpgemm_handle *h, int variant);
 
@@ -150,15 +152,17 @@ int gemm_query_plan(tpgemm_handle *h, int64_t M, int64_t N, int64_t K, int out_d
                     int *cluster, int *smem_bytes, int *launches);
 
 /*
- * Host copy of the persistent tile scheduler: for a grid of `grid` CTAs over
- * an mt x nt grid of output tiles with grouped raster `group_m`, writes the
- * (m_tile, n_tile) pair of the i-th tile visited by CTA `cta` into
- * out[2*i], out[2*i+1] for i < cap, and returns the number of tiles that CTA
- * owns (or a negative status). The kernels run the same function, so this is
- * what the partition tests check. No GPU is needed.
+ * Host copy of the persistent tile scheduler. For an mt x nt grid of output
+ * tiles (256 columns wide; rows of 128, or 256 for CTA pairs) walked by
+ * `workers` persistent workers with grouped raster `group_m`, writes the work
+ * items of worker `worker`, in order, as triples out[3*i .. 3*i+2] = (tile
+ * row, first column, width in columns) for i < cap, and returns how many items
+ * that worker owns (or a negative status). With allow_split != 0, a last round
+ * that is at most half full is cut into 128-column halves. The kernels run the
+ * same functions, so this is what the partition tests check. No GPU is needed.
  */
-int64_t gemm_schedule_tiles(int64_t mt, int64_t nt, int group_m, int grid, int cta, int32_t *out,
-                            int64_t cap);
+int64_t gemm_schedule_tiles(int64_t mt, int64_t nt, int group_m, int workers, int allow_split,
+                            int worker, int32_t *out, int64_t cap);
 
 /*
  * Watchdog self-test: launches one CTA that waits on a barrier no thread will

@@ -155,36 +155,61 @@ def _tile_grid(M, N, bm=128, bn=256):
     return (M + bm - 1) // bm, (N + bn - 1) // bn
 
 
-@pytest.mark.parametrize("mt,nt", [_tile_grid(256, 256), _tile_grid(4096, 4096), _tile_grid(8192, 6144),
-                                   _tile_grid(8192, 4096), (1, 1), (3, 7), (17, 5), (64, 1), (1, 224)])
-@pytest.mark.parametrize("grid", [1, 7, 148, 152, 160, 1000])
+GRIDS = [_tile_grid(256, 256), _tile_grid(4096, 4096), _tile_grid(8192, 6144), _tile_grid(8192, 4096),
+         _tile_grid(4096, 4096, bm=256), _tile_grid(8192, 6144, bm=256), _tile_grid(8192, 4096, bm=256),
+         (1, 1), (3, 7), (17, 5), (64, 1), (1, 224), (20, 8), (10, 8)]
+
+
+@pytest.mark.parametrize("mt,nt", GRIDS)
+@pytest.mark.parametrize("workers", [1, 7, 74, 76, 148, 152, 160, 1000])
 @pytest.mark.parametrize("group_m", [1, 8, 16])
-def test_schedule_is_an_exact_partition(mt, nt, grid, group_m):
-    grid = min(grid, mt * nt) if mt * nt else 1
-    seen = {}
-    for cta in range(grid):
-        tiles = tpd.gemm_schedule_tiles(mt, nt, group_m, grid, cta)
-        for (m, n) in tiles:
-            assert 0 <= m < mt and 0 <= n < nt
-            assert (m, n) not in seen, f"tile {(m, n)} owned by CTAs {seen[(m, n)]} and {cta}"
-            seen[(m, n)] = cta
-        # balanced: every CTA owns floor or ceil of tiles/grid
-        assert len(tiles) in (mt * nt // grid, -(-mt * nt // grid))
-    assert len(seen) == mt * nt
+@pytest.mark.parametrize("split", [False, True])
+def test_schedule_is_an_exact_partition(mt, nt, workers, group_m, split):
+    """Every output column of every tile row is owned by exactly one worker."""
+    workers = min(workers, mt * nt) if mt * nt else 1
+    owner = {}
+    loads = []
+    for w in range(workers):
+        items = tpd.gemm_schedule_tiles(mt, nt, group_m, workers, w, allow_split=split)
+        load = 0
+        for (m, n0, width) in items:
+            assert 0 <= m < mt and 0 <= n0 and n0 + width <= nt * 256
+            assert width in (256, 128) and n0 % width == 0
+            for c in range(n0 // 128, (n0 + width) // 128):  # 128-column granules
+                assert (m, c) not in owner, f"columns {c * 128}.. of tile row {m} owned twice"
+                owner[(m, c)] = w
+            load += width
+        loads.append(load)
+    assert len(owner) == mt * nt * 2
+    # balance: no worker does more than one whole tile beyond the average share
+    assert max(loads) - min(loads) <= 256
+
+
+def test_schedule_tail_split_balances_square():
+    # square 4096^3 in pair mode: 16 x 16 tiles of 256 x 256 on 76 pairs = 3 whole
+    # rounds + 28 tiles, which are cut into 56 halves: nobody does a 4th whole tile.
+    loads = []
+    for w in range(76):
+        items = tpd.gemm_schedule_tiles(16, 16, 8, 76, w)
+        loads.append(sum(width for (_, _, width) in items))
+    assert max(loads) == 3 * 256 + 128 and min(loads) == 3 * 256
+    # without the split the busiest workers own four whole tiles
+    loads = [sum(x[2] for x in tpd.gemm_schedule_tiles(16, 16, 8, 76, w, allow_split=False)) for w in range(76)]
+    assert max(loads) == 4 * 256
 
 
 def test_schedule_grouped_raster_order():
     # the first tiles of a band walk down the band before moving right
-    order = [tpd.gemm_schedule_tiles(40, 8, 16, 1, 0)[i] for i in range(20)]
-    assert order[:16] == [(m, 0) for m in range(16)]
-    assert order[16:20] == [(m, 1) for m in range(4)]
+    order = tpd.gemm_schedule_tiles(40, 8, 16, 1, 0)
+    assert [(m, n) for (m, n, _) in order[:16]] == [(m, 0) for m in range(16)]
+    assert [(m, n) for (m, n, _) in order[16:20]] == [(m, 256) for m in range(4)]
     # the last band has 40 - 32 = 8 rows
-    tail = tpd.gemm_schedule_tiles(40, 8, 16, 1, 0)[32 * 8:32 * 8 + 9]
-    assert tail[:8] == [(32 + m, 0) for m in range(8)] and tail[8] == (32, 1)
+    tail = order[32 * 8:32 * 8 + 9]
+    assert [(m, n) for (m, n, _) in tail[:8]] == [(32 + m, 0) for m in range(8)] and tail[8][:2] == (32, 256)
 
 
 def test_schedule_rejects_bad_arguments():
     lib = tpd.load_library()
-    assert lib.gemm_schedule_tiles(4, 4, 0, 1, 0, None, 0) == tpd.ERR_INVALID_ARG
-    assert lib.gemm_schedule_tiles(4, 4, 8, 2, 2, None, 0) == tpd.ERR_INVALID_ARG
-    assert lib.gemm_schedule_tiles(4, 4, 8, 2, 0, None, 3) == tpd.ERR_INVALID_ARG
+    assert lib.gemm_schedule_tiles(4, 4, 0, 1, 1, 0, None, 0) == tpd.ERR_INVALID_ARG
+    assert lib.gemm_schedule_tiles(4, 4, 8, 2, 1, 2, None, 0) == tpd.ERR_INVALID_ARG
+    assert lib.gemm_schedule_tiles(4, 4, 8, 2, 1, 0, None, 3) == tpd.ERR_INVALID_ARG

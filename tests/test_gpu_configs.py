@@ -82,12 +82,15 @@ def test_config_random_within_tolerance(h, name):
 def test_plans_match_the_design(h):
     sms = tpd.gemm_num_sms(h)
     p = tpd.gemm_query_plan(h, 4096, 4096, 4096, tpd.OUT_BF16)
-    assert p["variant"] == tpd.VARIANT_TILED and p["tile_m"] == 128 and p["tile_n"] == 256
-    assert p["num_tiles"] == 32 * 16 and p["grid"] == min(512, sms) and p["launches"] == 1
+    assert p["variant"] == tpd.VARIANT_TILED_PAIR and p["tile_m"] == 256 and p["tile_n"] == 256
+    assert p["num_tiles"] == 16 * 16 and p["cluster"] == 2 and p["launches"] == 1
+    assert p["grid"] % 2 == 0 and sms - 8 <= p["grid"] <= sms
     p = tpd.gemm_query_plan(h, 16, 28672, 4096, tpd.OUT_BF16)
     assert p["variant"] == tpd.VARIANT_STREAM and p["num_tiles"] == 224 and p["cluster"] == 2
     assert p["grid"] % 2 == 0 and p["grid"] <= sms
     p = tpd.gemm_query_plan(h, 256, 256, 256, tpd.OUT_F32)
-    assert p["variant"] == tpd.VARIANT_TILED and p["grid"] == 2
+    assert p["variant"] == tpd.VARIANT_TILED_PAIR and p["grid"] == 2
+    p = tpd.gemm_query_plan(h, 100, 256, 256, tpd.OUT_F32)
+    assert p["variant"] == tpd.VARIANT_TILED and p["grid"] == 1
     p = tpd.gemm_query_plan(h, 5, 5, 0, tpd.OUT_F32)
     assert p["variant"] == tpd.VARIANT_EPILOGUE_ONLY

@@ -143,3 +143,24 @@ def test_in_place_d_equals_c(h, out_dtype, M):
     Cd = to_device(C)
     D, _ = run(h, A, B, Cd, 1.0, 1.0, out_dtype, D=Cd)
     assert_bit_exact(bits(Cd), want, "in place")
+
+
+@pytest.mark.parametrize("shape", [(2560, 2048, 64), (2560, 1800, 72), (300, 520, 256)],
+                         ids=lambda s: "x".join(map(str, s)))
+@pytest.mark.parametrize("variant", [tpd.VARIANT_TILED, tpd.VARIANT_TILED_PAIR], ids=["tiled", "pair"])
+@pytest.mark.parametrize("out_dtype", [torch.bfloat16, torch.float32], ids=["bf16", "f32"])
+def test_tiled_modes_with_tail_split(h, shape, variant, out_dtype):
+    """Both tiled modes on shapes whose last round is cut into 128-column
+    halves (2560 x 2048: 160 tiles on 152 CTAs, 80 pair tiles on 76 pairs);
+    with N = 1800 one half lies entirely right of N."""
+    M, N, K = shape
+    A, B, C = _inputs(M, N, K, seed=M + N, integer=True, with_c=True, c_dtype=out_dtype)
+    _variant(h, variant)
+    try:
+        D, base = run(h, A, B, C, 1.0, 1.0, out_dtype, ldd=round8(N) + 8)
+    finally:
+        _variant(h, tpd.VARIANT_AUTO)
+    assert_bit_exact(bits(D), oracle_out(A, B, C, 1.0, 1.0, out_dtype), f"{shape} variant {variant}")
+    b = bits(base).view(np.uint16 if out_dtype == torch.bfloat16 else np.uint32)
+    s = bits(alloc_out(M, N, out_dtype, ldd=round8(N) + 8)[1]).view(b.dtype)
+    assert np.array_equal(b[:M, N:], s[:M, N:]) and np.array_equal(b[M:], s[M:])

@@ -21,6 +21,7 @@ VARIANT_AUTO = 0
 VARIANT_TILED = 1
 VARIANT_STREAM = 2
 VARIANT_EPILOGUE_ONLY = 3
+VARIANT_TILED_PAIR = 4
 
 OK = 0
 ERR_INVALID_ARG = -1
@@ -59,7 +60,7 @@ def load_library() -> ctypes.CDLL:
             "gemm_status_string": (ctypes.c_char_p, [i32]),
             "gemm_force_variant": (i32, [vp, i32]),
             "gemm_query_plan": (i32, [vp, i64, i64, i64, i32, pi32, pi32, pi32, pi64, pi32, pi32, pi32, pi32]),
-            "gemm_schedule_tiles": (i64, [i64, i64, i32, i32, i32, ctypes.POINTER(ctypes.c_int32), i64]),
+            "gemm_schedule_tiles": (i64, [i64, i64, i32, i32, i32, i32, ctypes.POINTER(ctypes.c_int32), i64]),
             "gemm_watchdog_selftest": (i32, [vp, ctypes.c_uint64, vp]),
             "gemm_num_sms": (i32, [vp]),
             "gemm_run_noalloc": (i32, [i64, i64, i64, vp, i64, vp, i64, vp, i64, vp, i64, f32, f32, i32, vp,
@@ -120,15 +121,15 @@ def gemm_query_plan(h, M, N, K, out_dtype) -> dict:
                 cluster=cl.value, smem_bytes=sm.value, launches=la.value)
 
 
-def gemm_schedule_tiles(mt: int, nt: int, group_m: int, grid: int, cta: int):
-    """List of (m_tile, n_tile) visited by CTA `cta` (the kernels' own schedule)."""
+def gemm_schedule_tiles(mt: int, nt: int, group_m: int, workers: int, worker: int, allow_split: bool = True):
+    """Work items (tile row, first column, width) of worker `worker`: the kernels' own schedule."""
     lib = load_library()
-    n = lib.gemm_schedule_tiles(mt, nt, group_m, grid, cta, None, 0)
+    n = lib.gemm_schedule_tiles(mt, nt, group_m, workers, int(allow_split), worker, None, 0)
     if n < 0:
         raise TpgemmError(int(n), "gemm_schedule_tiles")
-    buf = (ctypes.c_int32 * max(2 * n, 1))()
-    lib.gemm_schedule_tiles(mt, nt, group_m, grid, cta, buf, n)
-    return [(buf[2 * i], buf[2 * i + 1]) for i in range(n)]
+    buf = (ctypes.c_int32 * max(3 * n, 1))()
+    lib.gemm_schedule_tiles(mt, nt, group_m, workers, int(allow_split), worker, buf, n)
+    return [(buf[3 * i], buf[3 * i + 1], buf[3 * i + 2]) for i in range(n)]
 
 
 def gemm_watchdog_selftest(h, timeout_ns: int, stream=None) -> int:

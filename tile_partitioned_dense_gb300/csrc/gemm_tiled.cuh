@@ -1,15 +1,21 @@
 // Persistent, warp-specialised bf16 GEMM for sm_103a:  D = alpha*A*B + beta*C.
 //
-// One CTA per SM (192 threads) walks its share of 128 x 256 output tiles
-// (schedule.cuh). Inside the CTA three roles run concurrently, connected by
-// mbarriers:
+// Two modes of one kernel template:
+//   kPair = false  one CTA per SM owns 128 x 256 output tiles; MMAs are
+//                  tcgen05.mma.cta_group::1 with M = 128.
+//   kPair = true   the two CTAs of a cluster pair own a 256 x 256 tile; the even
+//                  CTA issues tcgen05.mma.cta_group::2 with M = 256 for both. Each
+//                  CTA stages its own 128 rows of A and its own half of B's
+//                  columns, so per SM the ring holds 32 KB per K block instead
+//                  of 48 KB and six stages fit where four did.
+// Inside a CTA three roles run concurrently, connected by mbarriers:
 //   warp 0      TMA producer: per 64-wide K block, one A box (128 rows x 64 K,
-//               K-major) and four B boxes (64 K rows x 64 N each, N-major), all
-//               128-byte swizzled, into a 4-stage shared-memory ring.
+//               K-major) and the B boxes (64 K rows x 64 N each, N-major), all
+//               128-byte swizzled, into the shared-memory ring.
 //   warp 1      allocates all 512 TMEM columns (two 128 x 256 fp32
-//               accumulators); one lane issues tcgen05.mma (M=128, N=256,
-//               K=16, four per K block) and frees each ring stage with
-//               tcgen05.commit when the MMAs reading it are done.
+//               accumulators); one lane (of the even CTA, in pair mode) issues
+//               the MMAs, K = 16 each, four per K block, and frees each ring
+//               stage with tcgen05.commit when the MMAs reading it are done.
 //   warps 2-5   epilogue: wait for a finished accumulator, read it from TMEM
 //               (each warp its 32-lane quarter = 32 rows), apply alpha and
 //               beta*C in fp32, round to the output type, write 128-byte
@@ -20,11 +26,11 @@
 // performance com CuteDSL" lists for near-peak GEMMs (tile sizes matched to
 // the tensor-core pipeline, explicit shared-memory stages, warp
 // specialisation, TMA); the epilogue's auxiliary-tensor add is the page's
-// epilogue-fusion roadmap. Each output tile is owned by one CTA ("cuTile Rust
-// explained", "Ownership crosses the launch boundary"); inside a CTA the
-// mbarrier full/empty protocol orders every load before the MMA that reads it
-// and every MMA before the epilogue that reads its result ("Disjointness
-// outside. Ordering inside.").
+// epilogue-fusion roadmap. Each output tile (or tile piece) is owned by one
+// CTA or CTA pair ("cuTile Rust explained", "Ownership crosses the launch
+// boundary"); inside, the mbarrier full/empty protocol orders every load
+// before the MMA that reads it and every MMA before the epilogue that reads
+// its result ("Disjointness outside. Ordering inside.").
 #pragma once
 
 #include <cuda_bf16.h>
@@ -36,8 +42,8 @@ namespace tpg {
 
 struct TiledParams {
     int32_t M, N, K;
-    int32_t mt, nt, kb; // tiles along M and N, 64-wide K blocks
-    int32_t group_m;
+    int32_t kb; // 64-wide K blocks
+    Schedule sched;
     // Columns [0, n_tma) of C and D go through the tensor maps; n_tma is N
     // rounded down to a multiple of 16 bytes, because a TMA store writes whole
     // 16-byte cells of the innermost dimension even past its bound. The last
@@ -54,32 +60,34 @@ struct TiledParams {
 
 namespace tiled {
 
-constexpr int BM = 128;
-constexpr int BN = 256;
+constexpr int BM = 128;  // rows per CTA
+constexpr int BN = 256;  // columns per tile
 constexpr int BK = 64;
-constexpr int STAGES = 4;
 constexpr int THREADS = 192;
 constexpr int EPI_THREADS = 128;
-constexpr uint32_t A_STAGE_BYTES = BM * BK * 2;              // 16 KB
-constexpr uint32_t B_BOX_BYTES = BK * 64 * 2;                // 8 KB: 64 K rows x 64 N
-constexpr uint32_t B_STAGE_BYTES = BN * BK * 2;              // 32 KB
-constexpr uint32_t STAGE_TX = A_STAGE_BYTES + B_STAGE_BYTES; // bytes TMA delivers per stage
-constexpr uint32_t EPI_BUF_BYTES = BM * 128;                 // 128 rows x 128 bytes
+constexpr uint32_t A_STAGE_BYTES = BM * BK * 2; // 16 KB
+constexpr uint32_t B_BOX_BYTES = BK * 64 * 2;   // 8 KB: 64 K rows x 64 N
+constexpr uint32_t EPI_BUF_BYTES = BM * 128;    // 128 rows x 128 bytes
 constexpr uint32_t TMEM_COLS = 512;
 
-// Shared-memory layout, offsets from a 1024-byte aligned base (the 128-byte
-// swizzle pattern repeats every 1024 bytes and is computed from address bits,
-// so every swizzled buffer starts on a 1024-byte boundary).
-constexpr uint32_t OFF_A = 0;
-constexpr uint32_t OFF_B = OFF_A + STAGES * A_STAGE_BYTES;
-constexpr uint32_t OFF_EPI = OFF_B + STAGES * B_STAGE_BYTES;
-constexpr uint32_t OFF_BAR = OFF_EPI + 2 * EPI_BUF_BYTES;
-constexpr uint32_t NUM_BARS = 2 * STAGES + 2 + 2 + 2 + 1; // full, empty, tfull, tempty, c, drain
-constexpr uint32_t OFF_MISC = OFF_BAR + NUM_BARS * 8;
-constexpr uint32_t SMEM_USED = OFF_MISC + 16;
-constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024; // slack for aligning the base
-
-static_assert(SMEM_BYTES <= 232448, "exceeds the 227 KB shared-memory limit per CTA");
+template <bool kPair>
+struct Layout {
+    static constexpr int STAGES = kPair ? 6 : 4;
+    static constexpr int B_BOXES = kPair ? 2 : 4; // per CTA, full-width tile
+    static constexpr uint32_t B_STAGE_BYTES = B_BOXES * B_BOX_BYTES;
+    // Offsets from a 1024-byte aligned base (the 128-byte swizzle pattern
+    // repeats every 1024 bytes and is computed from address bits).
+    static constexpr uint32_t OFF_A = 0;
+    static constexpr uint32_t OFF_B = OFF_A + STAGES * A_STAGE_BYTES;
+    static constexpr uint32_t OFF_EPI = OFF_B + STAGES * B_STAGE_BYTES;
+    static constexpr uint32_t OFF_BAR = OFF_EPI + 2 * EPI_BUF_BYTES;
+    static constexpr uint32_t NUM_BARS = 2 * STAGES + 2 + 2 + 2 + 1; // full, empty, tfull, tempty, c, drain
+    static constexpr uint32_t OFF_MISC = OFF_BAR + NUM_BARS * 8;
+    static constexpr uint32_t SMEM_BYTES = OFF_MISC + 16 + 1024; // + slack to align the base
+};
+static_assert(Layout<false>::SMEM_BYTES <= 232448, "exceeds the 227 KB shared-memory limit per CTA");
+static_assert(Layout<true>::SMEM_BYTES <= 232448, "exceeds the 227 KB shared-memory limit per CTA");
+constexpr uint32_t SMEM_BYTES = Layout<false>::SMEM_BYTES; // the 1-CTA mode
 
 // Waits, without looking at the abort flag, for an operation this CTA itself
 // started; used only on the abort path so nothing is in flight at exit.
@@ -93,29 +101,41 @@ __device__ __forceinline__ bool drain_wait(uint64_t *bar, uint32_t parity, uint6
     return false;
 }
 
-template <bool kOutF32>
+// Busy-waits `ns` nanoseconds (abort path only).
+__device__ __forceinline__ void settle(uint64_t ns) {
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t i = 0; i < (1u << 26) && globaltimer_ns() - t0 < ns; ++i) {
+    }
+}
+
+template <bool kOutF32, bool kPair>
 __global__ void __launch_bounds__(THREADS, 1)
     gemm_tiled_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                       const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmD,
                       const TiledParams p) {
+    using L = Layout<kPair>;
+    constexpr int STAGES = L::STAGES;
     constexpr int CHUNK = kOutF32 ? 32 : 64; // output columns per 128-byte staging row
-    constexpr int CHUNKS = BN / CHUNK;
+    constexpr int CL = kPair ? 2 : 1;        // CTAs per worker
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                 ~static_cast<uintptr_t>(1023));
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + OFF_BAR);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::OFF_BAR);
     uint64_t *full = bars;
     uint64_t *empty = bars + STAGES;
     uint64_t *tfull = bars + 2 * STAGES;
     uint64_t *tempty = tfull + 2;
     uint64_t *cbar = tempty + 2;
     uint64_t *drain = cbar + 2;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + OFF_MISC);
-    volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(smem + OFF_MISC + 4);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::OFF_MISC);
+    volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(smem + L::OFF_MISC + 4);
 
     const uint32_t warp = threadIdx.x / 32;
     const uint32_t lane = threadIdx.x % 32;
+    const uint32_t rank = kPair ? cluster_ctarank() : 0u; // 0 = the even CTA, which issues the MMAs
+    const int64_t worker = static_cast<int64_t>(blockIdx.x) / CL;
+    const int64_t workers = static_cast<int64_t>(gridDim.x) / CL;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
@@ -124,7 +144,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&tfull[b], 1);
-            mbar_init(&tempty[b], EPI_THREADS / 32);
+            // every epilogue warp of the worker hands the accumulator back
+            mbar_init(&tempty[b], CL * EPI_THREADS / 32);
             mbar_init(&cbar[b], 1);
         }
         mbar_init(drain, 1);
@@ -138,39 +159,58 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (p.beta != 0.0f) prefetch_tensormap(&tmC);
     }
     if (warp == 1) {
-        tmem_alloc(tmem_slot, TMEM_COLS);
-        tmem_relinquish();
+        if constexpr (kPair) {
+            tmem_alloc_pair(tmem_slot, TMEM_COLS);
+            tmem_relinquish_pair();
+        } else {
+            tmem_alloc(tmem_slot, TMEM_COLS);
+            tmem_relinquish();
+        }
     }
     tc_fence_before();
-    __syncthreads();
+    if constexpr (kPair)
+        cluster_sync(); // barriers of both CTAs initialised, TMEM allocated in both
+    else
+        __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
 
     const WaitCtl ctl{abort_flag, p.status, p.timeout_ns};
-    const int64_t num_tiles = static_cast<int64_t>(p.mt) * p.nt;
 
     if (warp == 0) {
         // ------------------------------------------------ TMA producer
         if (lane == 0) {
+            // In pair mode both CTAs' loads complete on the even CTA's barrier.
+            const uint32_t full0 = kPair ? map_to_rank(smem_addr(full), 0) : 0u;
             uint32_t stage = 0, phase = 0;
             int64_t issued = 0;
             bool ok = true;
-            for (int64_t t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
-                const TileCoord tc = tile_of_index(t, p.mt, p.nt, p.group_m);
-                const int32_t m0 = tc.m * BM;
-                const int32_t n0 = tc.n * BN;
+            WorkItem w;
+            for (int64_t t = worker; ok && work_item(p.sched, t, BN, w); t += workers) {
+                const int32_t m0 = w.m * (BM * CL) + static_cast<int32_t>(rank) * BM;
+                const int32_t cols = w.width / CL; // B columns this CTA stages
+                const int32_t nb = w.n + static_cast<int32_t>(rank) * cols;
+                const uint32_t tx = CL * (A_STAGE_BYTES + static_cast<uint32_t>(cols) * BK * 2);
                 for (int32_t kb = 0; kb < p.kb; ++kb) {
                     if (!mbar_wait(&empty[stage], phase ^ 1u, ctl, kStatusTimeoutProducer)) {
                         ok = false;
                         break;
                     }
-                    mbar_arrive_expect_tx(&full[stage], STAGE_TX);
                     const int32_t k0 = kb * BK;
-                    tma_load_2d(&tmA, &full[stage], smem + OFF_A + stage * A_STAGE_BYTES, k0, m0);
-                    uint8_t *bdst = smem + OFF_B + stage * B_STAGE_BYTES;
-#pragma unroll
-                    for (int c = 0; c < BN / 64; ++c)
-                        tma_load_2d(&tmB, &full[stage], bdst + c * B_BOX_BYTES, n0 + c * 64, k0);
+                    uint8_t *adst = smem + L::OFF_A + stage * A_STAGE_BYTES;
+                    uint8_t *bdst = smem + L::OFF_B + stage * L::B_STAGE_BYTES;
+                    if constexpr (kPair) {
+                        if (rank == 0) mbar_arrive_expect_tx(&full[stage], tx);
+                        const uint32_t fb = full0 + stage * 8u;
+                        tma_load_2d_pair(&tmA, fb, adst, k0, m0);
+                        for (int c = 0; c < cols / 64; ++c)
+                            tma_load_2d_pair(&tmB, fb, bdst + c * B_BOX_BYTES, nb + c * 64, k0);
+                    } else {
+                        mbar_arrive_expect_tx(&full[stage], tx);
+                        tma_load_2d(&tmA, &full[stage], adst, k0, m0);
+                        for (int c = 0; c < cols / 64; ++c)
+                            tma_load_2d(&tmB, &full[stage], bdst + c * B_BOX_BYTES, nb + c * 64, k0);
+                    }
                     ++issued;
                     if (++stage == STAGES) {
                         stage = 0;
@@ -179,31 +219,37 @@ __global__ void __launch_bounds__(THREADS, 1)
                 }
             }
             if (!ok) {
-                // Let the loads already issued land before the CTA exits.
-                const int64_t pending = issued < STAGES ? issued : STAGES;
-                uint32_t s = stage, ph = phase;
-                for (int64_t i = 0; i < pending; ++i) {
-                    if (s == 0) {
-                        s = STAGES - 1;
-                        ph ^= 1u;
-                    } else {
-                        --s;
+                if (!kPair || rank == 0) {
+                    // Let the loads already issued land before the CTA exits.
+                    const int64_t pending = issued < STAGES ? issued : STAGES;
+                    uint32_t s = stage, ph = phase;
+                    for (int64_t i = 0; i < pending; ++i) {
+                        if (s == 0) {
+                            s = STAGES - 1;
+                            ph ^= 1u;
+                        } else {
+                            --s;
+                        }
+                        if (!drain_wait(&full[s], ph, p.timeout_ns) && p.status)
+                            atomicOr(p.status, kStatusTimeoutDrain);
                     }
-                    if (!drain_wait(&full[s], ph, p.timeout_ns) && p.status)
-                        atomicOr(p.status, kStatusTimeoutDrain);
                 }
+                // The odd CTA's loads complete on the even CTA's barriers, which it
+                // cannot wait on: give them time to land.
+                if (kPair) settle(200000);
             }
         }
         __syncwarp();
     } else if (warp == 1) {
-        // ------------------------------------------------ MMA issuer
-        if (lane == 0) {
-            constexpr uint32_t idesc = make_idesc_bf16_f32(BM, BN, false, true);
+        // ------------------------------------------------ MMA issuer (even CTA only in pair mode)
+        if (lane == 0 && rank == 0) {
             uint32_t stage = 0, phase = 0;
             uint32_t acc = 0, acc_phase = 0;
             bool ok = true;
             bool any = false;
-            for (int64_t t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+            WorkItem w;
+            for (int64_t t = worker; ok && work_item(p.sched, t, BN, w); t += workers) {
+                const uint32_t idesc = make_idesc_bf16_f32(BM * CL, static_cast<uint32_t>(w.width), false, true);
                 if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, ctl, kStatusTimeoutMma)) {
                     ok = false;
                     break;
@@ -216,27 +262,35 @@ __global__ void __launch_bounds__(THREADS, 1)
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t a_addr = smem_addr(smem + OFF_A + stage * A_STAGE_BYTES);
-                    const uint32_t b_addr = smem_addr(smem + OFF_B + stage * B_STAGE_BYTES);
+                    const uint32_t a_addr = smem_addr(smem + L::OFF_A + stage * A_STAGE_BYTES);
+                    const uint32_t b_addr = smem_addr(smem + L::OFF_B + stage * L::B_STAGE_BYTES);
 #pragma unroll
                     for (int kk = 0; kk < BK / 16; ++kk) {
                         // A: K-major, advance 16 bf16 = 32 bytes inside the swizzle atom.
                         const uint64_t adesc = make_smem_desc_sw128(a_addr + kk * 32, 16, 1024);
                         // B: N-major, advance 16 K rows = 2048 bytes; 64-wide N blocks are
                         // one 8 KB box apart.
-                        const uint64_t bdesc =
-                            make_smem_desc_sw128(b_addr + kk * 2048, B_BOX_BYTES, 1024);
-                        tc_mma_f16(d_tmem, adesc, bdesc, idesc, (kb | kk) != 0 ? 1u : 0u);
+                        const uint64_t bdesc = make_smem_desc_sw128(b_addr + kk * 2048, B_BOX_BYTES, 1024);
+                        if constexpr (kPair)
+                            tc_mma_f16_pair(d_tmem, adesc, bdesc, idesc, (kb | kk) != 0 ? 1u : 0u);
+                        else
+                            tc_mma_f16(d_tmem, adesc, bdesc, idesc, (kb | kk) != 0 ? 1u : 0u);
                     }
                     any = true;
-                    tc_commit(&empty[stage]);
+                    if constexpr (kPair)
+                        tc_commit_pair_mc(&empty[stage], 0x3);
+                    else
+                        tc_commit(&empty[stage]);
                     if (++stage == STAGES) {
                         stage = 0;
                         phase ^= 1u;
                     }
                 }
                 if (!ok) break;
-                tc_commit(&tfull[acc]);
+                if constexpr (kPair)
+                    tc_commit_pair_mc(&tfull[acc], 0x3);
+                else
+                    tc_commit(&tfull[acc]);
                 if (++acc == 2) {
                     acc = 0;
                     acc_phase ^= 1u;
@@ -244,29 +298,32 @@ __global__ void __launch_bounds__(THREADS, 1)
             }
             if (!ok && any) {
                 // Wait for every MMA issued so far before TMEM is freed.
-                tc_commit(drain);
-                if (!drain_wait(drain, 0, p.timeout_ns) && p.status)
-                    atomicOr(p.status, kStatusTimeoutDrain);
+                if constexpr (kPair)
+                    tc_commit_pair_mc(drain, 0x1);
+                else
+                    tc_commit(drain);
+                if (!drain_wait(drain, 0, p.timeout_ns) && p.status) atomicOr(p.status, kStatusTimeoutDrain);
             }
         }
         __syncwarp();
     } else {
         // ------------------------------------------------ epilogue (warps 2..5)
-        const uint32_t q = warp & 3u;  // TMEM lane quarter this warp may read
-        const uint32_t row = q * 32u + lane; // row of the tile held by this thread
+        const uint32_t q = warp & 3u;        // TMEM lane quarter this warp may read
+        const uint32_t row = q * 32u + lane; // row of the CTA's 128 rows held by this thread
         const bool leader = threadIdx.x == 64;
         const bool has_beta = p.beta != 0.0f;
-        uint8_t *epi = smem + OFF_EPI;
+        const uint32_t tempty0 = kPair ? map_to_rank(smem_addr(tempty), 0) : 0u;
+        uint8_t *epi = smem + L::OFF_EPI;
         uint32_t acc = 0, acc_phase = 0;
         uint32_t slot = 0;
         uint32_t cphase = 0; // bit b: parity of the next wait on cbar[b]
         bool ok = true;
-        for (int64_t t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
-            const TileCoord tc = tile_of_index(t, p.mt, p.nt, p.group_m);
-            const int32_t m0 = tc.m * BM;
-            const int32_t n0 = tc.n * BN;
-            int nchunks = (p.N - n0 + CHUNK - 1) / CHUNK;
-            if (nchunks > CHUNKS) nchunks = CHUNKS;
+        WorkItem w;
+        for (int64_t t = worker; ok && work_item(p.sched, t, BN, w); t += workers) {
+            const int32_t m0 = w.m * (BM * CL) + static_cast<int32_t>(rank) * BM;
+            int nchunks = (p.N - w.n + CHUNK - 1) / CHUNK;
+            if (nchunks > w.width / CHUNK) nchunks = w.width / CHUNK;
+            if (p.N <= w.n) nchunks = 0;
             // Every wait of the epilogue ends in a vote, so that all 128 threads
             // leave together if any of them gave up (no thread is left behind
             // at a later bar.sync).
@@ -276,13 +333,27 @@ __global__ void __launch_bounds__(THREADS, 1)
                 break;
             }
             tc_fence_after();
+            const uint32_t acc_now = acc;
+            auto release = [&]() {
+                // Whole accumulator read: hand it back to the MMA warp.
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) {
+                    if constexpr (kPair)
+                        mbar_arrive_cluster(tempty0 + acc_now * 8u);
+                    else
+                        mbar_arrive(&tempty[acc_now]);
+                }
+            };
+            if (nchunks == 0) release(); // a piece entirely right of N: nothing to store
             for (int c = 0; c < nchunks; ++c) {
                 uint8_t *buf = epi + slot * EPI_BUF_BYTES;
-                const int32_t cb = n0 + c * CHUNK; // first column of this chunk
+                const int32_t cb = w.n + c * CHUNK; // first column of this chunk
                 const bool chunk_tma = cb < p.n_tma;
                 // the ragged cell [n_tma, N) when it falls in this chunk, else -1
-                const int tail_cell =
-                    (p.N > p.n_tma && cb <= p.n_tma && p.n_tma < cb + CHUNK) ? (p.n_tma - cb) / (16 / (kOutF32 ? 4 : 2)) : -1;
+                const int tail_cell = (p.N > p.n_tma && cb <= p.n_tma && p.n_tma < cb + CHUNK)
+                                          ? (p.n_tma - cb) / (16 / (kOutF32 ? 4 : 2))
+                                          : -1;
                 const int32_t grow = m0 + static_cast<int32_t>(row); // global row of this thread
                 const bool row_ok = grow < p.M;
                 // The store that last used this buffer must have finished reading it.
@@ -293,26 +364,20 @@ __global__ void __launch_bounds__(THREADS, 1)
                         mbar_arrive_expect_tx(&cbar[slot], EPI_BUF_BYTES);
                         tma_load_2d(&tmC, &cbar[slot], buf, cb, m0);
                     }
-                    const bool gotc =
-                        mbar_wait(&cbar[slot], (cphase >> slot) & 1u, ctl, kStatusTimeoutEpilogue);
+                    const bool gotc = mbar_wait(&cbar[slot], (cphase >> slot) & 1u, ctl, kStatusTimeoutEpilogue);
                     if (named_barrier_or(1, EPI_THREADS, !gotc)) {
                         ok = false;
                         break;
                     }
                     cphase ^= 1u << slot;
                 }
-                const uint32_t taddr = tmem_base + acc * BN + c * CHUNK + ((q * 32u) << 16);
+                const uint32_t taddr = tmem_base + acc * BN + static_cast<uint32_t>(c * CHUNK) + ((q * 32u) << 16);
                 uint32_t r0[32];
                 uint32_t r1[32];
                 tmem_ld32(taddr, r0);
                 if (!kOutF32) tmem_ld32(taddr + 32, r1);
                 tc_wait_ld();
-                if (c == nchunks - 1) {
-                    // Whole accumulator read: hand it back to the MMA warp.
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&tempty[acc]);
-                }
+                if (c == nchunks - 1) release();
                 uint8_t *rowp = buf + row * 128u;
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
@@ -343,8 +408,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                             v[2] = fmaf(p.beta, __uint_as_float(cv.z), v[2]);
                             v[3] = fmaf(p.beta, __uint_as_float(cv.w), v[3]);
                         }
-                        *cell = make_uint4(__float_as_uint(v[0]), __float_as_uint(v[1]),
-                                           __float_as_uint(v[2]), __float_as_uint(v[3]));
+                        *cell = make_uint4(__float_as_uint(v[0]), __float_as_uint(v[1]), __float_as_uint(v[2]),
+                                           __float_as_uint(v[3]));
                     } else {
                         float v[8];
 #pragma unroll
@@ -377,8 +442,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                                 v[2 * e + 1] = fmaf(p.beta, bf16hi_to_f32(cw[e]), v[2 * e + 1]);
                             }
                         }
-                        *cell = make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]),
-                                           pack_bf16x2(v[4], v[5]), pack_bf16x2(v[6], v[7]));
+                        *cell = make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]), pack_bf16x2(v[4], v[5]),
+                                           pack_bf16x2(v[6], v[7]));
                     }
                 }
                 fence_proxy_async_smem();
@@ -399,10 +464,16 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
 
     tc_fence_before();
-    __syncthreads();
+    if constexpr (kPair)
+        cluster_sync(); // the peer may still arrive on this CTA's barriers until here
+    else
+        __syncthreads();
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc(tmem_base, TMEM_COLS);
+        if constexpr (kPair)
+            tmem_dealloc_pair(tmem_base, TMEM_COLS);
+        else
+            tmem_dealloc(tmem_base, TMEM_COLS);
     }
 }
 

@@ -3,16 +3,23 @@
 // boundary": each tile program receives an exclusive output sub-tensor), turned
 // into a static schedule for a persistent grid.
 //
-// CTA c of a grid of G CTAs owns the tiles with linear index t = c, c + G,
-// c + 2G, ... < mt * nt. Each linear index maps to exactly one (m_tile,
-// n_tile) pair, and each pair to exactly one index, so every output tile has
-// exactly one owner and no two CTAs ever write the same element.
+// The output is a grid of mt x nt tiles (rows of BM, columns of BN). A grid of
+// P workers (CTAs, or CTA pairs) walks a single linear index t = w, w + P,
+// w + 2P, ... for worker w:
+//   - indices t < whole are whole tiles, mapped to (m, n) by a grouped raster;
+//   - indices whole <= t < whole + pieces are column pieces of the remaining
+//     tiles: tile whole + (t - whole) / split, piece (t - whole) % split, each
+//     BN / split columns wide.
+// whole is a multiple of P (the complete rounds), so the pieces start a new
+// round. Cutting a last round that is at most half full into halves lets every
+// worker take one half instead of leaving most workers idle while some finish a
+// whole tile (wave quantization). Every (tile, piece) pair has exactly one
+// index, so every output element has exactly one owner: no atomics, no split-K.
 //
-// The map is a grouped raster: the output is cut into bands of `group_m` tile
-// rows; inside a band the index runs down the band's rows first and then
-// across the columns. Tiles that run at the same time then share a few B
-// column panels and A row panels, which keeps the operands of concurrently
-// running tiles resident in L2.
+// The grouped raster: the tile grid is cut into bands of `group_m` tile rows;
+// inside a band the index runs down the band's rows first, then across the
+// columns, so tiles that run at the same time share a few B column panels and
+// A row panels and keep them resident in L2.
 #pragma once
 
 #include <stdint.h>
@@ -35,6 +42,58 @@ __host__ __device__ __forceinline__ TileCoord tile_of_index(int64_t t, int64_t m
     c.m = static_cast<int32_t>(first_m + local % rows_here);
     c.n = static_cast<int32_t>(local / rows_here);
     return c;
+}
+
+struct Schedule {
+    int64_t mt, nt;  // tile grid
+    int32_t group_m; // band height of the grouped raster, in tiles
+    int32_t split;   // 1 or 2: column pieces per tile after the whole rounds
+    int64_t whole;   // tiles processed whole (a multiple of the worker count)
+    int64_t pieces;  // split * (mt * nt - whole)
+};
+
+// One unit of work: tile row m (in tiles), first column n and width (in columns).
+struct WorkItem {
+    int32_t m;
+    int32_t n;
+    int32_t width;
+};
+
+// The unit with linear index t, or false past the end.
+__host__ __device__ __forceinline__ bool work_item(const Schedule &s, int64_t t, int32_t bn,
+                                                   WorkItem &w) {
+    if (t < s.whole) {
+        const TileCoord c = tile_of_index(t, s.mt, s.nt, s.group_m);
+        w.m = c.m;
+        w.n = c.n * bn;
+        w.width = bn;
+        return true;
+    }
+    const int64_t u = t - s.whole;
+    if (u >= s.pieces) return false;
+    const TileCoord c = tile_of_index(s.whole + u / s.split, s.mt, s.nt, s.group_m);
+    const int32_t width = bn / s.split;
+    w.m = c.m;
+    w.n = c.n * bn + static_cast<int32_t>(u % s.split) * width;
+    w.width = width;
+    return true;
+}
+
+// Host-side choice for `workers` persistent workers: whole rounds first, then
+// the remainder cut in halves when it fills at most half a round.
+__host__ __device__ __forceinline__ Schedule make_schedule(int64_t mt, int64_t nt, int32_t group_m,
+                                                           int64_t workers, bool allow_split) {
+    Schedule s;
+    s.mt = mt;
+    s.nt = nt;
+    s.group_m = group_m;
+    const int64_t total = mt * nt;
+    const int64_t rounds = workers > 0 ? total / workers : 0;
+    const int64_t rest = total - rounds * workers;
+    s.whole = rounds * workers;
+    s.split = (allow_split && rest > 0 && 2 * rest <= workers) ? 2 : 1;
+    s.pieces = s.split * rest;
+    return s;
 }
 
 } // namespace tpg

@@ -22,7 +22,8 @@
 namespace {
 
 constexpr int64_t kMaxDim = 2147483647; // 2^31 - 1
-constexpr int kGroupM = 16;             // grouped-raster band height, in tiles
+constexpr int kGroupM = 16;             // grouped-raster band height, in tiles (1-CTA mode)
+constexpr int kGroupMPair = 8;          // band height in 256-row pair tiles
 constexpr int kStreamMaxM = 64;
 
 struct Plan {
@@ -34,6 +35,7 @@ struct Plan {
     int smem = 0;
     int launches = 0;
     int mt_pad = 0, stages = 0, split = 1;
+    tpg::Schedule sched{};
 };
 
 } // namespace
@@ -47,6 +49,8 @@ struct tpgemm_handle {
     uint64_t timeout_ns = 2000000000ull;
     // co-resident 2-CTA clusters of the streaming kernel, per [out f32][mt/16 - 1]
     int stream_clusters[2][4] = {{0, 0, 0, 0}, {0, 0, 0, 0}};
+    // co-resident CTA pairs of the tiled kernel in pair mode, per [out f32]
+    int pair_clusters[2] = {0, 0};
 };
 
 namespace {
@@ -122,6 +126,31 @@ int stream_clusters_for(tpgemm_handle *h, bool f32, int mt, int stages) {
     return n;
 }
 
+int pair_clusters_for(tpgemm_handle *h, bool f32) {
+    int &slot = h->pair_clusters[f32 ? 1 : 0];
+    if (slot > 0) return slot;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * (h->num_sms / 2), 1, 1);
+    cfg.blockDim = dim3(tpg::tiled::THREADS, 1, 1);
+    cfg.dynamicSmemBytes = tpg::tiled::Layout<true>::SMEM_BYTES;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    cudaError_t e = f32 ? cudaOccupancyMaxActiveClusters(&n, tpg::tiled::gemm_tiled_kernel<true, true>, &cfg)
+                        : cudaOccupancyMaxActiveClusters(&n, tpg::tiled::gemm_tiled_kernel<false, true>, &cfg);
+    if (e != cudaSuccess || n <= 0) {
+        (void)cudaGetLastError();
+        n = h->num_sms / 2;
+    }
+    slot = n;
+    return n;
+}
+
 Plan make_plan(tpgemm_handle *h, int64_t M, int64_t N, int64_t K, int out_dtype) {
     Plan pl;
     if (M == 0 || N == 0) return pl;
@@ -135,18 +164,28 @@ Plan make_plan(tpgemm_handle *h, int64_t M, int64_t N, int64_t K, int out_dtype)
         return pl;
     }
     int variant = h->forced;
-    if (variant == TPGEMM_VARIANT_AUTO) variant = M <= kStreamMaxM ? TPGEMM_VARIANT_STREAM : TPGEMM_VARIANT_TILED;
+    if (variant == TPGEMM_VARIANT_AUTO)
+        variant = M <= kStreamMaxM ? TPGEMM_VARIANT_STREAM
+                  : M <= tpg::tiled::BM ? TPGEMM_VARIANT_TILED
+                                        : TPGEMM_VARIANT_TILED_PAIR;
     if (variant == TPGEMM_VARIANT_STREAM && M > kStreamMaxM) variant = TPGEMM_VARIANT_TILED;
     pl.variant = variant;
     pl.launches = 1;
-    if (variant == TPGEMM_VARIANT_TILED) {
-        const int64_t mt = (M + tpg::tiled::BM - 1) / tpg::tiled::BM;
+    if (variant == TPGEMM_VARIANT_TILED || variant == TPGEMM_VARIANT_TILED_PAIR) {
+        const bool pair = variant == TPGEMM_VARIANT_TILED_PAIR;
+        const int64_t rows = tpg::tiled::BM * (pair ? 2 : 1);
+        const int64_t mt = (M + rows - 1) / rows;
         const int64_t nt = (N + tpg::tiled::BN - 1) / tpg::tiled::BN;
-        pl.tile_m = tpg::tiled::BM;
+        pl.tile_m = static_cast<int>(rows);
         pl.tile_n = tpg::tiled::BN;
         pl.num_tiles = mt * nt;
-        pl.grid = static_cast<int>(pl.num_tiles < h->num_sms ? pl.num_tiles : h->num_sms);
-        pl.smem = static_cast<int>(tpg::tiled::SMEM_BYTES);
+        const int64_t cap = pair ? pair_clusters_for(h, out_dtype == TPGEMM_OUT_F32) : h->num_sms;
+        const int64_t workers = pl.num_tiles < cap ? pl.num_tiles : cap;
+        pl.cluster = pair ? 2 : 1;
+        pl.grid = static_cast<int>(workers * pl.cluster);
+        pl.sched = tpg::make_schedule(mt, nt, pair ? kGroupMPair : kGroupM, workers, true);
+        pl.split = pl.sched.split;
+        pl.smem = static_cast<int>(pair ? tpg::tiled::Layout<true>::SMEM_BYTES : tpg::tiled::Layout<false>::SMEM_BYTES);
         return pl;
     }
     // weight-streaming variant
@@ -243,10 +282,15 @@ int gemm_create(tpgemm_handle **out, int device) {
     }
     h->encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
     bool ok = true;
-    ok &= cudaFuncSetAttribute(tpg::tiled::gemm_tiled_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               static_cast<int>(tpg::tiled::SMEM_BYTES)) == cudaSuccess;
-    ok &= cudaFuncSetAttribute(tpg::tiled::gemm_tiled_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               static_cast<int>(tpg::tiled::SMEM_BYTES)) == cudaSuccess;
+    ok &= cudaFuncSetAttribute(tpg::tiled::gemm_tiled_kernel<false, false>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(tpg::tiled::Layout<false>::SMEM_BYTES)) == cudaSuccess;
+    ok &= cudaFuncSetAttribute(tpg::tiled::gemm_tiled_kernel<true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(tpg::tiled::Layout<false>::SMEM_BYTES)) == cudaSuccess;
+    ok &= cudaFuncSetAttribute(tpg::tiled::gemm_tiled_kernel<false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(tpg::tiled::Layout<true>::SMEM_BYTES)) == cudaSuccess;
+    ok &= cudaFuncSetAttribute(tpg::tiled::gemm_tiled_kernel<true, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(tpg::tiled::Layout<true>::SMEM_BYTES)) == cudaSuccess;
     const int stream_smem = static_cast<int>(tpg::stream::SMEM_LIMIT);
     ok &= cudaFuncSetAttribute(tpg::stream::gemm_stream_kernel<false, 1>,
                                cudaFuncAttributeMaxDynamicSharedMemorySize, stream_smem) == cudaSuccess;
@@ -282,7 +326,8 @@ int gemm_num_sms(tpgemm_handle *h) { return h ? h->num_sms : TPGEMM_ERR_INVALID_
 
 int gemm_force_variant(tpgemm_handle *h, int variant) {
     if (!h) return TPGEMM_ERR_INVALID_ARG;
-    if (variant != TPGEMM_VARIANT_AUTO && variant != TPGEMM_VARIANT_TILED && variant != TPGEMM_VARIANT_STREAM)
+    if (variant != TPGEMM_VARIANT_AUTO && variant != TPGEMM_VARIANT_TILED && variant != TPGEMM_VARIANT_STREAM &&
+        variant != TPGEMM_VARIANT_TILED_PAIR)
         return TPGEMM_ERR_INVALID_ARG;
     h->forced = variant;
     return TPGEMM_OK;
@@ -307,16 +352,19 @@ int gemm_query_plan(tpgemm_handle *h, int64_t M, int64_t N, int64_t K, int out_d
     return TPGEMM_OK;
 }
 
-int64_t gemm_schedule_tiles(int64_t mt, int64_t nt, int group_m, int grid, int cta, int32_t *out, int64_t cap) {
-    if (mt < 0 || nt < 0 || group_m < 1 || grid < 1 || cta < 0 || cta >= grid || cap < 0 || (cap > 0 && !out))
+int64_t gemm_schedule_tiles(int64_t mt, int64_t nt, int group_m, int workers, int allow_split, int worker,
+                            int32_t *out, int64_t cap) {
+    if (mt < 0 || nt < 0 || group_m < 1 || workers < 1 || worker < 0 || worker >= workers || cap < 0 ||
+        (cap > 0 && !out))
         return TPGEMM_ERR_INVALID_ARG;
-    const int64_t total = mt * nt;
+    const tpg::Schedule s = tpg::make_schedule(mt, nt, group_m, workers, allow_split != 0);
     int64_t count = 0;
-    for (int64_t t = cta; t < total; t += grid, ++count) {
+    tpg::WorkItem w;
+    for (int64_t t = worker; tpg::work_item(s, t, tpg::tiled::BN, w); t += workers, ++count) {
         if (count < cap) {
-            const tpg::TileCoord c = tpg::tile_of_index(t, mt, nt, group_m);
-            out[2 * count] = c.m;
-            out[2 * count + 1] = c.n;
+            out[3 * count] = w.m;
+            out[3 * count + 1] = w.n;
+            out[3 * count + 2] = w.width;
         }
     }
     return count;
@@ -378,7 +426,7 @@ int gemm_run(tpgemm_handle *h, int64_t M, int64_t N, int64_t K, const void *A, i
 
     const CUtensorMapDataType out_dt = f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
     CUtensorMap tmA, tmB;
-    if (pl.variant == TPGEMM_VARIANT_TILED) {
+    if (pl.variant == TPGEMM_VARIANT_TILED || pl.variant == TPGEMM_VARIANT_TILED_PAIR) {
         CUtensorMap tmC, tmD;
         const uint32_t chunk = f32 ? 32u : 64u;
         // C and D maps stop at the last whole 16-byte cell of a row (see TiledParams::n_tma);
@@ -397,10 +445,8 @@ int gemm_run(tpgemm_handle *h, int64_t M, int64_t N, int64_t K, const void *A, i
         p.M = static_cast<int32_t>(M);
         p.N = static_cast<int32_t>(N);
         p.K = static_cast<int32_t>(K);
-        p.mt = static_cast<int32_t>((M + tpg::tiled::BM - 1) / tpg::tiled::BM);
-        p.nt = static_cast<int32_t>((N + tpg::tiled::BN - 1) / tpg::tiled::BN);
         p.kb = static_cast<int32_t>((K + tpg::tiled::BK - 1) / tpg::tiled::BK);
-        p.group_m = kGroupM;
+        p.sched = pl.sched;
         p.n_tma = static_cast<int32_t>(n_tma);
         p.alpha = alpha;
         p.beta = beta;
@@ -410,10 +456,16 @@ int gemm_run(tpgemm_handle *h, int64_t M, int64_t N, int64_t K, const void *A, i
         p.ldd = ldd;
         p.status = h->status;
         p.timeout_ns = h->timeout_ns;
-        return f32 ? launch(tpg::tiled::gemm_tiled_kernel<true>, pl.grid, tpg::tiled::THREADS, pl.smem, 1, stream,
-                            tmA, tmB, tmC, tmD, p)
-                   : launch(tpg::tiled::gemm_tiled_kernel<false>, pl.grid, tpg::tiled::THREADS, pl.smem, 1, stream,
-                            tmA, tmB, tmC, tmD, p);
+        const int thr = tpg::tiled::THREADS;
+        if (pl.variant == TPGEMM_VARIANT_TILED_PAIR)
+            return f32 ? launch(tpg::tiled::gemm_tiled_kernel<true, true>, pl.grid, thr, pl.smem, 2, stream, tmA, tmB,
+                                tmC, tmD, p)
+                       : launch(tpg::tiled::gemm_tiled_kernel<false, true>, pl.grid, thr, pl.smem, 2, stream, tmA,
+                                tmB, tmC, tmD, p);
+        return f32 ? launch(tpg::tiled::gemm_tiled_kernel<true, false>, pl.grid, thr, pl.smem, 1, stream, tmA, tmB, tmC,
+                            tmD, p)
+                   : launch(tpg::tiled::gemm_tiled_kernel<false, false>, pl.grid, thr, pl.smem, 1, stream, tmA, tmB,
+                            tmC, tmD, p);
     }
 
     // weight-streaming variant
@@ -530,9 +582,11 @@ int noalloc_setup(int dev, NoallocDevice **out) {
                 cudaSuccess ||
             q != cudaDriverEntryPointSuccess || !fn)
             return TPGEMM_ERR_CUDA;
-        if (cudaFuncSetAttribute(tpg::tiled::gemm_tiled_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        if (cudaFuncSetAttribute(tpg::tiled::gemm_tiled_kernel<false, false>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  static_cast<int>(tpg::tiled::SMEM_BYTES)) != cudaSuccess ||
-            cudaFuncSetAttribute(tpg::tiled::gemm_tiled_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+            cudaFuncSetAttribute(tpg::tiled::gemm_tiled_kernel<true, false>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  static_cast<int>(tpg::tiled::SMEM_BYTES)) != cudaSuccess ||
             cudaMemset(ptr, 0, sizeof(uint32_t) * kNoallocStatusWords) != cudaSuccess) {
             (void)cudaGetLastError();
@@ -611,10 +665,12 @@ extern "C" int gemm_run_noalloc(int64_t M, int64_t N, int64_t K, const void *A, 
         p.M = static_cast<int32_t>(M);
         p.N = static_cast<int32_t>(N);
         p.K = static_cast<int32_t>(K);
-        p.mt = static_cast<int32_t>((M + tpg::tiled::BM - 1) / tpg::tiled::BM);
-        p.nt = static_cast<int32_t>((N + tpg::tiled::BN - 1) / tpg::tiled::BN);
+        const int64_t mt = (M + tpg::tiled::BM - 1) / tpg::tiled::BM;
+        const int64_t nt = (N + tpg::tiled::BN - 1) / tpg::tiled::BN;
+        const int64_t tiles = mt * nt;
+        const int grid = static_cast<int>(tiles < nd->num_sms ? tiles : nd->num_sms);
         p.kb = static_cast<int32_t>((K + tpg::tiled::BK - 1) / tpg::tiled::BK);
-        p.group_m = kGroupM;
+        p.sched = tpg::make_schedule(mt, nt, kGroupM, grid, true);
         p.n_tma = static_cast<int32_t>(n_tma);
         p.alpha = alpha;
         p.beta = beta;
@@ -624,13 +680,11 @@ extern "C" int gemm_run_noalloc(int64_t M, int64_t N, int64_t K, const void *A, 
         p.ldd = ldd;
         p.status = nd->status;
         p.timeout_ns = 2000000000ull;
-        const int64_t tiles = static_cast<int64_t>(p.mt) * p.nt;
-        const int grid = static_cast<int>(tiles < nd->num_sms ? tiles : nd->num_sms);
         const int smem = static_cast<int>(tpg::tiled::SMEM_BYTES);
-        rc = f32 ? launch(tpg::tiled::gemm_tiled_kernel<true>, grid, tpg::tiled::THREADS, smem, 1, stream, tmA, tmB,
-                          tmC, tmD, p)
-                 : launch(tpg::tiled::gemm_tiled_kernel<false>, grid, tpg::tiled::THREADS, smem, 1, stream, tmA, tmB,
-                          tmC, tmD, p);
+        rc = f32 ? launch(tpg::tiled::gemm_tiled_kernel<true, false>, grid, tpg::tiled::THREADS, smem, 1, stream, tmA,
+                          tmB, tmC, tmD, p)
+                 : launch(tpg::tiled::gemm_tiled_kernel<false, false>, grid, tpg::tiled::THREADS, smem, 1, stream,
+                          tmA, tmB, tmC, tmD, p);
     }
     if (rc != TPGEMM_OK || !check_status) return rc;
     if (cudaStreamSynchronize(stream) != cudaSuccess) return TPGEMM_ERR_CUDA;
