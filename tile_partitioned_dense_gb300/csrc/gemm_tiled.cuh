@@ -174,6 +174,9 @@ __global__ void __launch_bounds__(THREADS, 1)
         __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    // Everything above touched only on-chip state; from here on global memory.
+    grid_dependency_wait();
+    grid_launch_dependents();
 
     const WaitCtl ctl{abort_flag, p.status, p.timeout_ns};
 

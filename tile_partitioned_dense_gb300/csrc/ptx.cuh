@@ -146,6 +146,20 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint64_t *bar, uint32_t parity
     return mbar_wait_slow<true>(a, parity, ctl, code);
 }
 
+// ---------------------------------------------------------------- programmatic dependent launch
+// A kernel launched with programmatic stream serialisation may start while the
+// previous kernel in the stream is still running. It does its prologue (barrier
+// init, TMEM allocation, tensor-map prefetch), then waits here until the
+// previous grid has completed and its memory is visible, before it reads any
+// input or writes any output.
+__device__ __forceinline__ void grid_dependency_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+// Lets the next kernel in the stream be scheduled as soon as SMs free up.
+__device__ __forceinline__ void grid_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- cluster
 __device__ __forceinline__ uint32_t cluster_ctarank() {
     uint32_t r;

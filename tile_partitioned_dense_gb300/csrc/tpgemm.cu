@@ -211,25 +211,41 @@ Plan make_plan(tpgemm_handle *h, int64_t M, int64_t N, int64_t K, int out_dtype)
     return pl;
 }
 
+// Launches `kernel`. With pdl, the launch allows programmatic dependent launch:
+// the kernel may start its on-chip prologue while the previous kernel in the
+// stream finishes, and waits (griddepcontrol.wait) before touching global
+// memory; only the GEMM kernels, which do that wait, are launched this way.
 template <typename Kernel, typename... Args>
-int launch(Kernel kernel, int grid, int block, int smem, int cluster, cudaStream_t stream,
-           Args... args) {
+int launch_ex(Kernel kernel, int grid, int block, int smem, int cluster, bool pdl, cudaStream_t stream,
+              Args... args) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
     cfg.blockDim = dim3(static_cast<unsigned>(block), 1, 1);
     cfg.dynamicSmemBytes = static_cast<size_t>(smem);
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
+    unsigned n = 0;
     if (cluster > 1) {
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = static_cast<unsigned>(cluster);
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
+        attr[n].id = cudaLaunchAttributeClusterDimension;
+        attr[n].val.clusterDim.x = static_cast<unsigned>(cluster);
+        attr[n].val.clusterDim.y = 1;
+        attr[n].val.clusterDim.z = 1;
+        ++n;
     }
+    if (pdl) {
+        attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[n].val.programmaticStreamSerializationAllowed = 1;
+        ++n;
+    }
+    cfg.attrs = n ? attr : nullptr;
+    cfg.numAttrs = n;
     cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, args...);
     return e == cudaSuccess ? TPGEMM_OK : TPGEMM_ERR_CUDA;
+}
+
+template <typename Kernel, typename... Args>
+int launch(Kernel kernel, int grid, int block, int smem, int cluster, cudaStream_t stream, Args... args) {
+    return launch_ex(kernel, grid, block, smem, cluster, false, stream, args...);
 }
 
 } // namespace
@@ -458,14 +474,14 @@ int gemm_run(tpgemm_handle *h, int64_t M, int64_t N, int64_t K, const void *A, i
         p.timeout_ns = h->timeout_ns;
         const int thr = tpg::tiled::THREADS;
         if (pl.variant == TPGEMM_VARIANT_TILED_PAIR)
-            return f32 ? launch(tpg::tiled::gemm_tiled_kernel<true, true>, pl.grid, thr, pl.smem, 2, stream, tmA, tmB,
-                                tmC, tmD, p)
-                       : launch(tpg::tiled::gemm_tiled_kernel<false, true>, pl.grid, thr, pl.smem, 2, stream, tmA,
-                                tmB, tmC, tmD, p);
-        return f32 ? launch(tpg::tiled::gemm_tiled_kernel<true, false>, pl.grid, thr, pl.smem, 1, stream, tmA, tmB, tmC,
-                            tmD, p)
-                   : launch(tpg::tiled::gemm_tiled_kernel<false, false>, pl.grid, thr, pl.smem, 1, stream, tmA, tmB,
-                            tmC, tmD, p);
+            return f32 ? launch_ex(tpg::tiled::gemm_tiled_kernel<true, true>, pl.grid, thr, pl.smem, 2, true, stream,
+                                   tmA, tmB, tmC, tmD, p)
+                       : launch_ex(tpg::tiled::gemm_tiled_kernel<false, true>, pl.grid, thr, pl.smem, 2, true, stream,
+                                   tmA, tmB, tmC, tmD, p);
+        return f32 ? launch_ex(tpg::tiled::gemm_tiled_kernel<true, false>, pl.grid, thr, pl.smem, 1, true, stream, tmA,
+                               tmB, tmC, tmD, p)
+                   : launch_ex(tpg::tiled::gemm_tiled_kernel<false, false>, pl.grid, thr, pl.smem, 1, true, stream,
+                               tmA, tmB, tmC, tmD, p);
     }
 
     // weight-streaming variant
@@ -490,14 +506,14 @@ int gemm_run(tpgemm_handle *h, int64_t M, int64_t N, int64_t K, const void *A, i
     p.status = h->status;
     p.timeout_ns = h->timeout_ns;
     if (pl.split == 2)
-        return f32 ? launch(tpg::stream::gemm_stream_kernel<true, 2>, pl.grid, tpg::stream::THREADS, pl.smem, 2,
-                            stream, tmA, tmB, p)
-                   : launch(tpg::stream::gemm_stream_kernel<false, 2>, pl.grid, tpg::stream::THREADS, pl.smem, 2,
-                            stream, tmA, tmB, p);
-    return f32 ? launch(tpg::stream::gemm_stream_kernel<true, 1>, pl.grid, tpg::stream::THREADS, pl.smem, 1, stream,
-                        tmA, tmB, p)
-               : launch(tpg::stream::gemm_stream_kernel<false, 1>, pl.grid, tpg::stream::THREADS, pl.smem, 1, stream,
-                        tmA, tmB, p);
+        return f32 ? launch_ex(tpg::stream::gemm_stream_kernel<true, 2>, pl.grid, tpg::stream::THREADS, pl.smem, 2,
+                               true, stream, tmA, tmB, p)
+                   : launch_ex(tpg::stream::gemm_stream_kernel<false, 2>, pl.grid, tpg::stream::THREADS, pl.smem, 2,
+                               true, stream, tmA, tmB, p);
+    return f32 ? launch_ex(tpg::stream::gemm_stream_kernel<true, 1>, pl.grid, tpg::stream::THREADS, pl.smem, 1, true,
+                           stream, tmA, tmB, p)
+               : launch_ex(tpg::stream::gemm_stream_kernel<false, 1>, pl.grid, tpg::stream::THREADS, pl.smem, 1, true,
+                           stream, tmA, tmB, p);
 }
 
 int gemm_sync_status(tpgemm_handle *h, void *stream) {
