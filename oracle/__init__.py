@@ -22,6 +22,10 @@ import torch
 
 OUT_BF16 = 0
 OUT_F32 = 1
+ACT_NONE = 0
+ACT_RELU = 1
+ACT_SIGMOID = 2
+ACT_TANH = 3
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "oracle.c")
@@ -52,6 +56,12 @@ def _load():
         lib.oracle_gemm_rows.restype = ctypes.c_int
         lib.oracle_gemm_rows.argtypes = [i64, i64, i64, vp, i64, vp, i64, vp, i64, dbl, dbl,
                                          ctypes.c_int, vp, i64, vp, i64, vp, i64, ctypes.c_int]
+        lib.oracle_gemm_rows_epilogue.restype = ctypes.c_int
+        lib.oracle_gemm_rows_epilogue.argtypes = [i64, i64, i64, vp, i64, vp, i64, vp, i64, dbl, dbl,
+                                                  ctypes.c_int, vp, i64, vp, i64, vp, i64, ctypes.c_int,
+                                                  vp, ctypes.c_int, ctypes.c_int, vp, i64]
+        lib.oracle_act.restype = dbl
+        lib.oracle_act.argtypes = [ctypes.c_int, dbl]
         lib.oracle_round_bf16.restype = ctypes.c_uint16
         lib.oracle_round_bf16.argtypes = [dbl]
         lib.oracle_round_f32.restype = ctypes.c_float
@@ -121,6 +131,54 @@ def gemm_rows(A: torch.Tensor, B: torch.Tensor, C: torch.Tensor | None, alpha: f
     if rc != 0:
         raise RuntimeError("oracle_gemm_rows rejected its arguments")
     return D, pre
+
+
+def gemm_rows_epilogue(A, B, C, alpha, beta, out_dtype, bias=None, act=ACT_NONE, aux=None, rows=None,
+                       want_pre=False, nthreads=None):
+    """gemm_rows followed by the fused epilogue: v = alpha*acc + beta*C + bias[n];
+    v = act(v); v = v * aux[m, n]; one rounding. bias is a 1-D bf16/fp32 CPU
+    tensor of N values; aux an [M, N] CPU tensor of the output dtype."""
+    lib = _load()
+    if A.dtype != torch.bfloat16 or B.dtype != torch.bfloat16:
+        raise TypeError("A and B must be bf16")
+    M, K = A.shape
+    N = B.shape[1]
+    alpha = float(np.float32(alpha))
+    beta = float(np.float32(beta))
+    if rows is None:
+        rows = np.arange(M, dtype=np.int64)
+    rows = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+    a_ptr, lda = _bits_view(A, "A")
+    b_ptr, ldb = _bits_view(B, "B")
+    c_ptr, ldc = 0, max(N, 1)
+    if beta != 0.0:
+        c_ptr, ldc = _bits_view(C, "C")
+    bias_ptr, bias_dt = None, OUT_F32
+    if bias is not None:
+        bias = bias.contiguous()
+        if bias.numel() != N:
+            raise ValueError("bias must have N elements")
+        bias_ptr = bias.data_ptr()
+        bias_dt = OUT_BF16 if bias.dtype == torch.bfloat16 else OUT_F32
+    aux_ptr, ldaux = None, max(N, 1)
+    if aux is not None:
+        aux_ptr, ldaux = _bits_view(aux, "aux")
+    out_np = np.uint16 if out_dtype == OUT_BF16 else np.float32
+    D = np.zeros((len(rows), N), dtype=out_np)
+    pre = np.zeros((len(rows), N), dtype=np.float64) if want_pre else None
+    if nthreads is None:
+        nthreads = len(os.sched_getaffinity(0))
+    rc = lib.oracle_gemm_rows_epilogue(M, N, K, a_ptr, lda, b_ptr, ldb, c_ptr, ldc, alpha, beta,
+                                       out_dtype, rows.ctypes.data, len(rows), D.ctypes.data, max(N, 1),
+                                       pre.ctypes.data if pre is not None else None, max(N, 1),
+                                       int(nthreads), bias_ptr, bias_dt, int(act), aux_ptr, ldaux)
+    if rc != 0:
+        raise RuntimeError("oracle_gemm_rows_epilogue rejected its arguments")
+    return D, pre
+
+
+def activation(act: int, x: float) -> float:
+    return float(_load().oracle_act(int(act), float(x)))
 
 
 def round_bf16(x: float) -> int:

@@ -97,6 +97,36 @@ void oracle_round_bf16_array(const double *in, uint16_t *out, int64_t n) {
     for (int64_t i = 0; i < n; ++i) out[i] = oracle_round_bf16(in[i]);
 }
 
+/*
+ * Fused epilogue (the EFC capabilities listed in the epilogue-fusion roadmap
+ * paragraph of "TorchInductor ganha suporte a GEMMs de alta performance com
+ * CuteDSL": auxiliary tensor loads, element-wise add and mul, activations
+ * ReLU, sigmoid and tanh). The order, a reading of the page, is
+ *     v = alpha*acc + beta*C;  v = v + bias[n];  v = act(v);  v = v * aux[m,n]
+ * all in fp64 (libm exp and tanh), then one rounding to the output dtype.
+ */
+#define ORACLE_ACT_NONE 0
+#define ORACLE_ACT_RELU 1
+#define ORACLE_ACT_SIGMOID 2
+#define ORACLE_ACT_TANH 3
+
+static double oracle_activation(int act, double v) {
+    switch (act) {
+    case ORACLE_ACT_RELU: return v > 0.0 ? v : 0.0;
+    case ORACLE_ACT_SIGMOID: return 1.0 / (1.0 + exp(-v));
+    case ORACLE_ACT_TANH: return tanh(v);
+    default: return v;
+    }
+}
+
+typedef struct {
+    const void *bias; /* NULL or [N] of bias_dtype */
+    int bias_dtype;
+    int act;
+    const void *aux; /* NULL or [M, N] of the output dtype, row stride ldaux */
+    int64_t ldaux;
+} oracle_epilogue;
+
 typedef struct {
     int64_t N, K;
     const uint16_t *A;
@@ -113,8 +143,14 @@ typedef struct {
     int64_t ldd; /* row stride of D, in elements; D row r holds output row rows[r] */
     double *pre;
     int64_t ldpre; /* row stride of pre; NULL pre = not wanted */
+    const oracle_epilogue *epi; /* NULL = plain alpha*acc + beta*C */
     int status;
 } oracle_job;
+
+static double oracle_decode_out(int out_dtype, const void *base, int64_t idx) {
+    if (out_dtype == ORACLE_OUT_BF16) return oracle_decode_bf16(((const uint16_t *)base)[idx]);
+    return oracle_decode_f32((const float *)base + idx);
+}
 
 static void *oracle_rows_worker(void *arg) {
     oracle_job *j = (oracle_job *)arg;
@@ -142,6 +178,12 @@ static void *oracle_rows_worker(void *arg) {
                     c = oracle_decode_f32((const float *)j->C + i * j->ldc + n);
                 v = v + j->beta * c;
             }
+            if (j->epi) {
+                const oracle_epilogue *e = j->epi;
+                if (e->bias) v = v + oracle_decode_out(e->bias_dtype, e->bias, n);
+                v = oracle_activation(e->act, v);
+                if (e->aux) v = v * oracle_decode_out(j->out_dtype, e->aux, i * e->ldaux + n);
+            }
             if (j->pre) j->pre[r * j->ldpre + n] = v;
             if (j->out_dtype == ORACLE_OUT_BF16)
                 ((uint16_t *)j->D)[r * j->ldd + n] = oracle_round_bf16(v);
@@ -164,10 +206,11 @@ static void *oracle_rows_worker(void *arg) {
  * nthreads <= 0 means one thread. Returns 0, or -1 on a bad argument or an
  * allocation failure.
  */
-int oracle_gemm_rows(int64_t M, int64_t N, int64_t K, const uint16_t *A, int64_t lda,
-                     const uint16_t *B, int64_t ldb, const void *C, int64_t ldc, double alpha,
-                     double beta, int out_dtype, const int64_t *rows, int64_t nrows, void *D,
-                     int64_t ldd, double *pre, int64_t ldpre, int nthreads) {
+static int oracle_gemm_rows_impl(int64_t M, int64_t N, int64_t K, const uint16_t *A, int64_t lda,
+                                 const uint16_t *B, int64_t ldb, const void *C, int64_t ldc,
+                                 double alpha, double beta, int out_dtype, const int64_t *rows,
+                                 int64_t nrows, void *D, int64_t ldd, double *pre, int64_t ldpre,
+                                 int nthreads, const oracle_epilogue *epi) {
     if (M < 0 || N < 0 || K < 0 || nrows < 0) return -1;
     if (out_dtype != ORACLE_OUT_BF16 && out_dtype != ORACLE_OUT_F32) return -1;
     if (nrows == 0 || N == 0) return 0;
@@ -193,7 +236,7 @@ int oracle_gemm_rows(int64_t M, int64_t N, int64_t K, const uint16_t *A, int64_t
         oracle_job *j = &jobs[t];
         j->N = N; j->K = K; j->A = A; j->lda = lda; j->B = B; j->ldb = ldb;
         j->C = C; j->ldc = ldc; j->alpha = alpha; j->beta = beta; j->out_dtype = out_dtype;
-        j->rows = rows; j->D = D; j->ldd = ldd; j->pre = pre; j->ldpre = ldpre;
+        j->rows = rows; j->D = D; j->ldd = ldd; j->pre = pre; j->ldpre = ldpre; j->epi = epi;
         j->row_begin = nrows * t / nthreads;
         j->row_end = nrows * (t + 1) / nthreads;
         j->status = -1;
@@ -215,3 +258,29 @@ int oracle_gemm_rows(int64_t M, int64_t N, int64_t K, const uint16_t *A, int64_t
     free(spawned);
     return rc;
 }
+
+int oracle_gemm_rows(int64_t M, int64_t N, int64_t K, const uint16_t *A, int64_t lda,
+                     const uint16_t *B, int64_t ldb, const void *C, int64_t ldc, double alpha,
+                     double beta, int out_dtype, const int64_t *rows, int64_t nrows, void *D,
+                     int64_t ldd, double *pre, int64_t ldpre, int nthreads) {
+    return oracle_gemm_rows_impl(M, N, K, A, lda, B, ldb, C, ldc, alpha, beta, out_dtype, rows,
+                                 nrows, D, ldd, pre, ldpre, nthreads, NULL);
+}
+
+/* oracle_gemm_rows plus the fused epilogue described above oracle_activation. */
+int oracle_gemm_rows_epilogue(int64_t M, int64_t N, int64_t K, const uint16_t *A, int64_t lda,
+                              const uint16_t *B, int64_t ldb, const void *C, int64_t ldc,
+                              double alpha, double beta, int out_dtype, const int64_t *rows,
+                              int64_t nrows, void *D, int64_t ldd, double *pre, int64_t ldpre,
+                              int nthreads, const void *bias, int bias_dtype, int act,
+                              const void *aux, int64_t ldaux) {
+    if (act < ORACLE_ACT_NONE || act > ORACLE_ACT_TANH) return -1;
+    if (bias && bias_dtype != ORACLE_OUT_BF16 && bias_dtype != ORACLE_OUT_F32) return -1;
+    if (aux && ldaux < N) return -1;
+    oracle_epilogue e = {bias, bias_dtype, act, aux, ldaux};
+    return oracle_gemm_rows_impl(M, N, K, A, lda, B, ldb, C, ldc, alpha, beta, out_dtype, rows,
+                                 nrows, D, ldd, pre, ldpre, nthreads, &e);
+}
+
+/* The activation alone, for its pins. */
+double oracle_act(int act, double v) { return oracle_activation(act, v); }
