@@ -187,6 +187,39 @@ class Workload:
                             c.alpha, c.beta, self.out_code, stream)
 
 
+class FusedWorkload(Workload):
+    """A workload whose epilogue adds a bias row, applies an activation and
+    multiplies by an auxiliary [M, N] tensor: fused into gemm_run_epilogue, or
+    (unfused) the plain GEMM followed by the same element-wise work in torch."""
+
+    def __init__(self, cfg, torch, l2_bytes, activation, fused):
+        super().__init__(cfg, torch, l2_bytes, pinned=False)
+        g = torch.Generator().manual_seed(cfg.seed + 100)
+        self.torch = torch
+        self.act = activation
+        self.fused = fused
+        bias = (torch.randn(cfg.N, generator=g) * 0.1).to(torch.bfloat16).cuda()
+        for st in self.sets:
+            st["bias"] = bias
+            st["aux"] = torch.rand(cfg.M, cfg.N, generator=g).to(self.out_dtype).cuda()
+
+    def run(self, tpd, h, i, stream):
+        if not self.fused:
+            st = super().run(tpd, h, i, stream)
+            s = self.sets[i % self.nsets]
+            torch = self.torch
+            f = {1: torch.relu, 2: torch.sigmoid, 3: torch.tanh}[self.act]
+            s["D"].copy_(f(s["D"] + s["bias"]) * s["aux"])
+            return st
+        s = self.sets[i % self.nsets]
+        c = self.cfg
+        epi = tpd.Epilogue(s["bias"].data_ptr(), tpd.OUT_BF16, self.act, s["aux"].data_ptr(), c.N)
+        C = s["C"]
+        return tpd.gemm_run_epilogue(h, c.M, c.N, c.K, s["A"].data_ptr(), c.K, s["B"].data_ptr(), c.N,
+                                     C.data_ptr() if C is not None else None, c.N, s["D"].data_ptr(), c.N,
+                                     c.alpha, c.beta, self.out_code, epi, stream)
+
+
 def time_launches(torch, tpd, h, wl, steps, warmup, barrier):
     """Time `steps` back-to-back launches, bracketed by barrier + synchronize.
 
@@ -411,6 +444,25 @@ def run_ours(args):
             launches += steps2
             del w2
             torch.cuda.empty_cache()
+
+    if not args.no_extra:
+        # fused epilogue (bias + sigmoid + aux multiply) on the QKV shape, against the
+        # plain GEMM followed by the same element-wise work in torch
+        c2 = CONFIGS["qkv"]
+        out = {}
+        for fused in (True, False):
+            w2 = FusedWorkload(c2, torch, l2, tpd.ACT_SIGMOID, fused)
+            span2, _ = time_launches(torch, tpd, h, w2, 200, 5, barrier)
+            out[fused] = span2 / 200
+            del w2
+            torch.cuda.empty_cache()
+        per_config["qkv_bias_sigmoid_aux"] = {
+            "value": round(c2.flops / (out[True] * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+            "ms_per_step": round(out[True], 5), "unfused_ms_per_step": round(out[False], 5),
+            "speedup_vs_unfused": round(out[False] / out[True], 3),
+            "config": {"workload": "qkv shape, D = sigmoid(A*B + bias) * aux, bf16; unfused = gemm_run then "
+                                   "torch sigmoid(D + bias) * aux in the same graph", "M": c2.M, "N": c2.N, "K": c2.K}}
+        launches += 200
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

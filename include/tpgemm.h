@@ -76,6 +76,39 @@ enum tpgemm_variant {
     TPGEMM_VARIANT_TILED_PAIR = 4 /* the tiled kernel on CTA pairs: 256x256 tiles, cta_group::2 MMA */
 };
 
+/* Activation of the fused epilogue. */
+enum tpgemm_activation {
+    TPGEMM_ACT_NONE = 0,
+    TPGEMM_ACT_RELU = 1,    /* max(v, 0) */
+    TPGEMM_ACT_SIGMOID = 2, /* 1 / (1 + exp(-v)) */
+    TPGEMM_ACT_TANH = 3     /* tanh(v) */
+};
+
+/*
+ * Fused epilogue: the element-wise work that follows a GEMM in a transformer
+ * layer, done on the accumulator before the single rounding to the output
+ * type, instead of in separate kernels that re-read D ("TorchInductor ganha
+ * suporte a GEMMs de alta performance com CuteDSL", epilogue-fusion roadmap
+ * paragraph: auxiliary tensor loads, element-wise add and mul, ReLU,
+ * sigmoid, tanh). Per element, in fp32:
+ *     v = alpha * acc + beta * C[m,n]
+ *     v = v + bias[n]              (if bias != NULL)
+ *     v = activation(v)
+ *     v = v * aux[m,n]             (if aux != NULL)
+ *     D[m,n] = round(v)
+ * bias: N values of bias_dtype (TPGEMM_OUT_BF16 or TPGEMM_OUT_F32), 16-byte
+ * aligned. aux: [M, N] of the output dtype, row stride ldaux >= N, 16-byte
+ * aligned with ldaux * element size a multiple of 16; it may be D itself
+ * (same stride) but may not otherwise overlap D. Both are read-only.
+ */
+typedef struct tpgemm_epilogue {
+    const void *bias;
+    int bias_dtype;
+    int activation;
+    const void *aux;
+    int64_t ldaux;
+} tpgemm_epilogue;
+
 /*
  * Creates a handle for CUDA device `device`. Checks that the device is
  * compute capability 10.3, reads its SM count, resolves the driver's
@@ -107,6 +140,18 @@ int gemm_create(tpgemm_handle **out, int device);
 int gemm_run(tpgemm_handle *h, int64_t M, int64_t N, int64_t K, const void *A, int64_t lda,
              const void *B, int64_t ldb, const void *C, int64_t ldc, void *D, int64_t ldd,
              float alpha, float beta, int out_dtype, void *stream);
+
+/*
+ * gemm_run with a fused epilogue (see tpgemm_epilogue). epi == NULL is exactly
+ * gemm_run. Extra argument errors: TPGEMM_ERR_INVALID_ARG for a bad
+ * activation or bias dtype or ldaux < N, TPGEMM_ERR_ALIGNMENT for a misaligned
+ * bias, aux or ldaux, TPGEMM_ERR_OVERLAP when bias overlaps D or aux partially
+ * overlaps D. Like gemm_run it allocates nothing and never synchronises.
+ */
+int gemm_run_epilogue(tpgemm_handle *h, int64_t M, int64_t N, int64_t K, const void *A,
+                      int64_t lda, const void *B, int64_t ldb, const void *C, int64_t ldc,
+                      void *D, int64_t ldd, float alpha, float beta, int out_dtype,
+                      const tpgemm_epilogue *epi, void *stream);
 
 /*
  * Synchronises `stream`, then reads and clears the handle's device status

@@ -23,6 +23,11 @@ VARIANT_STREAM = 2
 VARIANT_EPILOGUE_ONLY = 3
 VARIANT_TILED_PAIR = 4
 
+ACT_NONE = 0
+ACT_RELU = 1
+ACT_SIGMOID = 2
+ACT_TANH = 3
+
 OK = 0
 ERR_INVALID_ARG = -1
 ERR_ALIGNMENT = -2
@@ -33,6 +38,12 @@ ERR_TIMEOUT = -6
 ERR_TOO_LARGE = -7
 
 _lib = None
+
+
+class Epilogue(ctypes.Structure):
+    """Mirror of struct tpgemm_epilogue (include/tpgemm.h)."""
+    _fields_ = [("bias", ctypes.c_void_p), ("bias_dtype", ctypes.c_int), ("activation", ctypes.c_int),
+                ("aux", ctypes.c_void_p), ("ldaux", ctypes.c_int64)]
 
 
 class TpgemmError(RuntimeError):
@@ -55,6 +66,8 @@ def load_library() -> ctypes.CDLL:
             "gemm_create": (i32, [ctypes.POINTER(vp), i32]),
             "gemm_run": (i32, [vp, i64, i64, i64, vp, i64, vp, i64, vp, i64, vp, i64, f32, f32, i32, vp]),
             "gemm_sync_status": (i32, [vp, vp]),
+            "gemm_run_epilogue": (i32, [vp, i64, i64, i64, vp, i64, vp, i64, vp, i64, vp, i64, f32, f32, i32,
+                                        ctypes.POINTER(Epilogue), vp]),
             "gemm_check_args": (i32, [i64, i64, i64, vp, i64, vp, i64, vp, i64, vp, i64, f32, i32]),
             "gemm_destroy": (i32, [vp]),
             "gemm_status_string": (ctypes.c_char_p, [i32]),
@@ -87,6 +100,12 @@ def gemm_create(device: int = 0) -> ctypes.c_void_p:
 def gemm_run(h, M, N, K, A, lda, B, ldb, C, ldc, D, ldd, alpha, beta, out_dtype, stream) -> int:
     return load_library().gemm_run(h, M, N, K, A, lda, B, ldb, C, ldc, D, ldd, alpha, beta,
                                    out_dtype, stream)
+
+
+def gemm_run_epilogue(h, M, N, K, A, lda, B, ldb, C, ldc, D, ldd, alpha, beta, out_dtype, epi, stream) -> int:
+    """epi: an Epilogue or None (plain gemm_run)."""
+    return load_library().gemm_run_epilogue(h, M, N, K, A, lda, B, ldb, C, ldc, D, ldd, alpha, beta,
+                                            out_dtype, ctypes.byref(epi) if epi is not None else None, stream)
 
 
 def gemm_sync_status(h, stream=None) -> int:
@@ -168,7 +187,8 @@ class Gemm:
         except Exception:
             pass
 
-    def __call__(self, A, B, C=None, alpha=1.0, beta=0.0, out_dtype=None, out=None, stream=None):
+    def __call__(self, A, B, C=None, alpha=1.0, beta=0.0, out_dtype=None, out=None, stream=None,
+                 bias=None, activation=ACT_NONE, aux=None):
         import torch
         if out_dtype is None:
             out_dtype = out.dtype if out is not None else torch.bfloat16
@@ -191,8 +211,14 @@ class Gemm:
         b, ldb = ptr_ld(B, N)
         c, ldc = ptr_ld(C, N)
         d, ldd = ptr_ld(out, N)
-        st = gemm_run(self.handle, M, N, K, a, lda, b, ldb, c, ldc, d, ldd, float(alpha), float(beta),
-                      odt, stream)
+        epi = None
+        if bias is not None or aux is not None or activation != ACT_NONE:
+            x, ldx = ptr_ld(aux, N)
+            epi = Epilogue(bias.data_ptr() if bias is not None else None,
+                           OUT_F32 if (bias is not None and bias.dtype == torch.float32) else OUT_BF16,
+                           int(activation), x, ldx)
+        st = gemm_run_epilogue(self.handle, M, N, K, a, lda, b, ldb, c, ldc, d, ldd, float(alpha),
+                               float(beta), odt, epi, stream)
         if st != OK:
             raise TpgemmError(st, "gemm_run")
         return out
@@ -201,9 +227,10 @@ class Gemm:
 _default = {}
 
 
-def matmul(A, B, C=None, alpha=1.0, beta=0.0, out_dtype=None, out=None, stream=None):
-    """D = alpha*A*B + beta*C on the GPU through the C ABI (one handle per device)."""
+def matmul(A, B, C=None, alpha=1.0, beta=0.0, out_dtype=None, out=None, stream=None, bias=None,
+           activation=ACT_NONE, aux=None):
+    """D = act(alpha*A*B + beta*C + bias) * aux on the GPU through the C ABI (one handle per device)."""
     dev = A.device.index if A.device.index is not None else 0
     if dev not in _default:
         _default[dev] = Gemm(dev)
-    return _default[dev](A, B, C, alpha, beta, out_dtype, out, stream)
+    return _default[dev](A, B, C, alpha, beta, out_dtype, out, stream, bias, activation, aux)

@@ -8,30 +8,31 @@
 //    forever).
 #pragma once
 
+#include "epilogue.cuh"
 #include "ptx.cuh"
 
 namespace tpg {
 
-template <bool kOutF32>
-__global__ void __launch_bounds__(256) epilogue_only_kernel(int32_t M, int32_t N, float beta,
-                                                            const void *C, int64_t ldc, void *D,
-                                                            int64_t ldd) {
+template <bool kOutF32, bool kEpi>
+__global__ void __launch_bounds__(256) epilogue_only_kernel(int32_t M, int32_t N, float beta, const void *C,
+                                                            int64_t ldc, void *D, int64_t ldd, EpiParams epi) {
     const int64_t total = static_cast<int64_t>(M) * N;
     for (int64_t idx = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; idx < total;
          idx += static_cast<int64_t>(gridDim.x) * blockDim.x) {
         const int64_t i = idx / N;
-        const int64_t j = idx - i * N;
-        if constexpr (kOutF32) {
-            const float c = beta != 0.0f ? beta * static_cast<const float *>(C)[i * ldc + j] : 0.0f;
-            static_cast<float *>(D)[i * ldd + j] = c;
-        } else {
-            float c = 0.0f;
-            if (beta != 0.0f) {
-                const uint16_t b = static_cast<const uint16_t *>(C)[i * ldc + j];
-                c = beta * __uint_as_float(static_cast<uint32_t>(b) << 16);
-            }
-            static_cast<uint16_t *>(D)[i * ldd + j] = static_cast<uint16_t>(pack_bf16x2(c, 0.0f) & 0xFFFFu);
+        const int32_t j = static_cast<int32_t>(idx - i * N);
+        float c = 0.0f;
+        if (beta != 0.0f) {
+            if constexpr (kOutF32)
+                c = beta * static_cast<const float *>(C)[i * ldc + j];
+            else
+                c = beta * __uint_as_float(static_cast<uint32_t>(static_cast<const uint16_t *>(C)[i * ldc + j]) << 16);
         }
+        if constexpr (kEpi) c = epilogue_one<kOutF32>(epi, i, j, c);
+        if constexpr (kOutF32)
+            static_cast<float *>(D)[i * ldd + j] = c;
+        else
+            static_cast<uint16_t *>(D)[i * ldd + j] = static_cast<uint16_t>(pack_bf16x2(c, 0.0f) & 0xFFFFu);
     }
 }
 

@@ -25,6 +25,7 @@
 // columns of D per warp, MT token rows per thread).
 #pragma once
 
+#include "epilogue.cuh"
 #include "ptx.cuh"
 
 namespace tpg {
@@ -42,6 +43,7 @@ struct StreamParams {
     int64_t ldd;
     uint32_t *status;
     uint64_t timeout_ns;
+    EpiParams epi; // read only by the kEpi instantiations
 };
 
 namespace stream {
@@ -87,7 +89,7 @@ __device__ __forceinline__ bool drain_wait(uint64_t *bar, uint32_t parity, uint6
     return false;
 }
 
-template <bool kOutF32, int SPLIT>
+template <bool kOutF32, int SPLIT, bool kEpi>
 __global__ void __launch_bounds__(THREADS, 1)
     gemm_stream_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                        const StreamParams p) {
@@ -335,12 +337,14 @@ __global__ void __launch_bounds__(THREADS, 1)
                     if constexpr (kOutF32) {
                         if (has_beta)
                             x = fmaf(p.beta, static_cast<const float *>(p.C)[m * p.ldc + n], x);
+                        if constexpr (kEpi) x = epilogue_one<true>(p.epi, m, n, x);
                         static_cast<float *>(p.D)[m * p.ldd + n] = x;
                     } else {
                         if (has_beta) {
                             const uint16_t cb = static_cast<const uint16_t *>(p.C)[m * p.ldc + n];
                             x = fmaf(p.beta, __uint_as_float(static_cast<uint32_t>(cb) << 16), x);
                         }
+                        if constexpr (kEpi) x = epilogue_one<false>(p.epi, m, n, x);
                         static_cast<uint16_t *>(p.D)[m * p.ldd + n] =
                             static_cast<uint16_t>(pack_bf16x2(x, 0.0f) & 0xFFFFu);
                     }

@@ -35,6 +35,7 @@
 
 #include <cuda_bf16.h>
 
+#include "epilogue.cuh"
 #include "ptx.cuh"
 #include "schedule.cuh"
 
@@ -56,6 +57,7 @@ struct TiledParams {
     int64_t ldd;
     uint32_t *status;
     uint64_t timeout_ns;
+    EpiParams epi; // read only by the fused-epilogue instantiations
 };
 
 namespace tiled {
@@ -108,7 +110,10 @@ __device__ __forceinline__ void settle(uint64_t ns) {
     }
 }
 
-template <bool kOutF32, bool kPair>
+// kEpi: 0 plain alpha*acc + beta*C; 1 + activation for the fused epilogue
+// (bias and aux are runtime options; the activation is compiled in, so each
+// instantiation carries only its own math).
+template <bool kOutF32, bool kPair, int kEpi>
 __global__ void __launch_bounds__(THREADS, 1)
     gemm_tiled_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                       const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmD,
@@ -359,6 +364,14 @@ __global__ void __launch_bounds__(THREADS, 1)
                                           : -1;
                 const int32_t grow = m0 + static_cast<int32_t>(row); // global row of this thread
                 const bool row_ok = grow < p.M;
+                // Fused epilogue: this row's aux cells for the chunk, all in flight at once,
+                // while the staging buffer frees up and C arrives.
+                uint4 auxq[8];
+                if constexpr (kEpi > 0) {
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        auxq[j] = load_aux_cell<kOutF32>(p.epi, p.N, grow, row_ok, cb + j * (kOutF32 ? 4 : 8));
+                }
                 // The store that last used this buffer must have finished reading it.
                 if (leader) bulk_wait_group_read<1>();
                 named_barrier_sync(1, EPI_THREADS);
@@ -395,12 +408,14 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
                             for (int e = 0; e < 4; ++e) {
                                 const int32_t col = cb + j * 4 + e;
-                                if (row_ok && col < p.N) {
-                                    float x = v[e];
-                                    if (has_beta)
-                                        x = fmaf(p.beta, static_cast<const float *>(p.C)[grow * p.ldc + col], x);
-                                    static_cast<float *>(p.D)[grow * p.ldd + col] = x;
-                                }
+                                if (has_beta && row_ok && col < p.N)
+                                    v[e] = fmaf(p.beta, static_cast<const float *>(p.C)[grow * p.ldc + col], v[e]);
+                            }
+                            if constexpr (kEpi > 0) epilogue_cell<4, true, kEpi - 1>(p.epi, p.N, grow, row_ok, cb + j * 4, v, auxq[j]);
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                const int32_t col = cb + j * 4 + e;
+                                if (row_ok && col < p.N) static_cast<float *>(p.D)[grow * p.ldd + col] = v[e];
                             }
                             continue;
                         }
@@ -411,6 +426,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                             v[2] = fmaf(p.beta, __uint_as_float(cv.z), v[2]);
                             v[3] = fmaf(p.beta, __uint_as_float(cv.w), v[3]);
                         }
+                        if constexpr (kEpi > 0) epilogue_cell<4, true, kEpi - 1>(p.epi, p.N, grow, row_ok, cb + j * 4, v, auxq[j]);
                         *cell = make_uint4(__float_as_uint(v[0]), __float_as_uint(v[1]), __float_as_uint(v[2]),
                                            __float_as_uint(v[3]));
                     } else {
@@ -424,15 +440,18 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
                             for (int e = 0; e < 8; ++e) {
                                 const int32_t col = cb + j * 8 + e;
-                                if (row_ok && col < p.N) {
-                                    float x = v[e];
-                                    if (has_beta) {
-                                        const uint16_t cbits = static_cast<const uint16_t *>(p.C)[grow * p.ldc + col];
-                                        x = fmaf(p.beta, __uint_as_float(static_cast<uint32_t>(cbits) << 16), x);
-                                    }
-                                    static_cast<uint16_t *>(p.D)[grow * p.ldd + col] =
-                                        static_cast<uint16_t>(pack_bf16x2(x, 0.0f) & 0xFFFFu);
+                                if (has_beta && row_ok && col < p.N) {
+                                    const uint16_t cbits = static_cast<const uint16_t *>(p.C)[grow * p.ldc + col];
+                                    v[e] = fmaf(p.beta, __uint_as_float(static_cast<uint32_t>(cbits) << 16), v[e]);
                                 }
+                            }
+                            if constexpr (kEpi > 0) epilogue_cell<8, false, kEpi - 1>(p.epi, p.N, grow, row_ok, cb + j * 8, v, auxq[j]);
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) {
+                                const int32_t col = cb + j * 8 + e;
+                                if (row_ok && col < p.N)
+                                    static_cast<uint16_t *>(p.D)[grow * p.ldd + col] =
+                                        static_cast<uint16_t>(pack_bf16x2(v[e], 0.0f) & 0xFFFFu);
                             }
                             continue;
                         }
@@ -445,6 +464,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                                 v[2 * e + 1] = fmaf(p.beta, bf16hi_to_f32(cw[e]), v[2 * e + 1]);
                             }
                         }
+                        if constexpr (kEpi > 0) epilogue_cell<8, false, kEpi - 1>(p.epi, p.N, grow, row_ok, cb + j * 8, v, auxq[j]);
                         *cell = make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]), pack_bf16x2(v[4], v[5]),
                                            pack_bf16x2(v[6], v[7]));
                     }

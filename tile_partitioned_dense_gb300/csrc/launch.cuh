@@ -1,0 +1,93 @@
+// Kernel launch helpers and the interface between the host library
+// (tpgemm.cu) and the translation units that instantiate the GEMM kernels
+// (tiled_inst.cu, once per fused-epilogue mode, and stream_inst.cu). Only
+// those units name kernel instantiations, so each instantiation is compiled
+// once, and the units build in parallel.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "gemm_stream.cuh"
+#include "gemm_tiled.cuh"
+
+namespace tpg {
+
+// Launches `kernel`. With pdl, the launch allows programmatic dependent launch:
+// the kernel may start its on-chip prologue while the previous kernel in the
+// stream finishes, and waits (griddepcontrol.wait) before touching global
+// memory; only the GEMM kernels, which do that wait, are launched this way.
+// Returns cudaSuccess or the launch error.
+template <typename Kernel, typename... Args>
+cudaError_t launch_ex(Kernel kernel, int grid, int block, int smem, int cluster, bool pdl, cudaStream_t stream,
+                      Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+    cfg.blockDim = dim3(static_cast<unsigned>(block), 1, 1);
+    cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    unsigned n = 0;
+    if (cluster > 1) {
+        attr[n].id = cudaLaunchAttributeClusterDimension;
+        attr[n].val.clusterDim.x = static_cast<unsigned>(cluster);
+        attr[n].val.clusterDim.y = 1;
+        attr[n].val.clusterDim.z = 1;
+        ++n;
+    }
+    if (pdl) {
+        attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[n].val.programmaticStreamSerializationAllowed = 1;
+        ++n;
+    }
+    cfg.attrs = n ? attr : nullptr;
+    cfg.numAttrs = n;
+    return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
+// Fused-epilogue modes of the tiled kernel (its kEpi template argument):
+// 0 plain alpha*acc + beta*C; 1 + activation otherwise (bias and aux are
+// runtime options inside every fused mode).
+constexpr int kEpiModes = 5;
+
+struct TiledLaunch {
+    int grid;
+    int smem;
+    bool pair;
+    bool f32;
+    cudaStream_t stream;
+    const CUtensorMap *a, *b, *c, *d;
+    const TiledParams *p;
+};
+
+struct StreamLaunch {
+    int grid;
+    int smem;
+    int split;
+    bool f32;
+    bool fused;
+    cudaStream_t stream;
+    const CUtensorMap *a, *b;
+    const StreamParams *p;
+};
+
+// tiled_inst.cu, one definition per mode E (compiled with -DTPG_EPI=E).
+cudaError_t tiled_launch_e0(const TiledLaunch &l);
+cudaError_t tiled_launch_e1(const TiledLaunch &l);
+cudaError_t tiled_launch_e2(const TiledLaunch &l);
+cudaError_t tiled_launch_e3(const TiledLaunch &l);
+cudaError_t tiled_launch_e4(const TiledLaunch &l);
+bool tiled_set_limits_e0();
+bool tiled_set_limits_e1();
+bool tiled_set_limits_e2();
+bool tiled_set_limits_e3();
+bool tiled_set_limits_e4();
+// co-resident CTA pairs of the pair-mode kernel (plain mode), or -1
+int tiled_pair_clusters(bool f32, int num_sms);
+
+// stream_inst.cu
+cudaError_t stream_launch(const StreamLaunch &l);
+bool stream_set_limits();
+int stream_split_clusters(bool f32, int num_sms, int smem);
+
+} // namespace tpg

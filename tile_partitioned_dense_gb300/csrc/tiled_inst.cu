@@ -1,0 +1,67 @@
+// Instantiations of the tiled GEMM kernel for one fused-epilogue mode, E =
+// TPG_EPI (see launch.cuh): the 1-CTA and CTA-pair modes, bf16 and fp32
+// output. Compiled once per mode; the host library reaches them through the
+// functions below.
+#include "launch.cuh"
+
+#ifndef TPG_EPI
+#error "compile with -DTPG_EPI=<0..4>"
+#endif
+#define TPG_CAT2(a, b) a##b
+#define TPG_CAT(a, b) TPG_CAT2(a, b)
+
+namespace tpg {
+
+namespace {
+template <bool kOutF32, bool kPair>
+bool set_limit() {
+    return cudaFuncSetAttribute(tiled::gemm_tiled_kernel<kOutF32, kPair, TPG_EPI>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                static_cast<int>(tiled::Layout<kPair>::SMEM_BYTES)) == cudaSuccess;
+}
+template <bool kOutF32, bool kPair>
+cudaError_t launch_one(const TiledLaunch &l) {
+    return launch_ex(tiled::gemm_tiled_kernel<kOutF32, kPair, TPG_EPI>, l.grid, tiled::THREADS, l.smem,
+                     kPair ? 2 : 1, true, l.stream, *l.a, *l.b, *l.c, *l.d, *l.p);
+}
+} // namespace
+
+cudaError_t TPG_CAT(tiled_launch_e, TPG_EPI)(const TiledLaunch &l) {
+    if (l.pair) return l.f32 ? launch_one<true, true>(l) : launch_one<false, true>(l);
+    return l.f32 ? launch_one<true, false>(l) : launch_one<false, false>(l);
+}
+
+bool TPG_CAT(tiled_set_limits_e, TPG_EPI)() {
+    bool ok = set_limit<false, false>();
+    ok = set_limit<true, false>() && ok;
+    ok = set_limit<false, true>() && ok;
+    ok = set_limit<true, true>() && ok;
+    return ok;
+}
+
+#if TPG_EPI == 0
+int tiled_pair_clusters(bool f32, int num_sms) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * (num_sms / 2), 1, 1);
+    cfg.blockDim = dim3(tiled::THREADS, 1, 1);
+    cfg.dynamicSmemBytes = tiled::Layout<true>::SMEM_BYTES;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    const cudaError_t e =
+        f32 ? cudaOccupancyMaxActiveClusters(&n, tiled::gemm_tiled_kernel<true, true, 0>, &cfg)
+            : cudaOccupancyMaxActiveClusters(&n, tiled::gemm_tiled_kernel<false, true, 0>, &cfg);
+    if (e != cudaSuccess) {
+        (void)cudaGetLastError();
+        return -1;
+    }
+    return n;
+}
+#endif
+
+} // namespace tpg

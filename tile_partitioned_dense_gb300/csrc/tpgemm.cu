@@ -15,8 +15,7 @@
 #include "tpgemm.h"
 
 #include "aux_kernels.cuh"
-#include "gemm_stream.cuh"
-#include "gemm_tiled.cuh"
+#include "launch.cuh"
 #include "schedule.cuh"
 
 namespace {
@@ -104,51 +103,17 @@ int encode_2d(tpgemm_handle *h, CUtensorMap *map, CUtensorMapDataType dt, const 
 int stream_clusters_for(tpgemm_handle *h, bool f32, int mt, int stages) {
     int &slot = h->stream_clusters[f32 ? 1 : 0][mt / 16 - 1];
     if (slot > 0) return slot;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(2 * (h->num_sms / 2), 1, 1);
-    cfg.blockDim = dim3(tpg::stream::THREADS, 1, 1);
-    cfg.dynamicSmemBytes = tpg::stream::smem_bytes(mt, stages, 2);
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    int n = 0;
-    cudaError_t e = f32 ? cudaOccupancyMaxActiveClusters(&n, tpg::stream::gemm_stream_kernel<true, 2>, &cfg)
-                        : cudaOccupancyMaxActiveClusters(&n, tpg::stream::gemm_stream_kernel<false, 2>, &cfg);
-    if (e != cudaSuccess || n <= 0) {
-        (void)cudaGetLastError();
-        n = h->num_sms / 2;
-    }
-    slot = n;
-    return n;
+    const int n = tpg::stream_split_clusters(f32, h->num_sms, static_cast<int>(tpg::stream::smem_bytes(mt, stages, 2)));
+    slot = n > 0 ? n : h->num_sms / 2;
+    return slot;
 }
 
 int pair_clusters_for(tpgemm_handle *h, bool f32) {
     int &slot = h->pair_clusters[f32 ? 1 : 0];
     if (slot > 0) return slot;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(2 * (h->num_sms / 2), 1, 1);
-    cfg.blockDim = dim3(tpg::tiled::THREADS, 1, 1);
-    cfg.dynamicSmemBytes = tpg::tiled::Layout<true>::SMEM_BYTES;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    int n = 0;
-    cudaError_t e = f32 ? cudaOccupancyMaxActiveClusters(&n, tpg::tiled::gemm_tiled_kernel<true, true>, &cfg)
-                        : cudaOccupancyMaxActiveClusters(&n, tpg::tiled::gemm_tiled_kernel<false, true>, &cfg);
-    if (e != cudaSuccess || n <= 0) {
-        (void)cudaGetLastError();
-        n = h->num_sms / 2;
-    }
-    slot = n;
-    return n;
+    const int n = tpg::tiled_pair_clusters(f32, h->num_sms);
+    slot = n > 0 ? n : h->num_sms / 2;
+    return slot;
 }
 
 Plan make_plan(tpgemm_handle *h, int64_t M, int64_t N, int64_t K, int out_dtype) {
@@ -211,42 +176,74 @@ Plan make_plan(tpgemm_handle *h, int64_t M, int64_t N, int64_t K, int out_dtype)
     return pl;
 }
 
-// Launches `kernel`. With pdl, the launch allows programmatic dependent launch:
-// the kernel may start its on-chip prologue while the previous kernel in the
-// stream finishes, and waits (griddepcontrol.wait) before touching global
-// memory; only the GEMM kernels, which do that wait, are launched this way.
+// Launches one of the small kernels of this file (no PDL, no cluster).
 template <typename Kernel, typename... Args>
-int launch_ex(Kernel kernel, int grid, int block, int smem, int cluster, bool pdl, cudaStream_t stream,
-              Args... args) {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
-    cfg.blockDim = dim3(static_cast<unsigned>(block), 1, 1);
-    cfg.dynamicSmemBytes = static_cast<size_t>(smem);
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[2];
-    unsigned n = 0;
-    if (cluster > 1) {
-        attr[n].id = cudaLaunchAttributeClusterDimension;
-        attr[n].val.clusterDim.x = static_cast<unsigned>(cluster);
-        attr[n].val.clusterDim.y = 1;
-        attr[n].val.clusterDim.z = 1;
-        ++n;
+int launch(Kernel kernel, int grid, int block, int smem, int cluster, cudaStream_t stream, Args... args) {
+    return tpg::launch_ex(kernel, grid, block, smem, cluster, false, stream, args...) == cudaSuccess
+               ? TPGEMM_OK
+               : TPGEMM_ERR_CUDA;
+}
+
+// Opts every GEMM instantiation into its dynamic shared-memory size (current device).
+bool set_smem_limits() {
+    bool ok = tpg::tiled_set_limits_e0();
+    ok = tpg::tiled_set_limits_e1() && ok;
+    ok = tpg::tiled_set_limits_e2() && ok;
+    ok = tpg::tiled_set_limits_e3() && ok;
+    ok = tpg::tiled_set_limits_e4() && ok;
+    ok = tpg::stream_set_limits() && ok;
+    return ok;
+}
+
+// Argument checks of the fused epilogue (see tpgemm_epilogue).
+int check_epilogue(int64_t M, int64_t N, const void *D, int64_t ldd, int out_dtype, const tpgemm_epilogue *e) {
+    if (!e) return TPGEMM_OK;
+    if (e->activation < TPGEMM_ACT_NONE || e->activation > TPGEMM_ACT_TANH) return TPGEMM_ERR_INVALID_ARG;
+    const int64_t elt = out_dtype == TPGEMM_OUT_F32 ? 4 : 2;
+    const Range rd = byte_range(D, M, N, ldd, elt);
+    if (e->bias) {
+        if (e->bias_dtype != TPGEMM_OUT_BF16 && e->bias_dtype != TPGEMM_OUT_F32) return TPGEMM_ERR_INVALID_ARG;
+        if (!aligned16(e->bias)) return TPGEMM_ERR_ALIGNMENT;
+        if (overlaps(rd, byte_range(e->bias, 1, N, N, e->bias_dtype == TPGEMM_OUT_F32 ? 4 : 2)))
+            return TPGEMM_ERR_OVERLAP;
     }
-    if (pdl) {
-        attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-        attr[n].val.programmaticStreamSerializationAllowed = 1;
-        ++n;
+    if (e->aux) {
+        if (e->ldaux < N) return TPGEMM_ERR_INVALID_ARG;
+        if (!aligned16(e->aux) || (M > 1 && (e->ldaux * elt) % 16 != 0)) return TPGEMM_ERR_ALIGNMENT;
+        if (!(e->aux == D && e->ldaux == ldd) && overlaps(rd, byte_range(e->aux, M, N, e->ldaux, elt)))
+            return TPGEMM_ERR_OVERLAP;
     }
-    cfg.attrs = n ? attr : nullptr;
-    cfg.numAttrs = n;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, args...);
+    return TPGEMM_OK;
+}
+
+tpg::EpiParams epi_params(const tpgemm_epilogue *e) {
+    tpg::EpiParams p{};
+    if (e) {
+        p.bias = e->bias;
+        p.bias_f32 = e->bias_dtype == TPGEMM_OUT_F32 ? 1 : 0;
+        p.act = e->activation;
+        p.aux = e->aux;
+        p.ldaux = e->ldaux;
+    }
+    return p;
+}
+
+// Launches the tiled kernel in fused-epilogue mode `mode` (0 plain, 1 + activation).
+int launch_tiled(int mode, const tpg::TiledLaunch &l) {
+    cudaError_t e;
+    switch (mode) {
+    case 1: e = tpg::tiled_launch_e1(l); break;
+    case 2: e = tpg::tiled_launch_e2(l); break;
+    case 3: e = tpg::tiled_launch_e3(l); break;
+    case 4: e = tpg::tiled_launch_e4(l); break;
+    default: e = tpg::tiled_launch_e0(l); break;
+    }
     return e == cudaSuccess ? TPGEMM_OK : TPGEMM_ERR_CUDA;
 }
 
-template <typename Kernel, typename... Args>
-int launch(Kernel kernel, int grid, int block, int smem, int cluster, cudaStream_t stream, Args... args) {
-    return launch_ex(kernel, grid, block, smem, cluster, false, stream, args...);
-}
+int run_impl(tpgemm_handle *h, int64_t M, int64_t N, int64_t K, const void *A, int64_t lda, const void *B,
+             int64_t ldb, const void *C, int64_t ldc, void *D, int64_t ldd, float alpha, float beta, int out_dtype,
+             const tpgemm_epilogue *epi, void *stream_ptr);
 
 } // namespace
 
@@ -297,25 +294,7 @@ int gemm_create(tpgemm_handle **out, int device) {
         return TPGEMM_ERR_CUDA;
     }
     h->encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
-    bool ok = true;
-    ok &= cudaFuncSetAttribute(tpg::tiled::gemm_tiled_kernel<false, false>,
-                               cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               static_cast<int>(tpg::tiled::Layout<false>::SMEM_BYTES)) == cudaSuccess;
-    ok &= cudaFuncSetAttribute(tpg::tiled::gemm_tiled_kernel<true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               static_cast<int>(tpg::tiled::Layout<false>::SMEM_BYTES)) == cudaSuccess;
-    ok &= cudaFuncSetAttribute(tpg::tiled::gemm_tiled_kernel<false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               static_cast<int>(tpg::tiled::Layout<true>::SMEM_BYTES)) == cudaSuccess;
-    ok &= cudaFuncSetAttribute(tpg::tiled::gemm_tiled_kernel<true, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               static_cast<int>(tpg::tiled::Layout<true>::SMEM_BYTES)) == cudaSuccess;
-    const int stream_smem = static_cast<int>(tpg::stream::SMEM_LIMIT);
-    ok &= cudaFuncSetAttribute(tpg::stream::gemm_stream_kernel<false, 1>,
-                               cudaFuncAttributeMaxDynamicSharedMemorySize, stream_smem) == cudaSuccess;
-    ok &= cudaFuncSetAttribute(tpg::stream::gemm_stream_kernel<true, 1>,
-                               cudaFuncAttributeMaxDynamicSharedMemorySize, stream_smem) == cudaSuccess;
-    ok &= cudaFuncSetAttribute(tpg::stream::gemm_stream_kernel<false, 2>,
-                               cudaFuncAttributeMaxDynamicSharedMemorySize, stream_smem) == cudaSuccess;
-    ok &= cudaFuncSetAttribute(tpg::stream::gemm_stream_kernel<true, 2>,
-                               cudaFuncAttributeMaxDynamicSharedMemorySize, stream_smem) == cudaSuccess;
+    const bool ok = set_smem_limits();
     if (!ok || cudaMalloc(&h->status, sizeof(uint64_t)) != cudaSuccess ||
         cudaMemset(h->status, 0, sizeof(uint64_t)) != cudaSuccess) {
         (void)cudaGetLastError();
@@ -421,9 +400,28 @@ int gemm_check_args(int64_t M, int64_t N, int64_t K, const void *A, int64_t lda,
 int gemm_run(tpgemm_handle *h, int64_t M, int64_t N, int64_t K, const void *A, int64_t lda, const void *B,
              int64_t ldb, const void *C, int64_t ldc, void *D, int64_t ldd, float alpha, float beta,
              int out_dtype, void *stream_ptr) {
+    return run_impl(h, M, N, K, A, lda, B, ldb, C, ldc, D, ldd, alpha, beta, out_dtype, nullptr, stream_ptr);
+}
+
+int gemm_run_epilogue(tpgemm_handle *h, int64_t M, int64_t N, int64_t K, const void *A, int64_t lda,
+                      const void *B, int64_t ldb, const void *C, int64_t ldc, void *D, int64_t ldd, float alpha,
+                      float beta, int out_dtype, const tpgemm_epilogue *epi, void *stream_ptr) {
+    return run_impl(h, M, N, K, A, lda, B, ldb, C, ldc, D, ldd, alpha, beta, out_dtype, epi, stream_ptr);
+}
+
+} // extern "C"
+
+namespace {
+
+int run_impl(tpgemm_handle *h, int64_t M, int64_t N, int64_t K, const void *A, int64_t lda, const void *B,
+             int64_t ldb, const void *C, int64_t ldc, void *D, int64_t ldd, float alpha, float beta, int out_dtype,
+             const tpgemm_epilogue *epi, void *stream_ptr) {
     if (!h) return TPGEMM_ERR_INVALID_ARG;
-    const int chk = gemm_check_args(M, N, K, A, lda, B, ldb, C, ldc, D, ldd, beta, out_dtype);
+    int chk = gemm_check_args(M, N, K, A, lda, B, ldb, C, ldc, D, ldd, beta, out_dtype);
+    if (chk == TPGEMM_OK && M > 0 && N > 0) chk = check_epilogue(M, N, D, ldd, out_dtype, epi);
     if (chk != TPGEMM_OK || M == 0 || N == 0) return chk;
+    const bool fused = epi && (epi->bias || epi->aux || epi->activation != TPGEMM_ACT_NONE);
+    const tpg::EpiParams ep = epi_params(epi);
     const int64_t elt = out_dtype == TPGEMM_OUT_F32 ? 4 : 2;
     const bool use_c = beta != 0.0f;
 
@@ -435,9 +433,15 @@ int gemm_run(tpgemm_handle *h, int64_t M, int64_t N, int64_t K, const void *A, i
     if (pl.variant == TPGEMM_VARIANT_EPILOGUE_ONLY) {
         const int32_t m = static_cast<int32_t>(M), n = static_cast<int32_t>(N);
         const void *c = use_c ? C : nullptr;
-        return f32 ? launch(tpg::epilogue_only_kernel<true>, pl.grid, 256, 0, 1, stream, m, n, beta, c, ldc, D, ldd)
-                   : launch(tpg::epilogue_only_kernel<false>, pl.grid, 256, 0, 1, stream, m, n, beta, c, ldc, D,
-                            ldd);
+        if (fused)
+            return f32 ? launch(tpg::epilogue_only_kernel<true, true>, pl.grid, 256, 0, 1, stream, m, n, beta, c, ldc,
+                                D, ldd, ep)
+                       : launch(tpg::epilogue_only_kernel<false, true>, pl.grid, 256, 0, 1, stream, m, n, beta, c,
+                                ldc, D, ldd, ep);
+        return f32 ? launch(tpg::epilogue_only_kernel<true, false>, pl.grid, 256, 0, 1, stream, m, n, beta, c, ldc, D,
+                            ldd, ep)
+                   : launch(tpg::epilogue_only_kernel<false, false>, pl.grid, 256, 0, 1, stream, m, n, beta, c, ldc,
+                            D, ldd, ep);
     }
 
     const CUtensorMapDataType out_dt = f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
@@ -472,16 +476,10 @@ int gemm_run(tpgemm_handle *h, int64_t M, int64_t N, int64_t K, const void *A, i
         p.ldd = ldd;
         p.status = h->status;
         p.timeout_ns = h->timeout_ns;
-        const int thr = tpg::tiled::THREADS;
-        if (pl.variant == TPGEMM_VARIANT_TILED_PAIR)
-            return f32 ? launch_ex(tpg::tiled::gemm_tiled_kernel<true, true>, pl.grid, thr, pl.smem, 2, true, stream,
-                                   tmA, tmB, tmC, tmD, p)
-                       : launch_ex(tpg::tiled::gemm_tiled_kernel<false, true>, pl.grid, thr, pl.smem, 2, true, stream,
-                                   tmA, tmB, tmC, tmD, p);
-        return f32 ? launch_ex(tpg::tiled::gemm_tiled_kernel<true, false>, pl.grid, thr, pl.smem, 1, true, stream, tmA,
-                               tmB, tmC, tmD, p)
-                   : launch_ex(tpg::tiled::gemm_tiled_kernel<false, false>, pl.grid, thr, pl.smem, 1, true, stream,
-                               tmA, tmB, tmC, tmD, p);
+        p.epi = ep;
+        const tpg::TiledLaunch l{pl.grid, pl.smem, pl.variant == TPGEMM_VARIANT_TILED_PAIR, f32, stream,
+                                 &tmA, &tmB, &tmC, &tmD, &p};
+        return launch_tiled(fused ? 1 + ep.act : 0, l);
     }
 
     // weight-streaming variant
@@ -505,16 +503,14 @@ int gemm_run(tpgemm_handle *h, int64_t M, int64_t N, int64_t K, const void *A, i
     p.ldd = ldd;
     p.status = h->status;
     p.timeout_ns = h->timeout_ns;
-    if (pl.split == 2)
-        return f32 ? launch_ex(tpg::stream::gemm_stream_kernel<true, 2>, pl.grid, tpg::stream::THREADS, pl.smem, 2,
-                               true, stream, tmA, tmB, p)
-                   : launch_ex(tpg::stream::gemm_stream_kernel<false, 2>, pl.grid, tpg::stream::THREADS, pl.smem, 2,
-                               true, stream, tmA, tmB, p);
-    return f32 ? launch_ex(tpg::stream::gemm_stream_kernel<true, 1>, pl.grid, tpg::stream::THREADS, pl.smem, 1, true,
-                           stream, tmA, tmB, p)
-               : launch_ex(tpg::stream::gemm_stream_kernel<false, 1>, pl.grid, tpg::stream::THREADS, pl.smem, 1, true,
-                           stream, tmA, tmB, p);
+    p.epi = ep;
+    const tpg::StreamLaunch l{pl.grid, pl.smem, pl.split, f32, fused, stream, &tmA, &tmB, &p};
+    return tpg::stream_launch(l) == cudaSuccess ? TPGEMM_OK : TPGEMM_ERR_CUDA;
 }
+
+} // namespace
+
+extern "C" {
 
 int gemm_sync_status(tpgemm_handle *h, void *stream) {
     if (!h) return TPGEMM_ERR_INVALID_ARG;
@@ -598,12 +594,7 @@ int noalloc_setup(int dev, NoallocDevice **out) {
                 cudaSuccess ||
             q != cudaDriverEntryPointSuccess || !fn)
             return TPGEMM_ERR_CUDA;
-        if (cudaFuncSetAttribute(tpg::tiled::gemm_tiled_kernel<false, false>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(tpg::tiled::SMEM_BYTES)) != cudaSuccess ||
-            cudaFuncSetAttribute(tpg::tiled::gemm_tiled_kernel<true, false>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(tpg::tiled::SMEM_BYTES)) != cudaSuccess ||
+        if (!tpg::tiled_set_limits_e0() ||
             cudaMemset(ptr, 0, sizeof(uint32_t) * kNoallocStatusWords) != cudaSuccess) {
             (void)cudaGetLastError();
             return TPGEMM_ERR_CUDA;
@@ -655,10 +646,11 @@ extern "C" int gemm_run_noalloc(int64_t M, int64_t N, int64_t K, const void *A, 
         if (blocks > 8LL * nd->num_sms) blocks = 8LL * nd->num_sms;
         const int32_t m = static_cast<int32_t>(M), n = static_cast<int32_t>(N);
         const void *c = use_c ? C : nullptr;
-        rc = f32 ? launch(tpg::epilogue_only_kernel<true>, static_cast<int>(blocks), 256, 0, 1, stream, m, n, beta, c,
-                          ldc, D, ldd)
-                 : launch(tpg::epilogue_only_kernel<false>, static_cast<int>(blocks), 256, 0, 1, stream, m, n, beta,
-                          c, ldc, D, ldd);
+        const tpg::EpiParams none{};
+        rc = f32 ? launch(tpg::epilogue_only_kernel<true, false>, static_cast<int>(blocks), 256, 0, 1, stream, m, n,
+                          beta, c, ldc, D, ldd, none)
+                 : launch(tpg::epilogue_only_kernel<false, false>, static_cast<int>(blocks), 256, 0, 1, stream, m, n,
+                          beta, c, ldc, D, ldd, none);
     } else {
         // The status word must start at zero: every call shares it.
         if (cudaMemsetAsync(nd->status, 0, sizeof(uint32_t), stream) != cudaSuccess) return TPGEMM_ERR_CUDA;
@@ -696,11 +688,9 @@ extern "C" int gemm_run_noalloc(int64_t M, int64_t N, int64_t K, const void *A, 
         p.ldd = ldd;
         p.status = nd->status;
         p.timeout_ns = 2000000000ull;
-        const int smem = static_cast<int>(tpg::tiled::SMEM_BYTES);
-        rc = f32 ? launch(tpg::tiled::gemm_tiled_kernel<true, false>, grid, tpg::tiled::THREADS, smem, 1, stream, tmA,
-                          tmB, tmC, tmD, p)
-                 : launch(tpg::tiled::gemm_tiled_kernel<false, false>, grid, tpg::tiled::THREADS, smem, 1, stream,
-                          tmA, tmB, tmC, tmD, p);
+        const tpg::TiledLaunch l{grid, static_cast<int>(tpg::tiled::SMEM_BYTES), false, f32, stream,
+                                 &tmA, &tmB, &tmC, &tmD, &p};
+        rc = tpg::tiled_launch_e0(l) == cudaSuccess ? TPGEMM_OK : TPGEMM_ERR_CUDA;
     }
     if (rc != TPGEMM_OK || !check_status) return rc;
     if (cudaStreamSynchronize(stream) != cudaSuccess) return TPGEMM_ERR_CUDA;
