@@ -187,6 +187,35 @@ class Workload:
                             c.alpha, c.beta, self.out_code, stream)
 
 
+class MultiWorkload:
+    """Batched (bmm) or grouped (mixture-of-experts) GEMM through
+    gemm_run_batched / gemm_run_grouped, with rotating device copies."""
+
+    def __init__(self, torch, l2_bytes, kind, M, N, K, count, group_rows=None):
+        g = torch.Generator().manual_seed(77)
+        self.kind, self.M, self.N, self.K, self.count = kind, M, N, K, count
+        self.group_rows = group_rows
+        rows = M * count if kind == "bmm" else sum(group_rows)
+        self.rows = rows
+        a = (torch.randn(rows, K, generator=g)).to(torch.bfloat16)
+        b = (torch.randn(count, K, N, generator=g) * 0.02).to(torch.bfloat16)
+        per_set = a.numel() * 2 + b.numel() * 2 + rows * N * 2
+        self.nsets = max(2, -(-3 * l2_bytes // per_set) + 1)
+        self.sets = [{"A": a.cuda(), "B": b.cuda(), "D": torch.empty(rows, N, dtype=torch.bfloat16, device="cuda")}
+                     for _ in range(self.nsets)]
+        self.flops = 2 * rows * N * K
+
+    def run(self, tpd, h, i, stream):
+        s = self.sets[i % self.nsets]
+        if self.kind == "bmm":
+            return tpd.gemm_run_batched(h, self.count, self.M, self.N, self.K, s["A"].data_ptr(), self.K,
+                                        self.M * self.K, s["B"].data_ptr(), self.N, self.K * self.N, None, self.N, 0,
+                                        s["D"].data_ptr(), self.N, self.M * self.N, 1.0, 0.0, 0, stream)
+        return tpd.gemm_run_grouped(h, self.group_rows, self.N, self.K, s["A"].data_ptr(), self.K, s["B"].data_ptr(),
+                                    self.N, self.K * self.N, None, self.N, s["D"].data_ptr(), self.N, 1.0, 0.0, 0,
+                                    stream)
+
+
 class FusedWorkload(Workload):
     """A workload whose epilogue adds a bias row, applies an activation and
     multiplies by an auxiliary [M, N] tensor: fused into gemm_run_epilogue, or
@@ -463,6 +492,24 @@ def run_ours(args):
             "config": {"workload": "qkv shape, D = sigmoid(A*B + bias) * aux, bf16; unfused = gemm_run then "
                                    "torch sigmoid(D + bias) * aux in the same graph", "M": c2.M, "N": c2.N, "K": c2.K}}
         launches += 200
+        # batched and grouped GEMM: 8 x 2048^3 and 8 experts of uneven size (8192 rows, 4096 x 4096)
+        peak = peaks["bf16_tflops"]
+        moe_rows = [512, 1024, 768, 2048, 256, 1536, 1024, 1024]
+        for name, wl2, desc in [
+                ("bmm_8x2048", MultiWorkload(torch, l2, "bmm", 2048, 2048, 2048, 8), "batched GEMM, 8 x 2048x2048x2048, bf16"),
+                ("grouped_moe8", MultiWorkload(torch, l2, "grouped", 0, 4096, 4096, 8, moe_rows),
+                 f"grouped GEMM, 8 experts with rows {moe_rows} (8192 total), N = K = 4096, bf16")]:
+            span2, eager2 = time_launches(torch, tpd, h, wl2, 100, 5, barrier)
+            ms2 = span2 / 100
+            v2 = wl2.flops / (ms2 * 1e-3) / 1e12
+            per_config[name] = {"value": round(v2, 2), "unit": "TFLOP/s", "ms_per_step": round(ms2, 5),
+                                "eager_ms_per_step": round(eager2 / 100, 5),
+                                "roofline": {"bound": "tensor", "achieved": round(v2, 2), "peak": peak,
+                                             "unit": "TFLOP/s", "frac": round(v2 / peak, 4)},
+                                "config": {"workload": desc}}
+            launches += 100
+            del wl2
+            torch.cuda.empty_cache()
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

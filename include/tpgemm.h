@@ -154,6 +154,44 @@ int gemm_run_epilogue(tpgemm_handle *h, int64_t M, int64_t N, int64_t K, const v
                       const tpgemm_epilogue *epi, void *stream);
 
 /*
+ * Batched GEMM ("TorchInductor ganha suporte a GEMMs de alta performance com
+ * CuteDSL", the enablement paragraph: NVGEMM covers mm, bmm, scaled_mm and
+ * grouped_mm). For b in [0, batch):
+ *     D_b = alpha * A_b * B_b + beta * C_b,   X_b = X + b * strideX (elements)
+ * with every slice laid out as in gemm_run. A stride of 0 shares one slice of
+ * A, B or C between all batches (e.g. one weight for every batch); D's slices
+ * must not overlap (strideD >= (M-1)*ldd + N when batch > 1). Strides times
+ * the element size must be multiples of 16 bytes. Runs the tiled kernel over
+ * all batches' tiles in one launch. batch == 0 enqueues nothing.
+ * Errors as gemm_run; overlap is checked over all slices.
+ */
+int gemm_run_batched(tpgemm_handle *h, int64_t batch, int64_t M, int64_t N, int64_t K,
+                     const void *A, int64_t lda, int64_t strideA, const void *B, int64_t ldb,
+                     int64_t strideB, const void *C, int64_t ldc, int64_t strideC, void *D,
+                     int64_t ldd, int64_t strideD, float alpha, float beta, int out_dtype,
+                     void *stream);
+
+/* Most groups gemm_run_grouped takes. */
+#define TPGEMM_MAX_GROUPS 256
+
+/*
+ * Grouped GEMM (grouped_mm of the same paragraph), as in a mixture-of-experts
+ * layer: group g owns rows [r_g, r_g + group_rows[g]) of A [R, K], C and D
+ * [R, N], stacked in group order (r_0 = 0, r_{g+1} = r_g + group_rows[g],
+ * R = sum of group_rows), and its own weight B_g = B + g * strideB, a [K, N]
+ * matrix with row stride ldb:
+ *     D[r_g + i, :] = alpha * A[r_g + i, :] * B_g + beta * C[r_g + i, :]
+ * group_rows is a host array of `groups` non-negative counts (empty groups are
+ * allowed); groups <= TPGEMM_MAX_GROUPS. Every output row belongs to exactly
+ * one group and is written by exactly one CTA. Layout, alignment and error
+ * rules as gemm_run (strideB * 2 a multiple of 16 bytes when groups > 1).
+ */
+int gemm_run_grouped(tpgemm_handle *h, int64_t groups, const int64_t *group_rows, int64_t N,
+                     int64_t K, const void *A, int64_t lda, const void *B, int64_t ldb,
+                     int64_t strideB, const void *C, int64_t ldc, void *D, int64_t ldd, float alpha,
+                     float beta, int out_dtype, void *stream);
+
+/*
  * Synchronises `stream`, then reads and clears the handle's device status
  * word. Returns TPGEMM_OK, TPGEMM_ERR_TIMEOUT if any kernel since the last
  * call gave up on a pipeline wait (its output is then incomplete), or

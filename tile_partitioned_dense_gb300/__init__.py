@@ -66,6 +66,10 @@ def load_library() -> ctypes.CDLL:
             "gemm_create": (i32, [ctypes.POINTER(vp), i32]),
             "gemm_run": (i32, [vp, i64, i64, i64, vp, i64, vp, i64, vp, i64, vp, i64, f32, f32, i32, vp]),
             "gemm_sync_status": (i32, [vp, vp]),
+            "gemm_run_batched": (i32, [vp, i64, i64, i64, i64, vp, i64, i64, vp, i64, i64, vp, i64, i64, vp, i64,
+                                       i64, f32, f32, i32, vp]),
+            "gemm_run_grouped": (i32, [vp, i64, pi64, i64, i64, vp, i64, vp, i64, i64, vp, i64, vp, i64, f32, f32,
+                                       i32, vp]),
             "gemm_run_epilogue": (i32, [vp, i64, i64, i64, vp, i64, vp, i64, vp, i64, vp, i64, f32, f32, i32,
                                         ctypes.POINTER(Epilogue), vp]),
             "gemm_check_args": (i32, [i64, i64, i64, vp, i64, vp, i64, vp, i64, vp, i64, f32, i32]),
@@ -106,6 +110,20 @@ def gemm_run_epilogue(h, M, N, K, A, lda, B, ldb, C, ldc, D, ldd, alpha, beta, o
     """epi: an Epilogue or None (plain gemm_run)."""
     return load_library().gemm_run_epilogue(h, M, N, K, A, lda, B, ldb, C, ldc, D, ldd, alpha, beta,
                                             out_dtype, ctypes.byref(epi) if epi is not None else None, stream)
+
+
+def gemm_run_batched(h, batch, M, N, K, A, lda, strideA, B, ldb, strideB, C, ldc, strideC, D, ldd, strideD,
+                     alpha, beta, out_dtype, stream) -> int:
+    return load_library().gemm_run_batched(h, batch, M, N, K, A, lda, strideA, B, ldb, strideB, C, ldc, strideC,
+                                           D, ldd, strideD, alpha, beta, out_dtype, stream)
+
+
+def gemm_run_grouped(h, group_rows, N, K, A, lda, B, ldb, strideB, C, ldc, D, ldd, alpha, beta, out_dtype,
+                     stream) -> int:
+    """group_rows: a sequence of per-group row counts (host)."""
+    rows = (ctypes.c_int64 * max(len(group_rows), 1))(*[int(r) for r in group_rows])
+    return load_library().gemm_run_grouped(h, len(group_rows), rows, N, K, A, lda, B, ldb, strideB, C, ldc, D, ldd,
+                                           alpha, beta, out_dtype, stream)
 
 
 def gemm_sync_status(h, stream=None) -> int:

@@ -35,6 +35,8 @@
 
 #include <cuda_bf16.h>
 
+#include <type_traits>
+
 #include "epilogue.cuh"
 #include "ptx.cuh"
 #include "schedule.cuh"
@@ -42,9 +44,12 @@
 namespace tpg {
 
 struct TiledParams {
-    int32_t M, N, K;
-    int32_t kb; // 64-wide K blocks
-    Schedule sched;
+    int32_t M, N, K; // M: rows per batch (uniform batches); grouped: unused
+    int32_t kb;      // 64-wide K blocks
+    Schedule sched;  // over all tile rows of all batches or groups
+    int32_t mt_batch; // tile rows per batch (uniform batches)
+    int32_t a_bcast, b_bcast, c_bcast; // 1: the operand has a single batch slice shared by all
+    int64_t sC, sD;  // batch strides of C and D in elements (plain-store paths)
     // Columns [0, n_tma) of C and D go through the tensor maps; n_tma is N
     // rounded down to a multiple of 16 bytes, because a TMA store writes whole
     // 16-byte cells of the innermost dimension even past its bound. The last
@@ -59,6 +64,60 @@ struct TiledParams {
     uint64_t timeout_ns;
     EpiParams epi; // read only by the fused-epilogue instantiations
 };
+
+// Grouped GEMM (one B slice per group, the groups' rows stacked in A, C and
+// D, as for mixture-of-experts layers): the group table travels as a kernel
+// argument of the grouped instantiations only.
+constexpr int kMaxGroups = 256;
+struct GroupTable {
+    int32_t groups;
+    int32_t tile_prefix[kMaxGroups + 1]; // tile rows of the groups before g
+    int32_t row_start[kMaxGroups];       // first row of group g in A, C and D
+    int32_t rows[kMaxGroups];            // rows of group g
+};
+struct NoGroups {
+    int32_t unused;
+};
+template <bool kGrouped>
+using SegArg = typename std::conditional<kGrouped, GroupTable, NoGroups>::type;
+
+// Where the tile row `tile_row` (of rows_per_tile rows) lives: the batch slice
+// of A/C/D and of B, its first row and how many rows of the segment remain
+// from there (more than the tile when the segment continues).
+struct Segment {
+    int32_t ab, bb, row0, rows_left;
+};
+
+template <bool kGrouped>
+__device__ __forceinline__ Segment segment_of(int32_t tile_row, int32_t rows_per_tile, const TiledParams &p,
+                                              const SegArg<kGrouped> &seg) {
+    Segment s;
+    if constexpr (kGrouped) {
+        // the last group whose first tile row is <= tile_row (empty groups are skipped
+        // because a later group with the same prefix wins)
+        int32_t lo = 0, hi = seg.groups - 1;
+        while (lo < hi) {
+            const int32_t mid = (lo + hi + 1) >> 1;
+            if (seg.tile_prefix[mid] <= tile_row)
+                lo = mid;
+            else
+                hi = mid - 1;
+        }
+        const int32_t local = tile_row - seg.tile_prefix[lo];
+        s.ab = 0;
+        s.bb = lo;
+        s.row0 = seg.row_start[lo] + local * rows_per_tile;
+        s.rows_left = seg.rows[lo] - local * rows_per_tile;
+    } else {
+        const int32_t b = tile_row / p.mt_batch;
+        const int32_t local = tile_row - b * p.mt_batch;
+        s.ab = b;
+        s.bb = b;
+        s.row0 = local * rows_per_tile;
+        s.rows_left = p.M - local * rows_per_tile;
+    }
+    return s;
+}
 
 namespace tiled {
 
@@ -113,11 +172,11 @@ __device__ __forceinline__ void settle(uint64_t ns) {
 // kEpi: 0 plain alpha*acc + beta*C; 1 + activation for the fused epilogue
 // (bias and aux are runtime options; the activation is compiled in, so each
 // instantiation carries only its own math).
-template <bool kOutF32, bool kPair, int kEpi>
+template <bool kOutF32, bool kPair, int kEpi, bool kGrouped = false>
 __global__ void __launch_bounds__(THREADS, 1)
     gemm_tiled_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                       const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmD,
-                      const TiledParams p) {
+                      const TiledParams p, const __grid_constant__ SegArg<kGrouped> seg) {
     using L = Layout<kPair>;
     constexpr int STAGES = L::STAGES;
     constexpr int CHUNK = kOutF32 ? 32 : 64; // output columns per 128-byte staging row
@@ -195,7 +254,10 @@ __global__ void __launch_bounds__(THREADS, 1)
             bool ok = true;
             WorkItem w;
             for (int64_t t = worker; ok && work_item(p.sched, t, BN, w); t += workers) {
-                const int32_t m0 = w.m * (BM * CL) + static_cast<int32_t>(rank) * BM;
+                const Segment sg = segment_of<kGrouped>(w.m, BM * CL, p, seg);
+                const int32_t m0 = sg.row0 + static_cast<int32_t>(rank) * BM;
+                const int32_t ab = p.a_bcast ? 0 : sg.ab;
+                const int32_t bb = p.b_bcast ? 0 : sg.bb;
                 const int32_t cols = w.width / CL; // B columns this CTA stages
                 const int32_t nb = w.n + static_cast<int32_t>(rank) * cols;
                 const uint32_t tx = CL * (A_STAGE_BYTES + static_cast<uint32_t>(cols) * BK * 2);
@@ -210,14 +272,14 @@ __global__ void __launch_bounds__(THREADS, 1)
                     if constexpr (kPair) {
                         if (rank == 0) mbar_arrive_expect_tx(&full[stage], tx);
                         const uint32_t fb = full0 + stage * 8u;
-                        tma_load_2d_pair(&tmA, fb, adst, k0, m0);
+                        tma_load_3d_pair(&tmA, fb, adst, k0, m0, ab);
                         for (int c = 0; c < cols / 64; ++c)
-                            tma_load_2d_pair(&tmB, fb, bdst + c * B_BOX_BYTES, nb + c * 64, k0);
+                            tma_load_3d_pair(&tmB, fb, bdst + c * B_BOX_BYTES, nb + c * 64, k0, bb);
                     } else {
                         mbar_arrive_expect_tx(&full[stage], tx);
-                        tma_load_2d(&tmA, &full[stage], adst, k0, m0);
+                        tma_load_3d(&tmA, &full[stage], adst, k0, m0, ab);
                         for (int c = 0; c < cols / 64; ++c)
-                            tma_load_2d(&tmB, &full[stage], bdst + c * B_BOX_BYTES, nb + c * 64, k0);
+                            tma_load_3d(&tmB, &full[stage], bdst + c * B_BOX_BYTES, nb + c * 64, k0, bb);
                     }
                     ++issued;
                     if (++stage == STAGES) {
@@ -328,7 +390,14 @@ __global__ void __launch_bounds__(THREADS, 1)
         bool ok = true;
         WorkItem w;
         for (int64_t t = worker; ok && work_item(p.sched, t, BN, w); t += workers) {
-            const int32_t m0 = w.m * (BM * CL) + static_cast<int32_t>(rank) * BM;
+            const Segment sg = segment_of<kGrouped>(w.m, BM * CL, p, seg);
+            const int32_t m0 = sg.row0 + static_cast<int32_t>(rank) * BM; // first row of this CTA's rows
+            int32_t rows_valid = sg.rows_left - static_cast<int32_t>(rank) * BM;
+            rows_valid = rows_valid < 0 ? 0 : (rows_valid > BM ? BM : rows_valid);
+            // A tile that runs past its group's last row must not store through
+            // the D map (its rows would land in the next group): plain stores.
+            const bool direct_tile = kGrouped && rows_valid < BM;
+            const int32_t cab = p.c_bcast ? 0 : sg.ab;
             int nchunks = (p.N - w.n + CHUNK - 1) / CHUNK;
             if (nchunks > w.width / CHUNK) nchunks = w.width / CHUNK;
             if (p.N <= w.n) nchunks = 0;
@@ -357,13 +426,15 @@ __global__ void __launch_bounds__(THREADS, 1)
             for (int c = 0; c < nchunks; ++c) {
                 uint8_t *buf = epi + slot * EPI_BUF_BYTES;
                 const int32_t cb = w.n + c * CHUNK; // first column of this chunk
-                const bool chunk_tma = cb < p.n_tma;
+                const bool chunk_tma = cb < p.n_tma && !direct_tile;
                 // the ragged cell [n_tma, N) when it falls in this chunk, else -1
                 const int tail_cell = (p.N > p.n_tma && cb <= p.n_tma && p.n_tma < cb + CHUNK)
                                           ? (p.n_tma - cb) / (16 / (kOutF32 ? 4 : 2))
                                           : -1;
-                const int32_t grow = m0 + static_cast<int32_t>(row); // global row of this thread
-                const bool row_ok = grow < p.M;
+                const int32_t grow = m0 + static_cast<int32_t>(row); // row of this thread within its batch
+                const bool row_ok = static_cast<int32_t>(row) < rows_valid;
+                const int64_t crow = static_cast<int64_t>(cab) * p.sC + static_cast<int64_t>(grow) * p.ldc;
+                const int64_t drow = static_cast<int64_t>(sg.ab) * p.sD + static_cast<int64_t>(grow) * p.ldd;
                 // Fused epilogue: this row's aux cells for the chunk, all in flight at once,
                 // while the staging buffer frees up and C arrives.
                 uint4 auxq[8];
@@ -378,7 +449,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 if (has_beta && chunk_tma) {
                     if (leader) {
                         mbar_arrive_expect_tx(&cbar[slot], EPI_BUF_BYTES);
-                        tma_load_2d(&tmC, &cbar[slot], buf, cb, m0);
+                        tma_load_3d(&tmC, &cbar[slot], buf, cb, m0, cab);
                     }
                     const bool gotc = mbar_wait(&cbar[slot], (cphase >> slot) & 1u, ctl, kStatusTimeoutEpilogue);
                     if (named_barrier_or(1, EPI_THREADS, !gotc)) {
@@ -398,7 +469,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
                     uint4 *cell = reinterpret_cast<uint4 *>(rowp + ((j ^ (row & 7u)) << 4));
-                    const bool tail = j == tail_cell;
+                    const bool tail = direct_tile || j == tail_cell;
                     if constexpr (kOutF32) {
                         float v[4];
 #pragma unroll
@@ -409,13 +480,13 @@ __global__ void __launch_bounds__(THREADS, 1)
                             for (int e = 0; e < 4; ++e) {
                                 const int32_t col = cb + j * 4 + e;
                                 if (has_beta && row_ok && col < p.N)
-                                    v[e] = fmaf(p.beta, static_cast<const float *>(p.C)[grow * p.ldc + col], v[e]);
+                                    v[e] = fmaf(p.beta, static_cast<const float *>(p.C)[crow + col], v[e]);
                             }
                             if constexpr (kEpi > 0) epilogue_cell<4, true, kEpi - 1>(p.epi, p.N, grow, row_ok, cb + j * 4, v, auxq[j]);
 #pragma unroll
                             for (int e = 0; e < 4; ++e) {
                                 const int32_t col = cb + j * 4 + e;
-                                if (row_ok && col < p.N) static_cast<float *>(p.D)[grow * p.ldd + col] = v[e];
+                                if (row_ok && col < p.N) static_cast<float *>(p.D)[drow + col] = v[e];
                             }
                             continue;
                         }
@@ -441,7 +512,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                             for (int e = 0; e < 8; ++e) {
                                 const int32_t col = cb + j * 8 + e;
                                 if (has_beta && row_ok && col < p.N) {
-                                    const uint16_t cbits = static_cast<const uint16_t *>(p.C)[grow * p.ldc + col];
+                                    const uint16_t cbits = static_cast<const uint16_t *>(p.C)[crow + col];
                                     v[e] = fmaf(p.beta, __uint_as_float(static_cast<uint32_t>(cbits) << 16), v[e]);
                                 }
                             }
@@ -450,7 +521,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                             for (int e = 0; e < 8; ++e) {
                                 const int32_t col = cb + j * 8 + e;
                                 if (row_ok && col < p.N)
-                                    static_cast<uint16_t *>(p.D)[grow * p.ldd + col] =
+                                    static_cast<uint16_t *>(p.D)[drow + col] =
                                         static_cast<uint16_t>(pack_bf16x2(v[e], 0.0f) & 0xFFFFu);
                             }
                             continue;
@@ -472,7 +543,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 fence_proxy_async_smem();
                 named_barrier_sync(1, EPI_THREADS);
                 if (leader && chunk_tma) {
-                    tma_store_2d(&tmD, buf, cb, m0);
+                    tma_store_3d(&tmD, buf, cb, m0, sg.ab);
                     bulk_commit_group();
                 }
                 slot ^= 1u;

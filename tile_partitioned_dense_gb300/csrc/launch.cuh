@@ -58,6 +58,7 @@ struct TiledLaunch {
     cudaStream_t stream;
     const CUtensorMap *a, *b, *c, *d;
     const TiledParams *p;
+    const GroupTable *groups; // grouped GEMM only (tiled_launch_g0)
 };
 
 struct StreamLaunch {
@@ -82,6 +83,9 @@ bool tiled_set_limits_e1();
 bool tiled_set_limits_e2();
 bool tiled_set_limits_e3();
 bool tiled_set_limits_e4();
+// grouped GEMM (plain epilogue), from tiled_inst.cu with -DTPG_EPI=0 -DTPG_GROUPED=1
+cudaError_t tiled_launch_g0(const TiledLaunch &l);
+bool tiled_set_limits_g0();
 // co-resident CTA pairs of the pair-mode kernel (plain mode), or -1
 int tiled_pair_clusters(bool f32, int num_sms);
 

@@ -7,31 +7,46 @@
 #ifndef TPG_EPI
 #error "compile with -DTPG_EPI=<0..4>"
 #endif
+#ifndef TPG_GROUPED
+#define TPG_GROUPED 0
+#endif
 #define TPG_CAT2(a, b) a##b
 #define TPG_CAT(a, b) TPG_CAT2(a, b)
+#if TPG_GROUPED
+#define TPG_NAME(base) TPG_CAT(base, g0)
+#else
+#define TPG_NAME(base) TPG_CAT(base, TPG_CAT(e, TPG_EPI))
+#endif
 
 namespace tpg {
 
 namespace {
+constexpr bool kGrouped = TPG_GROUPED != 0;
+
 template <bool kOutF32, bool kPair>
 bool set_limit() {
-    return cudaFuncSetAttribute(tiled::gemm_tiled_kernel<kOutF32, kPair, TPG_EPI>,
+    return cudaFuncSetAttribute(tiled::gemm_tiled_kernel<kOutF32, kPair, TPG_EPI, kGrouped>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 static_cast<int>(tiled::Layout<kPair>::SMEM_BYTES)) == cudaSuccess;
 }
 template <bool kOutF32, bool kPair>
 cudaError_t launch_one(const TiledLaunch &l) {
-    return launch_ex(tiled::gemm_tiled_kernel<kOutF32, kPair, TPG_EPI>, l.grid, tiled::THREADS, l.smem,
-                     kPair ? 2 : 1, true, l.stream, *l.a, *l.b, *l.c, *l.d, *l.p);
+    SegArg<kGrouped> seg{};
+    if constexpr (kGrouped) {
+        if (!l.groups) return cudaErrorInvalidValue;
+        seg = *l.groups;
+    }
+    return launch_ex(tiled::gemm_tiled_kernel<kOutF32, kPair, TPG_EPI, kGrouped>, l.grid, tiled::THREADS, l.smem,
+                     kPair ? 2 : 1, true, l.stream, *l.a, *l.b, *l.c, *l.d, *l.p, seg);
 }
 } // namespace
 
-cudaError_t TPG_CAT(tiled_launch_e, TPG_EPI)(const TiledLaunch &l) {
+cudaError_t TPG_NAME(tiled_launch_)(const TiledLaunch &l) {
     if (l.pair) return l.f32 ? launch_one<true, true>(l) : launch_one<false, true>(l);
     return l.f32 ? launch_one<true, false>(l) : launch_one<false, false>(l);
 }
 
-bool TPG_CAT(tiled_set_limits_e, TPG_EPI)() {
+bool TPG_NAME(tiled_set_limits_)() {
     bool ok = set_limit<false, false>();
     ok = set_limit<true, false>() && ok;
     ok = set_limit<false, true>() && ok;
@@ -39,7 +54,7 @@ bool TPG_CAT(tiled_set_limits_e, TPG_EPI)() {
     return ok;
 }
 
-#if TPG_EPI == 0
+#if TPG_EPI == 0 && !TPG_GROUPED
 int tiled_pair_clusters(bool f32, int num_sms) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * (num_sms / 2), 1, 1);
@@ -54,8 +69,8 @@ int tiled_pair_clusters(bool f32, int num_sms) {
     cfg.numAttrs = 1;
     int n = 0;
     const cudaError_t e =
-        f32 ? cudaOccupancyMaxActiveClusters(&n, tiled::gemm_tiled_kernel<true, true, 0>, &cfg)
-            : cudaOccupancyMaxActiveClusters(&n, tiled::gemm_tiled_kernel<false, true, 0>, &cfg);
+        f32 ? cudaOccupancyMaxActiveClusters(&n, tiled::gemm_tiled_kernel<true, true, 0, false>, &cfg)
+            : cudaOccupancyMaxActiveClusters(&n, tiled::gemm_tiled_kernel<false, true, 0, false>, &cfg);
     if (e != cudaSuccess) {
         (void)cudaGetLastError();
         return -1;

@@ -100,6 +100,85 @@ int encode_2d(tpgemm_handle *h, CUtensorMap *map, CUtensorMapDataType dt, const 
     return r == CUDA_SUCCESS ? TPGEMM_OK : TPGEMM_ERR_CUDA;
 }
 
+// Rank-3 tensor map of a row-major matrix stack: `slices` matrices of rows x
+// inner elements with row stride ld and slice stride slice_ld (elements). One
+// slice when slices == 1 (its slice stride is never used).
+int encode_3d(PFN_cuTensorMapEncodeTiled_v12000 encode, CUtensorMap *map, CUtensorMapDataType dt, const void *ptr,
+              uint64_t inner, uint64_t rows, uint64_t row_stride_bytes, uint64_t slices, int64_t slice_ld, int64_t elt,
+              uint32_t box_inner, uint32_t box_outer) {
+    cuuint64_t dims[3] = {inner, rows, slices};
+    uint64_t s2 = slices > 1 ? static_cast<uint64_t>(slice_ld * elt) : row_stride_bytes * (rows > 0 ? rows : 1);
+    s2 = (s2 + 15) / 16 * 16;
+    if (s2 >= (1ull << 40)) s2 = (1ull << 40) - 16;
+    cuuint64_t strides[2] = {row_stride_bytes, s2};
+    cuuint32_t box[3] = {box_inner, box_outer, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = encode(map, dt, 3, const_cast<void *>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? TPGEMM_OK : TPGEMM_ERR_CUDA;
+}
+
+// One tiled launch, in the general form: `batch` slices of A, C, D (rows rows
+// each, or one stack of rows rows for a grouped GEMM) and `bslices` slices of
+// B. A stride of 0 shares one slice between all batches.
+struct TiledCall {
+    int64_t rows, N, K, batch, bslices;
+    const void *A;
+    int64_t lda, sA;
+    const void *B;
+    int64_t ldb, sB;
+    const void *C;
+    int64_t ldc, sC;
+    void *D;
+    int64_t ldd, sD;
+    float alpha, beta;
+    bool f32;
+};
+
+int build_tiled(PFN_cuTensorMapEncodeTiled_v12000 encode, const TiledCall &c, CUtensorMap *tmA, CUtensorMap *tmB,
+                CUtensorMap *tmC, CUtensorMap *tmD, tpg::TiledParams *p) {
+    const int64_t elt = c.f32 ? 4 : 2;
+    const bool use_c = c.beta != 0.0f;
+    const CUtensorMapDataType out_dt = c.f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    const uint32_t chunk = c.f32 ? 32u : 64u;
+    // C and D maps stop at the last whole 16-byte cell of a row (see TiledParams::n_tma);
+    // with no whole cell the maps are placeholders and every column takes the plain path.
+    const int64_t cell = 16 / elt;
+    const int64_t n_tma = c.N / cell * cell;
+    const uint64_t map_n = static_cast<uint64_t>(n_tma > 0 ? n_tma : c.N);
+    const int64_t aslices = c.sA ? c.batch : 1, bslices = c.sB ? c.bslices : 1;
+    const int64_t cslices = (use_c && c.sC) ? c.batch : 1;
+    if (encode_3d(encode, tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, c.A, c.K, c.rows, tma_stride(c.rows, c.K, c.lda, 2),
+                  aslices, c.sA, 2, 64, tpg::tiled::BM) ||
+        encode_3d(encode, tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, c.B, c.N, c.K, tma_stride(c.K, c.N, c.ldb, 2),
+                  bslices, c.sB, 2, 64, 64) ||
+        encode_3d(encode, tmD, out_dt, c.D, map_n, c.rows, tma_stride(c.rows, c.N, c.ldd, elt), c.batch, c.sD, elt,
+                  chunk, tpg::tiled::BM) ||
+        encode_3d(encode, tmC, out_dt, use_c ? c.C : c.D, map_n, c.rows,
+                  use_c ? tma_stride(c.rows, c.N, c.ldc, elt) : tma_stride(c.rows, c.N, c.ldd, elt), cslices,
+                  use_c ? c.sC : c.sD, elt, chunk, tpg::tiled::BM))
+        return TPGEMM_ERR_CUDA;
+    *p = tpg::TiledParams{};
+    p->M = static_cast<int32_t>(c.rows);
+    p->N = static_cast<int32_t>(c.N);
+    p->K = static_cast<int32_t>(c.K);
+    p->kb = static_cast<int32_t>((c.K + tpg::tiled::BK - 1) / tpg::tiled::BK);
+    p->a_bcast = c.sA ? 0 : 1;
+    p->b_bcast = c.sB ? 0 : 1;
+    p->c_bcast = c.sC ? 0 : 1;
+    p->sC = c.sC;
+    p->sD = c.sD;
+    p->n_tma = static_cast<int32_t>(n_tma);
+    p->alpha = c.alpha;
+    p->beta = c.beta;
+    p->C = use_c ? c.C : nullptr;
+    p->ldc = c.ldc;
+    p->D = c.D;
+    p->ldd = c.ldd;
+    return TPGEMM_OK;
+}
+
 int stream_clusters_for(tpgemm_handle *h, bool f32, int mt, int stages) {
     int &slot = h->stream_clusters[f32 ? 1 : 0][mt / 16 - 1];
     if (slot > 0) return slot;
@@ -187,6 +266,7 @@ int launch(Kernel kernel, int grid, int block, int smem, int cluster, cudaStream
 // Opts every GEMM instantiation into its dynamic shared-memory size (current device).
 bool set_smem_limits() {
     bool ok = tpg::tiled_set_limits_e0();
+    ok = tpg::tiled_set_limits_g0() && ok;
     ok = tpg::tiled_set_limits_e1() && ok;
     ok = tpg::tiled_set_limits_e2() && ok;
     ok = tpg::tiled_set_limits_e3() && ok;
@@ -444,41 +524,19 @@ int run_impl(tpgemm_handle *h, int64_t M, int64_t N, int64_t K, const void *A, i
                             D, ldd, ep);
     }
 
-    const CUtensorMapDataType out_dt = f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
     CUtensorMap tmA, tmB;
     if (pl.variant == TPGEMM_VARIANT_TILED || pl.variant == TPGEMM_VARIANT_TILED_PAIR) {
         CUtensorMap tmC, tmD;
-        const uint32_t chunk = f32 ? 32u : 64u;
-        // C and D maps stop at the last whole 16-byte cell of a row (see TiledParams::n_tma);
-        // with no whole cell the maps are placeholders and every column takes the plain path.
-        const int64_t cell = 16 / elt;
-        const int64_t n_tma = N / cell * cell;
-        const uint64_t map_n = static_cast<uint64_t>(n_tma > 0 ? n_tma : N);
-        if (encode_2d(h, &tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, A, K, M, tma_stride(M, K, lda, 2), 64,
-                      tpg::tiled::BM) ||
-            encode_2d(h, &tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, B, N, K, tma_stride(K, N, ldb, 2), 64, 64) ||
-            encode_2d(h, &tmD, out_dt, D, map_n, M, tma_stride(M, N, ldd, elt), chunk, tpg::tiled::BM) ||
-            encode_2d(h, &tmC, out_dt, use_c ? C : D, map_n, M,
-                      use_c ? tma_stride(M, N, ldc, elt) : tma_stride(M, N, ldd, elt), chunk, tpg::tiled::BM))
-            return TPGEMM_ERR_CUDA;
         tpg::TiledParams p;
-        p.M = static_cast<int32_t>(M);
-        p.N = static_cast<int32_t>(N);
-        p.K = static_cast<int32_t>(K);
-        p.kb = static_cast<int32_t>((K + tpg::tiled::BK - 1) / tpg::tiled::BK);
+        const TiledCall call{M, N, K, 1, 1, A, lda, 0, B, ldb, 0, C, ldc, 0, D, ldd, 0, alpha, beta, f32};
+        if (build_tiled(h->encode, call, &tmA, &tmB, &tmC, &tmD, &p) != TPGEMM_OK) return TPGEMM_ERR_CUDA;
         p.sched = pl.sched;
-        p.n_tma = static_cast<int32_t>(n_tma);
-        p.alpha = alpha;
-        p.beta = beta;
-        p.C = use_c ? C : nullptr;
-        p.ldc = ldc;
-        p.D = D;
-        p.ldd = ldd;
+        p.mt_batch = static_cast<int32_t>(pl.sched.mt);
         p.status = h->status;
         p.timeout_ns = h->timeout_ns;
         p.epi = ep;
         const tpg::TiledLaunch l{pl.grid, pl.smem, pl.variant == TPGEMM_VARIANT_TILED_PAIR, f32, stream,
-                                 &tmA, &tmB, &tmC, &tmD, &p};
+                                 &tmA, &tmB, &tmC, &tmD, &p, nullptr};
         return launch_tiled(fused ? 1 + ep.act : 0, l);
     }
 
@@ -511,6 +569,139 @@ int run_impl(tpgemm_handle *h, int64_t M, int64_t N, int64_t K, const void *A, i
 } // namespace
 
 extern "C" {
+
+int gemm_run_batched(tpgemm_handle *h, int64_t batch, int64_t M, int64_t N, int64_t K, const void *A, int64_t lda,
+                     int64_t sA, const void *B, int64_t ldb, int64_t sB, const void *C, int64_t ldc, int64_t sC,
+                     void *D, int64_t ldd, int64_t sD, float alpha, float beta, int out_dtype, void *stream_ptr) {
+    if (!h) return TPGEMM_ERR_INVALID_ARG;
+    if (batch < 0 || sA < 0 || sB < 0 || sC < 0 || sD < 0) return TPGEMM_ERR_INVALID_ARG;
+    int chk = gemm_check_args(M, N, K, A, lda, B, ldb, C, ldc, D, ldd, beta, out_dtype);
+    if (chk != TPGEMM_OK || batch == 0 || M == 0 || N == 0) return chk;
+    if (batch > kMaxDim || batch * ((M + tpg::tiled::BM - 1) / tpg::tiled::BM) > kMaxDim) return TPGEMM_ERR_TOO_LARGE;
+    const bool f32 = out_dtype == TPGEMM_OUT_F32;
+    const int64_t elt = f32 ? 4 : 2;
+    const bool use_c = beta != 0.0f;
+    if (batch > 1) {
+        if ((sA * 2) % 16 || (sB * 2) % 16 || (use_c && (sC * elt) % 16) || (sD * elt) % 16)
+            return TPGEMM_ERR_ALIGNMENT;
+        if (sD < (M - 1) * ldd + N) return TPGEMM_ERR_OVERLAP; // D slices must be disjoint
+        // every byte any slice of D touches, against every byte any slice of an input touches
+        const uintptr_t dlo = reinterpret_cast<uintptr_t>(D);
+        const Range rd_all{dlo, dlo + static_cast<uintptr_t>(((batch - 1) * sD + (M - 1) * ldd + N) * elt)};
+        auto extent = [&](const void *ptr, int64_t rows, int64_t cols, int64_t ld, int64_t st, int64_t e) {
+            const uintptr_t lo = reinterpret_cast<uintptr_t>(ptr);
+            return Range{lo, lo + static_cast<uintptr_t>(((batch - 1) * st + (rows - 1) * ld + cols) * e)};
+        };
+        if (K > 0 && (overlaps(rd_all, extent(A, M, K, lda, sA, 2)) || overlaps(rd_all, extent(B, K, N, ldb, sB, 2))))
+            return TPGEMM_ERR_OVERLAP;
+        if (use_c && !(C == D && ldc == ldd && sC == sD) && overlaps(rd_all, extent(C, M, N, ldc, sC, elt)))
+            return TPGEMM_ERR_OVERLAP;
+    }
+    DeviceGuard guard(h->device);
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+    if (K == 0) {
+        // D_b = beta * C_b, one small launch per slice
+        int64_t blocks = (M * N + 1023) / 1024;
+        if (blocks > 8LL * h->num_sms) blocks = 8LL * h->num_sms;
+        const tpg::EpiParams none{};
+        for (int64_t b = 0; b < batch; ++b) {
+            const void *cb = use_c ? static_cast<const char *>(C) + b * sC * elt : nullptr;
+            void *db = static_cast<char *>(D) + b * sD * elt;
+            const int32_t m = static_cast<int32_t>(M), n = static_cast<int32_t>(N);
+            const int rc = f32 ? launch(tpg::epilogue_only_kernel<true, false>, static_cast<int>(blocks), 256, 0, 1,
+                                        stream, m, n, beta, cb, ldc, db, ldd, none)
+                               : launch(tpg::epilogue_only_kernel<false, false>, static_cast<int>(blocks), 256, 0, 1,
+                                        stream, m, n, beta, cb, ldc, db, ldd, none);
+            if (rc != TPGEMM_OK) return rc;
+        }
+        return TPGEMM_OK;
+    }
+    const bool pair = M > tpg::tiled::BM;
+    const int64_t rows_per_tile = tpg::tiled::BM * (pair ? 2 : 1);
+    const int64_t mt = (M + rows_per_tile - 1) / rows_per_tile;
+    const int64_t nt = (N + tpg::tiled::BN - 1) / tpg::tiled::BN;
+    const int64_t cap = pair ? pair_clusters_for(h, f32) : h->num_sms;
+    const int64_t workers = mt * batch * nt < cap ? mt * batch * nt : cap;
+    CUtensorMap tmA, tmB, tmC, tmD;
+    tpg::TiledParams p;
+    const TiledCall call{M, N, K, batch, batch, A, lda, sA, B, ldb, sB, C, ldc, sC, D, ldd, sD, alpha, beta, f32};
+    if (build_tiled(h->encode, call, &tmA, &tmB, &tmC, &tmD, &p) != TPGEMM_OK) return TPGEMM_ERR_CUDA;
+    p.sched = tpg::make_schedule(mt * batch, nt, pair ? kGroupMPair : kGroupM, workers, true);
+    p.mt_batch = static_cast<int32_t>(mt);
+    p.status = h->status;
+    p.timeout_ns = h->timeout_ns;
+    const int smem = static_cast<int>(pair ? tpg::tiled::Layout<true>::SMEM_BYTES : tpg::tiled::Layout<false>::SMEM_BYTES);
+    const tpg::TiledLaunch l{static_cast<int>(workers * (pair ? 2 : 1)), smem, pair, f32, stream,
+                             &tmA, &tmB, &tmC, &tmD, &p, nullptr};
+    return launch_tiled(0, l);
+}
+
+int gemm_run_grouped(tpgemm_handle *h, int64_t groups, const int64_t *group_rows, int64_t N, int64_t K,
+                     const void *A, int64_t lda, const void *B, int64_t ldb, int64_t sB, const void *C, int64_t ldc,
+                     void *D, int64_t ldd, float alpha, float beta, int out_dtype, void *stream_ptr) {
+    if (!h || groups < 0 || sB < 0 || (groups > 0 && !group_rows)) return TPGEMM_ERR_INVALID_ARG;
+    if (groups > TPGEMM_MAX_GROUPS) return TPGEMM_ERR_TOO_LARGE;
+    int64_t total = 0;
+    for (int64_t g = 0; g < groups; ++g) {
+        if (group_rows[g] < 0) return TPGEMM_ERR_INVALID_ARG;
+        total += group_rows[g];
+        if (total > kMaxDim) return TPGEMM_ERR_TOO_LARGE;
+    }
+    int chk = gemm_check_args(total, N, K, A, lda, B, ldb, C, ldc, D, ldd, beta, out_dtype);
+    if (chk != TPGEMM_OK || total == 0 || N == 0) return chk;
+    const bool f32 = out_dtype == TPGEMM_OUT_F32;
+    const int64_t elt = f32 ? 4 : 2;
+    if (groups > 1 && K > 0) {
+        if ((sB * 2) % 16) return TPGEMM_ERR_ALIGNMENT;
+        const uintptr_t lo = reinterpret_cast<uintptr_t>(B);
+        const Range rb{lo, lo + static_cast<uintptr_t>(((groups - 1) * sB + (K - 1) * ldb + N) * 2)};
+        if (overlaps(byte_range(D, total, N, ldd, elt), rb)) return TPGEMM_ERR_OVERLAP;
+    }
+    DeviceGuard guard(h->device);
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+    const bool use_c = beta != 0.0f;
+    if (K == 0) {
+        int64_t blocks = (total * N + 1023) / 1024;
+        if (blocks > 8LL * h->num_sms) blocks = 8LL * h->num_sms;
+        const tpg::EpiParams none{};
+        const int32_t m = static_cast<int32_t>(total), n = static_cast<int32_t>(N);
+        const void *c = use_c ? C : nullptr;
+        return f32 ? launch(tpg::epilogue_only_kernel<true, false>, static_cast<int>(blocks), 256, 0, 1, stream, m, n,
+                            beta, c, ldc, D, ldd, none)
+                   : launch(tpg::epilogue_only_kernel<false, false>, static_cast<int>(blocks), 256, 0, 1, stream, m,
+                            n, beta, c, ldc, D, ldd, none);
+    }
+    // CTA pairs when groups are large enough on average to fill 256-row tiles
+    const bool pair = total > static_cast<int64_t>(tpg::tiled::BM) * groups;
+    const int32_t rows_per_tile = tpg::tiled::BM * (pair ? 2 : 1);
+    tpg::GroupTable table{};
+    table.groups = static_cast<int32_t>(groups);
+    int64_t row = 0, tiles = 0;
+    for (int64_t g = 0; g < groups; ++g) {
+        table.tile_prefix[g] = static_cast<int32_t>(tiles);
+        table.row_start[g] = static_cast<int32_t>(row);
+        table.rows[g] = static_cast<int32_t>(group_rows[g]);
+        row += group_rows[g];
+        tiles += (group_rows[g] + rows_per_tile - 1) / rows_per_tile;
+    }
+    table.tile_prefix[groups] = static_cast<int32_t>(tiles);
+    const int64_t nt = (N + tpg::tiled::BN - 1) / tpg::tiled::BN;
+    const int64_t cap = pair ? pair_clusters_for(h, f32) : h->num_sms;
+    const int64_t workers = tiles * nt < cap ? tiles * nt : cap;
+    CUtensorMap tmA, tmB, tmC, tmD;
+    tpg::TiledParams p;
+    const TiledCall call{total, N, K, 1, groups, A, lda, 0, B, ldb, groups > 1 ? sB : 0, C, ldc, 0, D, ldd, 0,
+                         alpha, beta, f32};
+    if (build_tiled(h->encode, call, &tmA, &tmB, &tmC, &tmD, &p) != TPGEMM_OK) return TPGEMM_ERR_CUDA;
+    p.sched = tpg::make_schedule(tiles, nt, pair ? kGroupMPair : kGroupM, workers, true);
+    p.mt_batch = 1;
+    p.status = h->status;
+    p.timeout_ns = h->timeout_ns;
+    const int smem = static_cast<int>(pair ? tpg::tiled::Layout<true>::SMEM_BYTES : tpg::tiled::Layout<false>::SMEM_BYTES);
+    const tpg::TiledLaunch l{static_cast<int>(workers * (pair ? 2 : 1)), smem, pair, f32, stream,
+                             &tmA, &tmB, &tmC, &tmD, &p, &table};
+    return tpg::tiled_launch_g0(l) == cudaSuccess ? TPGEMM_OK : TPGEMM_ERR_CUDA;
+}
 
 int gemm_sync_status(tpgemm_handle *h, void *stream) {
     if (!h) return TPGEMM_ERR_INVALID_ARG;
@@ -608,19 +799,6 @@ int noalloc_setup(int dev, NoallocDevice **out) {
     return TPGEMM_OK;
 }
 
-int noalloc_encode(PFN_cuTensorMapEncodeTiled_v12000 encode, CUtensorMap *map, CUtensorMapDataType dt,
-                   const void *ptr, uint64_t inner, uint64_t outer, uint64_t stride_bytes, uint32_t box_inner,
-                   uint32_t box_outer) {
-    cuuint64_t dims[2] = {inner, outer};
-    cuuint64_t strides[1] = {stride_bytes};
-    cuuint32_t box[2] = {box_inner, box_outer};
-    cuuint32_t estr[2] = {1, 1};
-    CUresult r = encode(map, dt, 2, const_cast<void *>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS ? TPGEMM_OK : TPGEMM_ERR_CUDA;
-}
-
 } // namespace
 
 extern "C" int gemm_run_noalloc(int64_t M, int64_t N, int64_t K, const void *A, int64_t lda, const void *B,
@@ -654,42 +832,20 @@ extern "C" int gemm_run_noalloc(int64_t M, int64_t N, int64_t K, const void *A, 
     } else {
         // The status word must start at zero: every call shares it.
         if (cudaMemsetAsync(nd->status, 0, sizeof(uint32_t), stream) != cudaSuccess) return TPGEMM_ERR_CUDA;
-        const CUtensorMapDataType out_dt = f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-        const uint32_t chunk = f32 ? 32u : 64u;
-        const int64_t cell = 16 / elt;
-        const int64_t n_tma = N / cell * cell;
-        const uint64_t map_n = static_cast<uint64_t>(n_tma > 0 ? n_tma : N);
         CUtensorMap tmA, tmB, tmC, tmD;
-        if (noalloc_encode(nd->encode, &tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, A, K, M, tma_stride(M, K, lda, 2), 64,
-                           tpg::tiled::BM) ||
-            noalloc_encode(nd->encode, &tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, B, N, K, tma_stride(K, N, ldb, 2), 64,
-                           64) ||
-            noalloc_encode(nd->encode, &tmD, out_dt, D, map_n, M, tma_stride(M, N, ldd, elt), chunk,
-                           tpg::tiled::BM) ||
-            noalloc_encode(nd->encode, &tmC, out_dt, use_c ? C : D, map_n, M,
-                           use_c ? tma_stride(M, N, ldc, elt) : tma_stride(M, N, ldd, elt), chunk, tpg::tiled::BM))
-            return TPGEMM_ERR_CUDA;
         tpg::TiledParams p;
-        p.M = static_cast<int32_t>(M);
-        p.N = static_cast<int32_t>(N);
-        p.K = static_cast<int32_t>(K);
+        const TiledCall call{M, N, K, 1, 1, A, lda, 0, B, ldb, 0, C, ldc, 0, D, ldd, 0, alpha, beta, f32};
+        if (build_tiled(nd->encode, call, &tmA, &tmB, &tmC, &tmD, &p) != TPGEMM_OK) return TPGEMM_ERR_CUDA;
         const int64_t mt = (M + tpg::tiled::BM - 1) / tpg::tiled::BM;
         const int64_t nt = (N + tpg::tiled::BN - 1) / tpg::tiled::BN;
         const int64_t tiles = mt * nt;
         const int grid = static_cast<int>(tiles < nd->num_sms ? tiles : nd->num_sms);
-        p.kb = static_cast<int32_t>((K + tpg::tiled::BK - 1) / tpg::tiled::BK);
         p.sched = tpg::make_schedule(mt, nt, kGroupM, grid, true);
-        p.n_tma = static_cast<int32_t>(n_tma);
-        p.alpha = alpha;
-        p.beta = beta;
-        p.C = use_c ? C : nullptr;
-        p.ldc = ldc;
-        p.D = D;
-        p.ldd = ldd;
+        p.mt_batch = static_cast<int32_t>(mt);
         p.status = nd->status;
         p.timeout_ns = 2000000000ull;
         const tpg::TiledLaunch l{grid, static_cast<int>(tpg::tiled::SMEM_BYTES), false, f32, stream,
-                                 &tmA, &tmB, &tmC, &tmD, &p};
+                                 &tmA, &tmB, &tmC, &tmD, &p, nullptr};
         rc = tpg::tiled_launch_e0(l) == cudaSuccess ? TPGEMM_OK : TPGEMM_ERR_CUDA;
     }
     if (rc != TPGEMM_OK || !check_status) return rc;
