@@ -337,6 +337,44 @@ def time_e2e(torch, tpd, h, wl, steps):
     return ms, wl.bytes_A + wl.bytes_B + wl.bytes_C, wl.bytes_D
 
 
+def chunk_tradeoff(torch, tpd, h, M=1024, N=8192, K=3584, reps=30):
+    """The chunk-size tradeoff of the tensor-parallel overlay loop on this GPU:
+    gemm_run_chunked on one shard of an MLP down-projection (1024 tokens,
+    hidden 8192, K = 28672 / 8), 1/2/4/8 chunks. Reports the median total time
+    and the time until chunk 0's rows are done (when a collective could start).
+    A device sleep ahead of the timed region keeps the GPU busy while the host
+    issues every chunk, so the times are the GPU's, not the launch latency's."""
+    g = torch.Generator().manual_seed(9)
+    A = torch.randn(M, K, generator=g).to(torch.bfloat16).cuda()
+    B = (torch.randn(K, N, generator=g) * 0.02).to(torch.bfloat16).cuda()
+    D = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
+    stream = torch.cuda.current_stream()
+    out = {}
+    for chunks in (1, 2, 4, 8):
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(chunks)]
+        for e in evs:
+            e.record(stream)
+        torch.cuda.synchronize()
+        totals, firsts = [], []
+        for r in range(reps + 3):
+            t0 = torch.cuda.Event(enable_timing=True)
+            torch.cuda._sleep(400_000)  # ~0.2 ms: longer than issuing 8 chunks from the host
+            t0.record(stream)
+            st = tpd.gemm_run_chunked(h, chunks, M, N, K, A.data_ptr(), K, B.data_ptr(), N, None, N, D.data_ptr(),
+                                      N, 1.0, 0.0, 0, [e.cuda_event for e in evs], stream.cuda_stream)
+            if st != 0:
+                raise RuntimeError(tpd.gemm_status_string(st))
+            torch.cuda.synchronize()
+            if r >= 3:
+                totals.append(t0.elapsed_time(evs[-1]))
+                firsts.append(t0.elapsed_time(evs[0]))
+        tot = statistics.median(totals)
+        out[str(chunks)] = {"total_ms": round(tot, 4), "first_chunk_ms": round(statistics.median(firsts), 4),
+                            "tflops": round(2 * M * N * K / (tot * 1e-3) / 1e12, 1)}
+    return {"unit": "ms", "config": {"workload": f"gemm_run_chunked, M={M} N={N} K={K} bf16, launches queued behind a "
+                                                 "device sleep, median of 30"}, "chunks": out}
+
+
 def roofline_entry(cfg, kernel, avg_ms, peaks, peak_src):
     if cfg.name == "decode":
         b_bytes = cfg.K * cfg.N * 2
@@ -510,6 +548,9 @@ def run_ours(args):
             launches += 100
             del wl2
             torch.cuda.empty_cache()
+
+    if not args.no_extra:
+        per_config["tp_overlay_chunks"] = chunk_tradeoff(torch, tpd, h)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

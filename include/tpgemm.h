@@ -192,6 +192,29 @@ int gemm_run_grouped(tpgemm_handle *h, int64_t groups, const int64_t *group_rows
                      float beta, int out_dtype, void *stream);
 
 /*
+ * M-chunked GEMM for overlapping a GEMM with the collective that consumes it
+ * ("Implementing Tensor Parallelism Communication Overlays ...", "Pipelining
+ * GEMM and Collectives: The Core Overlay Loop"): the rows of D are cut into
+ * `chunks` consecutive chunks; for each chunk i the chunk's GEMM (the same
+ * D = alpha*A*B + beta*C on its rows) is enqueued on `stream` and then
+ * events[i] is recorded on `stream`. A communication stream can wait on
+ * events[i] and start the collective on chunk i's rows of D while chunk i+1
+ * is computed ("Performance Tradeoffs": more chunks expose more overlap but
+ * make each GEMM smaller).
+ *   chunks    1 .. 64.
+ *   events    `chunks` cudaEvent_t handles created by the caller (with or
+ *             without timing), all non-NULL; the library only records them.
+ * Chunk boundaries are multiples of 128 rows: chunk i covers rows
+ * [b_i, b_{i+1}) with b_i = floor(i*M/chunks / 128) * 128 (b_chunks = M); a
+ * chunk may be empty, and its event is still recorded. Other arguments, rules
+ * and errors as gemm_run. Allocates nothing and never synchronises.
+ */
+int gemm_run_chunked(tpgemm_handle *h, int chunks, int64_t M, int64_t N, int64_t K,
+                     const void *A, int64_t lda, const void *B, int64_t ldb, const void *C,
+                     int64_t ldc, void *D, int64_t ldd, float alpha, float beta, int out_dtype,
+                     void *const *events, void *stream);
+
+/*
  * Synchronises `stream`, then reads and clears the handle's device status
  * word. Returns TPGEMM_OK, TPGEMM_ERR_TIMEOUT if any kernel since the last
  * call gave up on a pipeline wait (its output is then incomplete), or
@@ -236,16 +259,22 @@ int gemm_query_plan(tpgemm_handle *h, int64_t M, int64_t N, int64_t K, int out_d
 
 /*
  * Host copy of the persistent tile scheduler. For an mt x nt grid of output
- * tiles (256 columns wide; rows of 128, or 256 for CTA pairs) walked by
- * `workers` persistent workers with grouped raster `group_m`, writes the work
- * items of worker `worker`, in order, as triples out[3*i .. 3*i+2] = (tile
- * row, first column, width in columns) for i < cap, and returns how many items
- * that worker owns (or a negative status). With allow_split != 0, a last round
- * that is at most half full is cut into 128-column halves. The kernels run the
- * same functions, so this is what the partition tests check. No GPU is needed.
+ * tiles (256 columns wide; 128 rows, or 256 rows when pair != 0) and at most
+ * `cap` persistent workers (CTAs, or CTA pairs), gemm_schedule_workers returns
+ * how many workers the tiled kernels launch, and gemm_schedule_tiles writes
+ * the work items of worker `worker`, in order, as triples out[3*i .. 3*i+2] =
+ * (tile row, first column, width in columns) for i < cap_items, with the
+ * grouped raster's band height set to group_m; it returns how many items that
+ * worker owns (0 for a worker past the last; TPGEMM_ERR_INVALID_ARG on bad
+ * arguments). With allow_split, the tiles of a nearly empty last round (or all
+ * tiles, when there are fewer than workers) are cut into 2 or 4 column pieces
+ * (2 at most for pairs) when that shortens the estimated time. The kernels run
+ * the same functions, so this is what the partition tests check. No GPU is
+ * needed.
  */
-int64_t gemm_schedule_tiles(int64_t mt, int64_t nt, int group_m, int workers, int allow_split,
-                            int worker, int32_t *out, int64_t cap);
+int gemm_schedule_workers(int64_t mt, int64_t nt, int cap, int pair, int allow_split);
+int64_t gemm_schedule_tiles(int64_t mt, int64_t nt, int group_m, int cap, int pair, int allow_split, int worker,
+                            int32_t *out, int64_t cap_items);
 
 /*
  * Watchdog self-test: launches one CTA that waits on a barrier no thread will

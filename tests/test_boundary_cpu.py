@@ -161,41 +161,58 @@ GRIDS = [_tile_grid(256, 256), _tile_grid(4096, 4096), _tile_grid(8192, 6144), _
 
 
 @pytest.mark.parametrize("mt,nt", GRIDS)
-@pytest.mark.parametrize("workers", [1, 7, 74, 76, 148, 152, 160, 1000])
+@pytest.mark.parametrize("cap", [1, 7, 74, 76, 148, 152, 160, 1000])
 @pytest.mark.parametrize("group_m", [1, 8, 16])
-@pytest.mark.parametrize("split", [False, True])
-def test_schedule_is_an_exact_partition(mt, nt, workers, group_m, split):
-    """Every output column of every tile row is owned by exactly one worker."""
-    workers = min(workers, mt * nt) if mt * nt else 1
+@pytest.mark.parametrize("mode", ["whole", "cta", "pair"])
+def test_schedule_is_an_exact_partition(mt, nt, cap, group_m, mode):
+    """Every 64-column granule of every tile row is owned by exactly one worker."""
+    pair, split = mode == "pair", mode != "whole"
+    workers = tpd.gemm_schedule_workers(mt, nt, cap, pair, split)
+    assert 1 <= workers <= cap
     owner = {}
     loads = []
+    narrowest = 256 if not split else (128 if pair else 64)
     for w in range(workers):
-        items = tpd.gemm_schedule_tiles(mt, nt, group_m, workers, w, allow_split=split)
+        items = tpd.gemm_schedule_tiles(mt, nt, group_m, cap, w, pair, split)
         load = 0
         for (m, n0, width) in items:
             assert 0 <= m < mt and 0 <= n0 and n0 + width <= nt * 256
-            assert width in (256, 128) and n0 % width == 0
-            for c in range(n0 // 128, (n0 + width) // 128):  # 128-column granules
-                assert (m, c) not in owner, f"columns {c * 128}.. of tile row {m} owned twice"
+            assert width in (256, 128, 64) and width >= narrowest and n0 % width == 0
+            for c in range(n0 // 64, (n0 + width) // 64):
+                assert (m, c) not in owner, f"columns {c * 64}.. of tile row {m} owned twice"
                 owner[(m, c)] = w
             load += width
         loads.append(load)
-    assert len(owner) == mt * nt * 2
-    # balance: no worker does more than one whole tile beyond the average share
+    assert tpd.gemm_schedule_tiles(mt, nt, group_m, cap, workers, pair, split) == []  # past the last worker
+    assert len(owner) == mt * nt * 4
+    # balance: no worker does more than one whole tile beyond another
     assert max(loads) - min(loads) <= 256
 
 
 def test_schedule_tail_split_balances_square():
     # square 4096^3 in pair mode: 16 x 16 tiles of 256 x 256 on 76 pairs = 3 whole
     # rounds + 28 tiles, which are cut into 56 halves: nobody does a 4th whole tile.
-    loads = []
-    for w in range(76):
-        items = tpd.gemm_schedule_tiles(16, 16, 8, 76, w)
-        loads.append(sum(width for (_, _, width) in items))
+    loads = [sum(x[2] for x in tpd.gemm_schedule_tiles(16, 16, 8, 76, w, True)) for w in range(76)]
     assert max(loads) == 3 * 256 + 128 and min(loads) == 3 * 256
-    # without the split the busiest workers own four whole tiles
-    loads = [sum(x[2] for x in tpd.gemm_schedule_tiles(16, 16, 8, 76, w, allow_split=False)) for w in range(76)]
+    # without splitting the busiest workers own four whole tiles
+    loads = [sum(x[2] for x in tpd.gemm_schedule_tiles(16, 16, 8, 76, w, True, False)) for w in range(76)]
     assert max(loads) == 4 * 256
+
+
+def test_schedule_split_choice_follows_the_cost_model():
+    # A piece 1/f wide costs a + (1 - a)/f of a tile (a = 1/3 for 1-CTA tiles).
+    # 160 tiles on 152 CTAs: 8 left over -> quarters (one round at 1/2 a tile)
+    assert tpd.gemm_schedule_tiles(20, 8, 16, 152, 0)[-1][2] == 64
+    # 222 tiles: 70 left -> halves (1 round at 2/3) beat quarters (2 rounds at 1/2)
+    assert tpd.gemm_schedule_tiles(222, 1, 16, 152, 0)[-1][2] == 128
+    # 252 tiles: 100 left -> halves would take 2 rounds at 2/3 > 1 whole round
+    assert all(x[2] == 256 for x in tpd.gemm_schedule_tiles(252, 1, 16, 152, 0))
+    # a 128-row chunk of an 8192-wide output: 32 tiles on 152 CTAs -> 128 quarter tiles
+    assert tpd.gemm_schedule_workers(1, 32, 152) == 128
+    items = [tpd.gemm_schedule_tiles(1, 32, 16, 152, w) for w in range(128)]
+    assert all(len(i) == 1 and i[0][2] == 64 for i in items)
+    # pairs (halves at most, a = 1/2): 32 pair tiles on 76 pairs -> 64 halves
+    assert tpd.gemm_schedule_workers(1, 32, 76, True) == 64
 
 
 def test_schedule_grouped_raster_order():
@@ -210,6 +227,7 @@ def test_schedule_grouped_raster_order():
 
 def test_schedule_rejects_bad_arguments():
     lib = tpd.load_library()
-    assert lib.gemm_schedule_tiles(4, 4, 0, 1, 1, 0, None, 0) == tpd.ERR_INVALID_ARG
-    assert lib.gemm_schedule_tiles(4, 4, 8, 2, 1, 2, None, 0) == tpd.ERR_INVALID_ARG
-    assert lib.gemm_schedule_tiles(4, 4, 8, 2, 1, 0, None, 3) == tpd.ERR_INVALID_ARG
+    assert lib.gemm_schedule_tiles(4, 4, 0, 1, 0, 1, 0, None, 0) == tpd.ERR_INVALID_ARG
+    assert lib.gemm_schedule_tiles(4, 4, 8, 2, 0, 1, -1, None, 0) == tpd.ERR_INVALID_ARG
+    assert lib.gemm_schedule_tiles(4, 4, 8, 2, 0, 1, 0, None, 3) == tpd.ERR_INVALID_ARG
+    assert lib.gemm_schedule_workers(4, 4, 0, 0, 1) == tpd.ERR_INVALID_ARG

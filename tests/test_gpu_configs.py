@@ -88,9 +88,13 @@ def test_plans_match_the_design(h):
     p = tpd.gemm_query_plan(h, 16, 28672, 4096, tpd.OUT_BF16)
     assert p["variant"] == tpd.VARIANT_STREAM and p["num_tiles"] == 224 and p["cluster"] == 2
     assert p["grid"] % 2 == 0 and p["grid"] <= sms
+    # one tile: cut in two halves on two pairs, or four quarters on four CTAs
     p = tpd.gemm_query_plan(h, 256, 256, 256, tpd.OUT_F32)
-    assert p["variant"] == tpd.VARIANT_TILED_PAIR and p["grid"] == 2
+    assert p["variant"] == tpd.VARIANT_TILED_PAIR and p["grid"] == 4
     p = tpd.gemm_query_plan(h, 100, 256, 256, tpd.OUT_F32)
-    assert p["variant"] == tpd.VARIANT_TILED and p["grid"] == 1
+    assert p["variant"] == tpd.VARIANT_TILED and p["grid"] == 4
+    # a 128-row slice of an 8192-wide output: 32 tiles become 128 quarter tiles
+    p = tpd.gemm_query_plan(h, 128, 8192, 4096, tpd.OUT_BF16)
+    assert p["variant"] == tpd.VARIANT_TILED and p["grid"] == min(128, sms)
     p = tpd.gemm_query_plan(h, 5, 5, 0, tpd.OUT_F32)
     assert p["variant"] == tpd.VARIANT_EPILOGUE_ONLY

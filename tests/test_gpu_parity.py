@@ -150,9 +150,11 @@ def test_in_place_d_equals_c(h, out_dtype, M):
 @pytest.mark.parametrize("variant", [tpd.VARIANT_TILED, tpd.VARIANT_TILED_PAIR], ids=["tiled", "pair"])
 @pytest.mark.parametrize("out_dtype", [torch.bfloat16, torch.float32], ids=["bf16", "f32"])
 def test_tiled_modes_with_tail_split(h, shape, variant, out_dtype):
-    """Both tiled modes on shapes whose last round is cut into 128-column
-    halves (2560 x 2048: 160 tiles on 152 CTAs, 80 pair tiles on 76 pairs);
-    with N = 1800 one half lies entirely right of N."""
+    """Both tiled modes on shapes whose last round is cut into column pieces
+    (2560 x 2048: 160 tiles on 152 CTAs leave 8, cut into 64-column quarters;
+    80 pair tiles on 76 pairs leave 4, cut into halves); with N = 1800 some
+    pieces lie entirely right of N; 300 x 520 has fewer tiles than CTAs, so
+    every tile is cut."""
     M, N, K = shape
     A, B, C = _inputs(M, N, K, seed=M + N, integer=True, with_c=True, c_dtype=out_dtype)
     _variant(h, variant)

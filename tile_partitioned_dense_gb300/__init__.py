@@ -66,6 +66,8 @@ def load_library() -> ctypes.CDLL:
             "gemm_create": (i32, [ctypes.POINTER(vp), i32]),
             "gemm_run": (i32, [vp, i64, i64, i64, vp, i64, vp, i64, vp, i64, vp, i64, f32, f32, i32, vp]),
             "gemm_sync_status": (i32, [vp, vp]),
+            "gemm_run_chunked": (i32, [vp, i32, i64, i64, i64, vp, i64, vp, i64, vp, i64, vp, i64, f32, f32, i32,
+                                       ctypes.POINTER(vp), vp]),
             "gemm_run_batched": (i32, [vp, i64, i64, i64, i64, vp, i64, i64, vp, i64, i64, vp, i64, i64, vp, i64,
                                        i64, f32, f32, i32, vp]),
             "gemm_run_grouped": (i32, [vp, i64, pi64, i64, i64, vp, i64, vp, i64, i64, vp, i64, vp, i64, f32, f32,
@@ -77,7 +79,8 @@ def load_library() -> ctypes.CDLL:
             "gemm_status_string": (ctypes.c_char_p, [i32]),
             "gemm_force_variant": (i32, [vp, i32]),
             "gemm_query_plan": (i32, [vp, i64, i64, i64, i32, pi32, pi32, pi32, pi64, pi32, pi32, pi32, pi32]),
-            "gemm_schedule_tiles": (i64, [i64, i64, i32, i32, i32, i32, ctypes.POINTER(ctypes.c_int32), i64]),
+            "gemm_schedule_tiles": (i64, [i64, i64, i32, i32, i32, i32, i32, ctypes.POINTER(ctypes.c_int32), i64]),
+            "gemm_schedule_workers": (i32, [i64, i64, i32, i32, i32]),
             "gemm_watchdog_selftest": (i32, [vp, ctypes.c_uint64, vp]),
             "gemm_num_sms": (i32, [vp]),
             "gemm_run_noalloc": (i32, [i64, i64, i64, vp, i64, vp, i64, vp, i64, vp, i64, f32, f32, i32, vp,
@@ -126,6 +129,14 @@ def gemm_run_grouped(h, group_rows, N, K, A, lda, B, ldb, strideB, C, ldc, D, ld
                                            alpha, beta, out_dtype, stream)
 
 
+def gemm_run_chunked(h, chunks, M, N, K, A, lda, B, ldb, C, ldc, D, ldd, alpha, beta, out_dtype, events,
+                     stream) -> int:
+    """events: `chunks` raw cudaEvent_t handles (e.g. torch.cuda.Event().cuda_event)."""
+    ev = (ctypes.c_void_p * max(len(events), 1))(*[int(e) for e in events])
+    return load_library().gemm_run_chunked(h, chunks, M, N, K, A, lda, B, ldb, C, ldc, D, ldd, alpha, beta,
+                                           out_dtype, ev, stream)
+
+
 def gemm_sync_status(h, stream=None) -> int:
     return load_library().gemm_sync_status(h, stream)
 
@@ -158,14 +169,19 @@ def gemm_query_plan(h, M, N, K, out_dtype) -> dict:
                 cluster=cl.value, smem_bytes=sm.value, launches=la.value)
 
 
-def gemm_schedule_tiles(mt: int, nt: int, group_m: int, workers: int, worker: int, allow_split: bool = True):
+def gemm_schedule_workers(mt: int, nt: int, cap: int, pair: bool = False, allow_split: bool = True) -> int:
+    return load_library().gemm_schedule_workers(mt, nt, cap, int(pair), int(allow_split))
+
+
+def gemm_schedule_tiles(mt: int, nt: int, group_m: int, cap: int, worker: int, pair: bool = False,
+                        allow_split: bool = True):
     """Work items (tile row, first column, width) of worker `worker`: the kernels' own schedule."""
     lib = load_library()
-    n = lib.gemm_schedule_tiles(mt, nt, group_m, workers, int(allow_split), worker, None, 0)
+    n = lib.gemm_schedule_tiles(mt, nt, group_m, cap, int(pair), int(allow_split), worker, None, 0)
     if n < 0:
         raise TpgemmError(int(n), "gemm_schedule_tiles")
     buf = (ctypes.c_int32 * max(3 * n, 1))()
-    lib.gemm_schedule_tiles(mt, nt, group_m, workers, int(allow_split), worker, buf, n)
+    lib.gemm_schedule_tiles(mt, nt, group_m, cap, int(pair), int(allow_split), worker, buf, n)
     return [(buf[3 * i], buf[3 * i + 1], buf[3 * i + 2]) for i in range(n)]
 
 

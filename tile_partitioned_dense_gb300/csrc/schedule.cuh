@@ -11,10 +11,11 @@
 //     tiles: tile whole + (t - whole) / split, piece (t - whole) % split, each
 //     BN / split columns wide.
 // whole is a multiple of P (the complete rounds), so the pieces start a new
-// round. Cutting a last round that is at most half full into halves lets every
-// worker take one half instead of leaving most workers idle while some finish a
-// whole tile (wave quantization). Every (tile, piece) pair has exactly one
-// index, so every output element has exactly one owner: no atomics, no split-K.
+// round. Cutting a nearly empty last round (or, with fewer tiles than workers,
+// every tile) into column pieces lets more workers share it instead of leaving
+// most of them idle while some finish a whole tile (wave quantization). Every
+// (tile, piece) pair has exactly one index, so every output element has
+// exactly one owner: no atomics, no split-K.
 //
 // The grouped raster: the tile grid is cut into bands of `group_m` tile rows;
 // inside a band the index runs down the band's rows first, then across the
@@ -47,9 +48,10 @@ __host__ __device__ __forceinline__ TileCoord tile_of_index(int64_t t, int64_t m
 struct Schedule {
     int64_t mt, nt;  // tile grid
     int32_t group_m; // band height of the grouped raster, in tiles
-    int32_t split;   // 1 or 2: column pieces per tile after the whole rounds
+    int32_t split;   // 1, 2 or 4: column pieces per tile after the whole rounds
     int64_t whole;   // tiles processed whole (a multiple of the worker count)
     int64_t pieces;  // split * (mt * nt - whole)
+    int64_t workers; // persistent workers to launch
 };
 
 // One unit of work: tile row m (in tiles), first column n and width (in columns).
@@ -79,20 +81,45 @@ __host__ __device__ __forceinline__ bool work_item(const Schedule &s, int64_t t,
     return true;
 }
 
-// Host-side choice for `workers` persistent workers: whole rounds first, then
-// the remainder cut in halves when it fills at most half a round.
-__host__ __device__ __forceinline__ Schedule make_schedule(int64_t mt, int64_t nt, int32_t group_m,
-                                                           int64_t workers, bool allow_split) {
+// Host-side choice for at most `cap` persistent workers. With at least `cap`
+// tiles: whole rounds of whole tiles, then the remaining tiles cut into
+// `split` column pieces; with fewer tiles than workers every tile is cut, so
+// that more workers have work. split is taken from {1, 2, 4} (up to
+// max_split) to minimise the estimated time of the cut part: its rounds times
+// the cost of one piece. The tiles are bound by operand loads, and a piece
+// 1/f of a tile wide still loads all of the tile's A rows, so a piece costs
+// a_share + (1 - a_share) / f of a whole tile, a_share being A's part of the
+// operand bytes a whole tile loads per k-block.
+__host__ __device__ __forceinline__ Schedule make_schedule(int64_t mt, int64_t nt, int32_t group_m, int64_t cap,
+                                                           int32_t max_split, double a_share) {
     Schedule s;
     s.mt = mt;
     s.nt = nt;
     s.group_m = group_m;
     const int64_t total = mt * nt;
-    const int64_t rounds = workers > 0 ? total / workers : 0;
-    const int64_t rest = total - rounds * workers;
-    s.whole = rounds * workers;
-    s.split = (allow_split && rest > 0 && 2 * rest <= workers) ? 2 : 1;
-    s.pieces = s.split * rest;
+    if (cap < 1) cap = 1;
+    const int64_t rest = total >= cap ? total - (total / cap) * cap : total;
+    int32_t best = 1;
+    double best_cost = 1e300;
+    for (int32_t f = 1; f <= max_split && f <= 4; f *= 2) {
+        const double rounds = static_cast<double>((f * rest + cap - 1) / cap);
+        const double cost = rounds * (a_share + (1.0 - a_share) / f);
+        if (cost < best_cost - 1e-9) {
+            best_cost = cost;
+            best = f;
+        }
+    }
+    s.split = best;
+    if (total >= cap) {
+        s.workers = cap;
+        s.whole = (total / cap) * cap;
+        s.pieces = s.split * (total - s.whole);
+    } else {
+        s.whole = 0;
+        s.pieces = s.split * total;
+        s.workers = s.pieces < cap ? s.pieces : cap;
+        if (s.workers < 1) s.workers = 1;
+    }
     return s;
 }
 

@@ -25,6 +25,16 @@ constexpr int kGroupM = 16;             // grouped-raster band height, in tiles 
 constexpr int kGroupMPair = 8;          // band height in 256-row pair tiles
 constexpr int kStreamMaxM = 64;
 
+// The tiled kernels' schedule for an mt x nt tile grid on at most `cap`
+// workers. A 1-CTA tile loads 128 A rows and 256 B columns per k-block (A is a
+// third of the bytes) and may be cut into 2 or 4 column pieces; a pair tile
+// loads 128 A rows and 128 B columns per CTA (A is half) and is cut in halves
+// at most, so that each CTA of the pair keeps a 64-column B box.
+tpg::Schedule tiled_schedule(int64_t mt, int64_t nt, int64_t cap, bool pair, bool allow_split) {
+    const int max_split = allow_split ? (pair ? 2 : 4) : 1;
+    return tpg::make_schedule(mt, nt, pair ? kGroupMPair : kGroupM, cap, max_split, pair ? 0.5 : 1.0 / 3.0);
+}
+
 struct Plan {
     int variant = TPGEMM_VARIANT_AUTO;
     int tile_m = 0, tile_n = 0;
@@ -224,10 +234,9 @@ Plan make_plan(tpgemm_handle *h, int64_t M, int64_t N, int64_t K, int out_dtype)
         pl.tile_n = tpg::tiled::BN;
         pl.num_tiles = mt * nt;
         const int64_t cap = pair ? pair_clusters_for(h, out_dtype == TPGEMM_OUT_F32) : h->num_sms;
-        const int64_t workers = pl.num_tiles < cap ? pl.num_tiles : cap;
         pl.cluster = pair ? 2 : 1;
-        pl.grid = static_cast<int>(workers * pl.cluster);
-        pl.sched = tpg::make_schedule(mt, nt, pair ? kGroupMPair : kGroupM, workers, true);
+        pl.sched = tiled_schedule(mt, nt, cap, pair, true);
+        pl.grid = static_cast<int>(pl.sched.workers * pl.cluster);
         pl.split = pl.sched.split;
         pl.smem = static_cast<int>(pair ? tpg::tiled::Layout<true>::SMEM_BYTES : tpg::tiled::Layout<false>::SMEM_BYTES);
         return pl;
@@ -427,16 +436,22 @@ int gemm_query_plan(tpgemm_handle *h, int64_t M, int64_t N, int64_t K, int out_d
     return TPGEMM_OK;
 }
 
-int64_t gemm_schedule_tiles(int64_t mt, int64_t nt, int group_m, int workers, int allow_split, int worker,
-                            int32_t *out, int64_t cap) {
-    if (mt < 0 || nt < 0 || group_m < 1 || workers < 1 || worker < 0 || worker >= workers || cap < 0 ||
-        (cap > 0 && !out))
+int gemm_schedule_workers(int64_t mt, int64_t nt, int cap, int pair, int allow_split) {
+    if (mt < 0 || nt < 0 || cap < 1) return TPGEMM_ERR_INVALID_ARG;
+    return static_cast<int>(tiled_schedule(mt, nt, cap, pair != 0, allow_split != 0).workers);
+}
+
+int64_t gemm_schedule_tiles(int64_t mt, int64_t nt, int group_m, int cap, int pair, int allow_split, int worker,
+                            int32_t *out, int64_t cap_items) {
+    if (mt < 0 || nt < 0 || group_m < 1 || cap < 1 || worker < 0 || cap_items < 0 || (cap_items > 0 && !out))
         return TPGEMM_ERR_INVALID_ARG;
-    const tpg::Schedule s = tpg::make_schedule(mt, nt, group_m, workers, allow_split != 0);
+    tpg::Schedule s = tiled_schedule(mt, nt, cap, pair != 0, allow_split != 0);
+    s.group_m = group_m;
+    if (worker >= s.workers) return 0;
     int64_t count = 0;
     tpg::WorkItem w;
-    for (int64_t t = worker; tpg::work_item(s, t, tpg::tiled::BN, w); t += workers, ++count) {
-        if (count < cap) {
+    for (int64_t t = worker; tpg::work_item(s, t, tpg::tiled::BN, w); t += s.workers, ++count) {
+        if (count < cap_items) {
             out[3 * count] = w.m;
             out[3 * count + 1] = w.n;
             out[3 * count + 2] = w.width;
@@ -621,17 +636,16 @@ int gemm_run_batched(tpgemm_handle *h, int64_t batch, int64_t M, int64_t N, int6
     const int64_t mt = (M + rows_per_tile - 1) / rows_per_tile;
     const int64_t nt = (N + tpg::tiled::BN - 1) / tpg::tiled::BN;
     const int64_t cap = pair ? pair_clusters_for(h, f32) : h->num_sms;
-    const int64_t workers = mt * batch * nt < cap ? mt * batch * nt : cap;
     CUtensorMap tmA, tmB, tmC, tmD;
     tpg::TiledParams p;
     const TiledCall call{M, N, K, batch, batch, A, lda, sA, B, ldb, sB, C, ldc, sC, D, ldd, sD, alpha, beta, f32};
     if (build_tiled(h->encode, call, &tmA, &tmB, &tmC, &tmD, &p) != TPGEMM_OK) return TPGEMM_ERR_CUDA;
-    p.sched = tpg::make_schedule(mt * batch, nt, pair ? kGroupMPair : kGroupM, workers, true);
+    p.sched = tiled_schedule(mt * batch, nt, cap, pair, true);
     p.mt_batch = static_cast<int32_t>(mt);
     p.status = h->status;
     p.timeout_ns = h->timeout_ns;
     const int smem = static_cast<int>(pair ? tpg::tiled::Layout<true>::SMEM_BYTES : tpg::tiled::Layout<false>::SMEM_BYTES);
-    const tpg::TiledLaunch l{static_cast<int>(workers * (pair ? 2 : 1)), smem, pair, f32, stream,
+    const tpg::TiledLaunch l{static_cast<int>(p.sched.workers * (pair ? 2 : 1)), smem, pair, f32, stream,
                              &tmA, &tmB, &tmC, &tmD, &p, nullptr};
     return launch_tiled(0, l);
 }
@@ -687,20 +701,50 @@ int gemm_run_grouped(tpgemm_handle *h, int64_t groups, const int64_t *group_rows
     table.tile_prefix[groups] = static_cast<int32_t>(tiles);
     const int64_t nt = (N + tpg::tiled::BN - 1) / tpg::tiled::BN;
     const int64_t cap = pair ? pair_clusters_for(h, f32) : h->num_sms;
-    const int64_t workers = tiles * nt < cap ? tiles * nt : cap;
     CUtensorMap tmA, tmB, tmC, tmD;
     tpg::TiledParams p;
     const TiledCall call{total, N, K, 1, groups, A, lda, 0, B, ldb, groups > 1 ? sB : 0, C, ldc, 0, D, ldd, 0,
                          alpha, beta, f32};
     if (build_tiled(h->encode, call, &tmA, &tmB, &tmC, &tmD, &p) != TPGEMM_OK) return TPGEMM_ERR_CUDA;
-    p.sched = tpg::make_schedule(tiles, nt, pair ? kGroupMPair : kGroupM, workers, true);
+    p.sched = tiled_schedule(tiles, nt, cap, pair, true);
     p.mt_batch = 1;
     p.status = h->status;
     p.timeout_ns = h->timeout_ns;
     const int smem = static_cast<int>(pair ? tpg::tiled::Layout<true>::SMEM_BYTES : tpg::tiled::Layout<false>::SMEM_BYTES);
-    const tpg::TiledLaunch l{static_cast<int>(workers * (pair ? 2 : 1)), smem, pair, f32, stream,
+    const tpg::TiledLaunch l{static_cast<int>(p.sched.workers * (pair ? 2 : 1)), smem, pair, f32, stream,
                              &tmA, &tmB, &tmC, &tmD, &p, &table};
     return tpg::tiled_launch_g0(l) == cudaSuccess ? TPGEMM_OK : TPGEMM_ERR_CUDA;
+}
+
+int gemm_run_chunked(tpgemm_handle *h, int chunks, int64_t M, int64_t N, int64_t K, const void *A, int64_t lda,
+                     const void *B, int64_t ldb, const void *C, int64_t ldc, void *D, int64_t ldd, float alpha,
+                     float beta, int out_dtype, void *const *events, void *stream_ptr) {
+    if (!h || chunks < 1 || chunks > 64 || !events) return TPGEMM_ERR_INVALID_ARG;
+    for (int i = 0; i < chunks; ++i)
+        if (!events[i]) return TPGEMM_ERR_INVALID_ARG;
+    const int chk = gemm_check_args(M, N, K, A, lda, B, ldb, C, ldc, D, ldd, beta, out_dtype);
+    if (chk != TPGEMM_OK) return chk;
+    const int64_t elt = out_dtype == TPGEMM_OUT_F32 ? 4 : 2;
+    const bool use_c = beta != 0.0f;
+    DeviceGuard guard(h->device);
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+    int64_t r0 = 0;
+    for (int i = 0; i < chunks; ++i) {
+        const int64_t r1 = (i == chunks - 1) ? M : (static_cast<int64_t>(i + 1) * M / chunks) / 128 * 128;
+        const int64_t rows = r1 > r0 ? r1 - r0 : 0;
+        if (rows > 0 && N > 0) {
+            // row offsets are multiples of 128, so every chunk keeps the 16-byte alignment of the whole
+            const void *a = K > 0 ? static_cast<const char *>(A) + r0 * lda * 2 : A;
+            const void *c = use_c ? static_cast<const char *>(C) + r0 * ldc * elt : C;
+            void *d = static_cast<char *>(D) + r0 * ldd * elt;
+            const int rc = run_impl(h, rows, N, K, a, lda, B, ldb, c, ldc, d, ldd, alpha, beta, out_dtype, nullptr,
+                                    stream_ptr);
+            if (rc != TPGEMM_OK) return rc;
+        }
+        if (cudaEventRecord(static_cast<cudaEvent_t>(events[i]), stream) != cudaSuccess) return TPGEMM_ERR_CUDA;
+        if (r1 > r0) r0 = r1;
+    }
+    return TPGEMM_OK;
 }
 
 int gemm_sync_status(tpgemm_handle *h, void *stream) {
@@ -838,9 +882,8 @@ extern "C" int gemm_run_noalloc(int64_t M, int64_t N, int64_t K, const void *A, 
         if (build_tiled(nd->encode, call, &tmA, &tmB, &tmC, &tmD, &p) != TPGEMM_OK) return TPGEMM_ERR_CUDA;
         const int64_t mt = (M + tpg::tiled::BM - 1) / tpg::tiled::BM;
         const int64_t nt = (N + tpg::tiled::BN - 1) / tpg::tiled::BN;
-        const int64_t tiles = mt * nt;
-        const int grid = static_cast<int>(tiles < nd->num_sms ? tiles : nd->num_sms);
-        p.sched = tpg::make_schedule(mt, nt, kGroupM, grid, true);
+        p.sched = tiled_schedule(mt, nt, nd->num_sms, false, true);
+        const int grid = static_cast<int>(p.sched.workers);
         p.mt_batch = static_cast<int32_t>(mt);
         p.status = nd->status;
         p.timeout_ns = 2000000000ull;
