@@ -10,8 +10,11 @@
 //                  of 48 KB and six stages fit where four did.
 // Inside a CTA three roles run concurrently, connected by mbarriers:
 //   warp 0      TMA producer: per 64-wide K block, one A box (128 rows x 64 K,
-//               K-major) and the B boxes (64 K rows x 64 N each, N-major), all
-//               128-byte swizzled, into the shared-memory ring.
+//               K-major) and the B boxes (64 K rows x 64 N each, N-major, two
+//               per instruction when N is a multiple of 64), all 128-byte
+//               swizzled, into the shared-memory ring. The TMA unit's cost
+//               grows with the number of instructions, not only with bytes, so
+//               fewer, larger boxes keep the ring fuller.
 //   warp 1      allocates all 512 TMEM columns (two 128 x 256 fp32
 //               accumulators); one lane (of the even CTA, in pair mode) issues
 //               the MMAs, K = 16 each, four per K block, and frees each ring
@@ -55,6 +58,11 @@ struct TiledParams {
     // 16-byte cells of the innermost dimension even past its bound. The last
     // n_tma..N-1 columns (fewer than one cell) use plain loads and stores.
     int32_t n_tma;
+    // 1: B's tensor map is 4-D, [slice][N/64 groups][K][64 columns] (N a multiple
+    // of 64), and each load brings two 64-column groups of one K block (one
+    // TMA instruction where the 3-D map needs two); 0: B's map is 3-D,
+    // [slice][K][N], loaded one 64 x 64 box at a time.
+    int32_t b_grouped;
     float alpha, beta;
     const void *C;
     int64_t ldc;
@@ -260,7 +268,12 @@ __global__ void __launch_bounds__(THREADS, 1)
                 const int32_t bb = p.b_bcast ? 0 : sg.bb;
                 const int32_t cols = w.width / CL; // B columns this CTA stages
                 const int32_t nb = w.n + static_cast<int32_t>(rank) * cols;
-                const uint32_t tx = CL * (A_STAGE_BYTES + static_cast<uint32_t>(cols) * BK * 2);
+                // Grouped B: boxes of two 64-column groups. A piece 64 columns wide
+                // still loads two (the second one's columns are not used; the
+                // stage has room for them), so the byte count is whole boxes.
+                const int32_t nload = p.b_grouped ? (cols / 64 + 1) / 2 : cols / 64;
+                const uint32_t bbytes = static_cast<uint32_t>(p.b_grouped ? 2 * nload : nload) * B_BOX_BYTES;
+                const uint32_t tx = CL * (A_STAGE_BYTES + bbytes);
                 for (int32_t kb = 0; kb < p.kb; ++kb) {
                     if (!mbar_wait(&empty[stage], phase ^ 1u, ctl, kStatusTimeoutProducer)) {
                         ok = false;
@@ -273,13 +286,24 @@ __global__ void __launch_bounds__(THREADS, 1)
                         if (rank == 0) mbar_arrive_expect_tx(&full[stage], tx);
                         const uint32_t fb = full0 + stage * 8u;
                         tma_load_3d_pair(&tmA, fb, adst, k0, m0, ab);
-                        for (int c = 0; c < cols / 64; ++c)
-                            tma_load_3d_pair(&tmB, fb, bdst + c * B_BOX_BYTES, nb + c * 64, k0, bb);
+                        if (p.b_grouped) {
+                            for (int c = 0; c < nload; ++c)
+                                tma_load_4d_pair(&tmB, fb, bdst + 2 * c * B_BOX_BYTES, 0, k0, (nb >> 6) + 2 * c, bb);
+                        } else {
+                            for (int c = 0; c < nload; ++c)
+                                tma_load_3d_pair(&tmB, fb, bdst + c * B_BOX_BYTES, nb + c * 64, k0, bb);
+                        }
                     } else {
                         mbar_arrive_expect_tx(&full[stage], tx);
                         tma_load_3d(&tmA, &full[stage], adst, k0, m0, ab);
-                        for (int c = 0; c < cols / 64; ++c)
-                            tma_load_3d(&tmB, &full[stage], bdst + c * B_BOX_BYTES, nb + c * 64, k0, bb);
+                        if (p.b_grouped) {
+                            for (int c = 0; c < nload; ++c)
+                                tma_load_4d(&tmB, &full[stage], bdst + 2 * c * B_BOX_BYTES, 0, k0, (nb >> 6) + 2 * c,
+                                            bb);
+                        } else {
+                            for (int c = 0; c < nload; ++c)
+                                tma_load_3d(&tmB, &full[stage], bdst + c * B_BOX_BYTES, nb + c * 64, k0, bb);
+                        }
                     }
                     ++issued;
                     if (++stage == STAGES) {

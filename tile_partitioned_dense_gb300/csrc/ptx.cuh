@@ -222,6 +222,26 @@ __device__ __forceinline__ void tma_load_3d(const CUtensorMap *m, uint64_t *bar,
         : "memory");
 }
 
+// 4-D forms: B viewed as [slice][64-column group][K row][64 columns], so that
+// one box brings several 64-column groups of one K block.
+__device__ __forceinline__ void tma_load_4d(const CUtensorMap *m, uint64_t *bar, void *dst, int32_t c0,
+                                            int32_t c1, int32_t c2, int32_t c3) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(smem_addr(dst)),
+        "l"(reinterpret_cast<uint64_t>(m)), "r"(smem_addr(bar)), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_load_4d_pair(const CUtensorMap *m, uint32_t bar_cluster_addr, void *dst,
+                                                 int32_t c0, int32_t c1, int32_t c2, int32_t c3) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(smem_addr(dst)),
+        "l"(reinterpret_cast<uint64_t>(m)), "r"(bar_cluster_addr), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+        : "memory");
+}
+
 __device__ __forceinline__ void tma_load_3d_pair(const CUtensorMap *m, uint32_t bar_cluster_addr, void *dst,
                                                  int32_t c0, int32_t c1, int32_t c2) {
     asm volatile(

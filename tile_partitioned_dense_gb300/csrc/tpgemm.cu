@@ -129,6 +129,26 @@ int encode_3d(PFN_cuTensorMapEncodeTiled_v12000 encode, CUtensorMap *map, CUtens
     return r == CUDA_SUCCESS ? TPGEMM_OK : TPGEMM_ERR_CUDA;
 }
 
+// B (bf16, [slices][K][N] with row stride ldb) viewed as [slices][N/64][K][64]:
+// a box of {64 columns, 64 K rows, 2 groups} is two 64 x 64 boxes of the 3-D
+// view, side by side in shared memory. N must be a multiple of 64, so that no
+// group runs past the end of a row.
+int encode_b_grouped(PFN_cuTensorMapEncodeTiled_v12000 encode, CUtensorMap *map, const void *ptr, int64_t N,
+                     int64_t K, int64_t ldb, int64_t slices, int64_t slice_ld) {
+    cuuint64_t dims[4] = {64, static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(N / 64),
+                          static_cast<cuuint64_t>(slices)};
+    uint64_t s3 = slices > 1 ? static_cast<uint64_t>(slice_ld * 2) : static_cast<uint64_t>(ldb * 2 * K);
+    s3 = (s3 + 15) / 16 * 16;
+    if (s3 >= (1ull << 40)) s3 = (1ull << 40) - 16;
+    cuuint64_t strides[3] = {static_cast<cuuint64_t>(ldb * 2), 128, s3};
+    cuuint32_t box[4] = {64, 64, 2, 1};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(ptr), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? TPGEMM_OK : TPGEMM_ERR_CUDA;
+}
+
 // One tiled launch, in the general form: `batch` slices of A, C, D (rows rows
 // each, or one stack of rows rows for a grouped GEMM) and `bslices` slices of
 // B. A stride of 0 shares one slice between all batches.
@@ -159,10 +179,12 @@ int build_tiled(PFN_cuTensorMapEncodeTiled_v12000 encode, const TiledCall &c, CU
     const uint64_t map_n = static_cast<uint64_t>(n_tma > 0 ? n_tma : c.N);
     const int64_t aslices = c.sA ? c.batch : 1, bslices = c.sB ? c.bslices : 1;
     const int64_t cslices = (use_c && c.sC) ? c.batch : 1;
+    const bool b_grouped = c.N % 64 == 0;
     if (encode_3d(encode, tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, c.A, c.K, c.rows, tma_stride(c.rows, c.K, c.lda, 2),
                   aslices, c.sA, 2, 64, tpg::tiled::BM) ||
-        encode_3d(encode, tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, c.B, c.N, c.K, tma_stride(c.K, c.N, c.ldb, 2),
-                  bslices, c.sB, 2, 64, 64) ||
+        (b_grouped ? encode_b_grouped(encode, tmB, c.B, c.N, c.K, c.ldb, bslices, c.sB)
+                   : encode_3d(encode, tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, c.B, c.N, c.K,
+                               tma_stride(c.K, c.N, c.ldb, 2), bslices, c.sB, 2, 64, 64)) ||
         encode_3d(encode, tmD, out_dt, c.D, map_n, c.rows, tma_stride(c.rows, c.N, c.ldd, elt), c.batch, c.sD, elt,
                   chunk, tpg::tiled::BM) ||
         encode_3d(encode, tmC, out_dt, use_c ? c.C : c.D, map_n, c.rows,
@@ -180,6 +202,7 @@ int build_tiled(PFN_cuTensorMapEncodeTiled_v12000 encode, const TiledCall &c, CU
     p->sC = c.sC;
     p->sD = c.sD;
     p->n_tma = static_cast<int32_t>(n_tma);
+    p->b_grouped = b_grouped ? 1 : 0;
     p->alpha = c.alpha;
     p->beta = c.beta;
     p->C = use_c ? c.C : nullptr;
