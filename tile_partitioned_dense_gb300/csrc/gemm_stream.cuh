@@ -13,12 +13,13 @@
 // 128-column panels of B through a deep TMA ring; A (a few hundred KB) stays
 // in L2.
 //
-// Output ownership is per 128-column panel. With SPLIT == 2 the panel's K
-// range is cut in two between the two CTAs of a cluster: the second CTA sends
-// its fp32 partial sum through distributed shared memory and the first adds
-// it in a fixed order (first half + second half) and writes the panel, so the
-// result is deterministic and no panel is written by two CTAs (no atomics,
-// no global split-K buffer).
+// Output ownership is per 128-column panel. With SPLIT > 1 (2, 3 or 4) the
+// panel's K range is cut into SPLIT nearly equal parts between the CTAs of a
+// cluster: the other CTAs send their fp32 partial sums through distributed
+// shared memory and the first adds them in a fixed order (part 0 + part 1 +
+// ...) and writes the panel, so the result is deterministic and no panel is
+// written by two CTAs (no atomics, no global split-K buffer). Few panels (a
+// narrow N) get a larger SPLIT, so that every SM streams part of B.
 //
 // Warp roles as in the tiled kernel: warp 0 TMA producer, warp 1 TMEM owner
 // and MMA issuer, warps 2-5 epilogue (one TMEM lane quarter each, i.e. 32
@@ -56,7 +57,9 @@ constexpr int EPI_THREADS = 128;
 constexpr uint32_t B_BOX_BYTES = BK * 64 * 2;   // 64 K rows x 64 N
 constexpr uint32_t B_STAGE_BYTES = 2 * B_BOX_BYTES;
 constexpr uint32_t TMEM_COLS = 128;             // two accumulators of up to 64 columns
-constexpr uint32_t NUM_BARS = 2 * MAX_STAGES + 2 + 2 + 2 + 2 + 1;
+constexpr int MAX_SPLIT = 4;
+// full, empty; tfull, tempty; red_full (per sending CTA, two slots); red_empty; drain
+constexpr uint32_t NUM_BARS = 2 * MAX_STAGES + 2 + 2 + 2 * (MAX_SPLIT - 1) + 2 + 1;
 constexpr uint32_t BAR_BYTES = NUM_BARS * 8 + 16;
 constexpr uint32_t SMEM_LIMIT = 232448;
 
@@ -67,16 +70,21 @@ __host__ __device__ constexpr uint32_t stage_bytes(int mt) { return B_STAGE_BYTE
 __host__ __device__ constexpr uint32_t red_row_bytes(int mt) { return static_cast<uint32_t>(mt) * 4u + 16u; }
 __host__ __device__ constexpr uint32_t red_slot_bytes(int mt) { return BN * red_row_bytes(mt); }
 
-// Stage count that fits beside the barrier block and (for SPLIT 2) the two
-// reduction slots, leaving 1 KB to align the base.
+// Partial-sum slots of the first CTA of a cluster: two per sending CTA.
+__host__ __device__ constexpr uint32_t red_bytes(int mt, int split) {
+    return split > 1 ? static_cast<uint32_t>(split - 1) * 2u * red_slot_bytes(mt) : 0u;
+}
+
+// Stage count that fits beside the barrier block and the reduction slots,
+// leaving 1 KB to align the base.
 __host__ __device__ constexpr int max_stages(int mt, int split) {
-    const uint32_t fixed = 1024 + BAR_BYTES + (split == 2 ? 2 * red_slot_bytes(mt) : 0);
-    const int s = static_cast<int>((SMEM_LIMIT - fixed) / stage_bytes(mt));
+    const uint32_t fixed = 1024 + BAR_BYTES + red_bytes(mt, split);
+    const int s = fixed < SMEM_LIMIT ? static_cast<int>((SMEM_LIMIT - fixed) / stage_bytes(mt)) : 0;
     return s > MAX_STAGES ? MAX_STAGES : s;
 }
 
 __host__ __device__ constexpr uint32_t smem_bytes(int mt, int stages, int split) {
-    return 1024 + stages * stage_bytes(mt) + (split == 2 ? 2 * red_slot_bytes(mt) : 0) + BAR_BYTES;
+    return 1024 + stages * stage_bytes(mt) + red_bytes(mt, split) + BAR_BYTES;
 }
 
 __device__ __forceinline__ bool drain_wait(uint64_t *bar, uint32_t parity, uint64_t limit_ns) {
@@ -93,7 +101,7 @@ template <bool kOutF32, int SPLIT, bool kEpi>
 __global__ void __launch_bounds__(THREADS, 1)
     gemm_stream_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                        const StreamParams p) {
-    static_assert(SPLIT == 1 || SPLIT == 2, "K split of 1 or 2");
+    static_assert(SPLIT >= 1 && SPLIT <= MAX_SPLIT, "K split of 1 to 4");
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                 ~static_cast<uintptr_t>(1023));
@@ -102,30 +110,29 @@ __global__ void __launch_bounds__(THREADS, 1)
     const uint32_t a_bytes = a_slot_bytes(MT);
     const uint32_t st_bytes = stage_bytes(MT);
     uint8_t *ring = smem;                                  // stage s: B boxes, then the A box
-    uint8_t *red = smem + S * st_bytes;                    // SPLIT 2: two partial-sum slots
-    uint8_t *barblk = red + (SPLIT == 2 ? 2 * red_slot_bytes(MT) : 0);
+    uint8_t *red = smem + S * st_bytes;                    // SPLIT > 1: partial-sum slots
+    uint8_t *barblk = red + red_bytes(MT, SPLIT);
     uint64_t *bars = reinterpret_cast<uint64_t *>(barblk);
     uint64_t *full = bars;
     uint64_t *empty = bars + MAX_STAGES;
     uint64_t *tfull = bars + 2 * MAX_STAGES;
     uint64_t *tempty = tfull + 2;
-    uint64_t *red_full = tempty + 2;  // in the first CTA: the second CTA's partial has landed
-    uint64_t *red_empty = red_full + 2; // in the second CTA: the first CTA has consumed it
+    uint64_t *red_full = tempty + 2;  // in the first CTA, [sender - 1][slot]: that CTA's partial has landed
+    uint64_t *red_empty = red_full + 2 * (MAX_SPLIT - 1); // in each sender, [slot]: the first CTA has consumed it
     uint64_t *drain = red_empty + 2;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(barblk + NUM_BARS * 8);
     volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(barblk + NUM_BARS * 8 + 4);
 
     const uint32_t warp = threadIdx.x / 32;
     const uint32_t lane = threadIdx.x % 32;
-    const uint32_t rank = SPLIT == 2 ? cluster_ctarank() : 0u;
+    const uint32_t rank = SPLIT > 1 ? cluster_ctarank() : 0u;
     const int32_t cluster_id = static_cast<int32_t>(blockIdx.x) / SPLIT;
     const int32_t num_clusters = static_cast<int32_t>(gridDim.x) / SPLIT;
 
-    // K blocks of this CTA: the first CTA of a pair takes the first half.
-    const int32_t kb_half = (p.kb + SPLIT - 1) / SPLIT;
-    const int32_t kb_begin = SPLIT == 2 ? static_cast<int32_t>(rank) * kb_half : 0;
-    const int32_t kb_end = SPLIT == 2 ? (rank == 0 ? kb_half : p.kb) : p.kb;
-    const int32_t my_kb = kb_end - kb_begin; // the host guarantees >= 1
+    // K blocks of this CTA: part `rank` of SPLIT nearly equal parts, in order.
+    const int32_t kb_begin = static_cast<int32_t>(rank) * p.kb / SPLIT;
+    const int32_t kb_end = (static_cast<int32_t>(rank) + 1) * p.kb / SPLIT;
+    const int32_t my_kb = kb_end - kb_begin; // the host guarantees kb >= SPLIT, so >= 1
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < MAX_STAGES; ++s) {
@@ -135,9 +142,9 @@ __global__ void __launch_bounds__(THREADS, 1)
         for (int b = 0; b < 2; ++b) {
             mbar_init(&tfull[b], 1);
             mbar_init(&tempty[b], EPI_THREADS / 32);
-            mbar_init(&red_full[b], EPI_THREADS);
             mbar_init(&red_empty[b], EPI_THREADS);
         }
+        for (int b = 0; b < 2 * (MAX_SPLIT - 1); ++b) mbar_init(&red_full[b], EPI_THREADS);
         mbar_init(drain, 1);
         *abort_flag = 0u;
         fence_barrier_init();
@@ -151,8 +158,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         tmem_relinquish();
     }
     tc_fence_before();
-    if (SPLIT == 2)
-        cluster_sync(); // the peer's barriers are initialised before any remote arrive
+    if (SPLIT > 1)
+        cluster_sync(); // the peers' barriers are initialised before any remote arrive
     else
         __syncthreads();
     tc_fence_after();
@@ -292,11 +299,11 @@ __global__ void __launch_bounds__(THREADS, 1)
                 acc_phase ^= 1u;
             }
 
-            if (SPLIT == 2) {
-                uint8_t *slot = red + rslot * red_slot_bytes(MT);
+            if (SPLIT > 1) {
                 const uint32_t row_off = col * red_row_bytes(MT);
-                if (rank == 1) {
-                    // Hand the partial sum of the second K half to the first CTA.
+                if (rank != 0) {
+                    // Hand this part's partial sum to the first CTA.
+                    uint8_t *slot = red + ((rank - 1) * 2 + rslot) * red_slot_bytes(MT);
                     const bool free_ok =
                         mbar_wait_cluster(&red_empty[rslot], rphase ^ 1u, ctl, kStatusTimeoutReduce);
                     if (named_barrier_or(1, EPI_THREADS, !free_ok)) {
@@ -306,29 +313,34 @@ __global__ void __launch_bounds__(THREADS, 1)
                     const uint32_t dst = map_to_rank(smem_addr(slot + row_off), 0);
                     for (int m = 0; m < MT; m += 4)
                         st_cluster_v4(dst + m * 4, v[m], v[m + 1], v[m + 2], v[m + 3]);
-                    mbar_arrive_cluster(map_to_rank(smem_addr(&red_full[rslot]), 0));
+                    mbar_arrive_cluster(map_to_rank(smem_addr(&red_full[(rank - 1) * 2 + rslot]), 0));
                 } else {
-                    const bool have =
-                        mbar_wait_cluster(&red_full[rslot], rphase, ctl, kStatusTimeoutReduce);
-                    if (named_barrier_or(1, EPI_THREADS, !have)) {
-                        ok = false;
-                        break;
+                    // part 0 + part 1 + ... + part SPLIT-1, always in this order
+                    for (int r = 1; r < SPLIT && ok; ++r) {
+                        const uint8_t *slot = red + ((r - 1) * 2 + rslot) * red_slot_bytes(MT);
+                        const bool have =
+                            mbar_wait_cluster(&red_full[(r - 1) * 2 + rslot], rphase, ctl, kStatusTimeoutReduce);
+                        if (named_barrier_or(1, EPI_THREADS, !have)) {
+                            ok = false;
+                            break;
+                        }
+                        const float4 *src = reinterpret_cast<const float4 *>(slot + row_off);
+                        for (int m = 0; m < MT; m += 4) {
+                            const float4 w = src[m / 4];
+                            v[m] += w.x;
+                            v[m + 1] += w.y;
+                            v[m + 2] += w.z;
+                            v[m + 3] += w.w;
+                        }
+                        mbar_arrive_cluster(map_to_rank(smem_addr(&red_empty[rslot]), static_cast<uint32_t>(r)));
                     }
-                    const float4 *src = reinterpret_cast<const float4 *>(slot + row_off);
-                    for (int m = 0; m < MT; m += 4) {
-                        const float4 w = src[m / 4];
-                        v[m] += w.x; // first K half + second K half, always in this order
-                        v[m + 1] += w.y;
-                        v[m + 2] += w.z;
-                        v[m + 3] += w.w;
-                    }
-                    mbar_arrive_cluster(map_to_rank(smem_addr(&red_empty[rslot]), 1));
+                    if (!ok) break;
                 }
                 if (++rslot == 2) {
                     rslot = 0;
                     rphase ^= 1u;
                 }
-                if (rank == 1) continue; // the first CTA owns and writes the panel
+                if (rank != 0) continue; // the first CTA owns and writes the panel
             }
 
             if (n < p.N) {
@@ -354,8 +366,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
 
     tc_fence_before();
-    if (SPLIT == 2)
-        cluster_sync(); // no CTA leaves while its peer may still arrive on its barriers
+    if (SPLIT > 1)
+        cluster_sync(); // no CTA leaves while a peer may still arrive on its barriers
     else
         __syncthreads();
     if (warp == 1) {

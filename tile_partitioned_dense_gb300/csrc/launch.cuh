@@ -92,6 +92,7 @@ int tiled_pair_clusters(bool f32, int num_sms);
 // stream_inst.cu
 cudaError_t stream_launch(const StreamLaunch &l);
 bool stream_set_limits();
-int stream_split_clusters(bool f32, int num_sms, int smem);
+// co-resident clusters of `split` CTAs of the streaming kernel with `smem` bytes each
+int stream_split_clusters(bool f32, int num_sms, int smem, int split);
 
 } // namespace tpg

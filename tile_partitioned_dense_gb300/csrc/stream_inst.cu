@@ -1,5 +1,5 @@
 // Instantiations of the small-M weight-streaming kernel (bf16 / fp32 output,
-// K split 1 or 2, plain or fused epilogue). The host library reaches them
+// K split 1 to 4, plain or fused epilogue). The host library reaches them
 // through the functions below.
 #include "launch.cuh"
 
@@ -19,7 +19,28 @@ cudaError_t launch_one(const StreamLaunch &l) {
 }
 template <bool kOutF32, bool kEpi>
 cudaError_t launch_split(const StreamLaunch &l) {
-    return l.split == 2 ? launch_one<kOutF32, 2, kEpi>(l) : launch_one<kOutF32, 1, kEpi>(l);
+    switch (l.split) {
+    case 1: return launch_one<kOutF32, 1, kEpi>(l);
+    case 2: return launch_one<kOutF32, 2, kEpi>(l);
+    case 3: return launch_one<kOutF32, 3, kEpi>(l);
+    case 4: return launch_one<kOutF32, 4, kEpi>(l);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+template <bool kOutF32, bool kEpi>
+bool set_limits_all() {
+    bool ok = set_limit<kOutF32, 1, kEpi>();
+    ok = set_limit<kOutF32, 2, kEpi>() && ok;
+    ok = set_limit<kOutF32, 3, kEpi>() && ok;
+    ok = set_limit<kOutF32, 4, kEpi>() && ok;
+    return ok;
+}
+
+template <int kSplit>
+int clusters_of(bool f32, const cudaLaunchConfig_t &cfg, int *n) {
+    return f32 ? static_cast<int>(cudaOccupancyMaxActiveClusters(n, stream::gemm_stream_kernel<true, kSplit, false>, &cfg))
+               : static_cast<int>(cudaOccupancyMaxActiveClusters(n, stream::gemm_stream_kernel<false, kSplit, false>, &cfg));
 }
 } // namespace
 
@@ -29,34 +50,30 @@ cudaError_t stream_launch(const StreamLaunch &l) {
 }
 
 bool stream_set_limits() {
-    bool ok = set_limit<false, 1, false>();
-    ok = set_limit<true, 1, false>() && ok;
-    ok = set_limit<false, 2, false>() && ok;
-    ok = set_limit<true, 2, false>() && ok;
-    ok = set_limit<false, 1, true>() && ok;
-    ok = set_limit<true, 1, true>() && ok;
-    ok = set_limit<false, 2, true>() && ok;
-    ok = set_limit<true, 2, true>() && ok;
+    bool ok = set_limits_all<false, false>();
+    ok = set_limits_all<true, false>() && ok;
+    ok = set_limits_all<false, true>() && ok;
+    ok = set_limits_all<true, true>() && ok;
     return ok;
 }
 
-int stream_split_clusters(bool f32, int num_sms, int smem) {
+int stream_split_clusters(bool f32, int num_sms, int smem, int split) {
+    if (split < 2 || split > stream::MAX_SPLIT) return -1;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(2 * (num_sms / 2), 1, 1);
+    cfg.gridDim = dim3(static_cast<unsigned>(split * (num_sms / split)), 1, 1);
     cfg.blockDim = dim3(stream::THREADS, 1, 1);
     cfg.dynamicSmemBytes = static_cast<size_t>(smem);
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(split);
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int n = 0;
-    const cudaError_t e =
-        f32 ? cudaOccupancyMaxActiveClusters(&n, stream::gemm_stream_kernel<true, 2, false>, &cfg)
-            : cudaOccupancyMaxActiveClusters(&n, stream::gemm_stream_kernel<false, 2, false>, &cfg);
-    if (e != cudaSuccess) {
+    const int e = split == 2 ? clusters_of<2>(f32, cfg, &n) : split == 3 ? clusters_of<3>(f32, cfg, &n)
+                                                                         : clusters_of<4>(f32, cfg, &n);
+    if (e != static_cast<int>(cudaSuccess)) {
         (void)cudaGetLastError();
         return -1;
     }

@@ -56,8 +56,8 @@ struct tpgemm_handle {
     PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
     int forced = TPGEMM_VARIANT_AUTO;
     uint64_t timeout_ns = 2000000000ull;
-    // co-resident 2-CTA clusters of the streaming kernel, per [out f32][mt/16 - 1]
-    int stream_clusters[2][4] = {{0, 0, 0, 0}, {0, 0, 0, 0}};
+    // co-resident clusters of the streaming kernel, per [out f32][K split - 2][mt/16 - 1]
+    int stream_clusters[2][3][4] = {};
     // co-resident CTA pairs of the tiled kernel in pair mode, per [out f32]
     int pair_clusters[2] = {0, 0};
 };
@@ -212,11 +212,12 @@ int build_tiled(PFN_cuTensorMapEncodeTiled_v12000 encode, const TiledCall &c, CU
     return TPGEMM_OK;
 }
 
-int stream_clusters_for(tpgemm_handle *h, bool f32, int mt, int stages) {
-    int &slot = h->stream_clusters[f32 ? 1 : 0][mt / 16 - 1];
+int stream_clusters_for(tpgemm_handle *h, bool f32, int mt, int stages, int split) {
+    int &slot = h->stream_clusters[f32 ? 1 : 0][split - 2][mt / 16 - 1];
     if (slot > 0) return slot;
-    const int n = tpg::stream_split_clusters(f32, h->num_sms, static_cast<int>(tpg::stream::smem_bytes(mt, stages, 2)));
-    slot = n > 0 ? n : h->num_sms / 2;
+    const int n = tpg::stream_split_clusters(f32, h->num_sms,
+                                             static_cast<int>(tpg::stream::smem_bytes(mt, stages, split)), split);
+    slot = n > 0 ? n : h->num_sms / split;
     return slot;
 }
 
@@ -272,18 +273,34 @@ Plan make_plan(tpgemm_handle *h, int64_t M, int64_t N, int64_t K, int out_dtype)
     pl.tile_n = tpg::stream::BN;
     pl.num_tiles = nt;
     pl.mt_pad = mt_pad;
-    // Split K across a CTA pair when one CTA per panel would leave SMs idle.
-    pl.split = (kb >= 2 && nt < 2LL * h->num_sms) ? 2 : 1;
+    // K split: each panel's K range over s CTAs of a cluster, s from 1 to 4,
+    // so that narrow outputs (few panels) still stream B on every SM. Each CTA
+    // needs at least one K block and a ring of at least 4 stages beside the
+    // reduction slots. A panel takes one time unit on one CTA, so s costs
+    // rounds(s) / s, rounds(s) being the panels over the co-resident clusters
+    // of s CTAs, plus 2% per extra CTA for the reduction.
+    const bool f32 = out_dtype == TPGEMM_OUT_F32;
+    int best_s = 1, best_clusters = h->num_sms;
+    double best_cost = 1e300;
+    for (int sp = 1; sp <= tpg::stream::MAX_SPLIT && sp <= kb; ++sp) {
+        const int st = tpg::stream::max_stages(mt_pad, sp);
+        if (st < 4) continue;
+        const int clusters = sp == 1 ? h->num_sms : stream_clusters_for(h, f32, mt_pad, st, sp);
+        if (clusters < 1) continue;
+        const int64_t rounds = (nt + clusters - 1) / clusters;
+        const double cost = static_cast<double>(rounds) / sp * (1.0 + 0.02 * (sp - 1));
+        if (cost < best_cost - 1e-9) {
+            best_cost = cost;
+            best_s = sp;
+            best_clusters = clusters;
+        }
+    }
+    pl.split = best_s;
     pl.stages = tpg::stream::max_stages(mt_pad, pl.split);
     pl.smem = static_cast<int>(tpg::stream::smem_bytes(mt_pad, pl.stages, pl.split));
-    if (pl.split == 2) {
-        const int clusters = stream_clusters_for(h, out_dtype == TPGEMM_OUT_F32, mt_pad, pl.stages);
-        const int64_t c = nt < clusters ? nt : clusters;
-        pl.grid = static_cast<int>(2 * c);
-        pl.cluster = 2;
-    } else {
-        pl.grid = static_cast<int>(nt < h->num_sms ? nt : h->num_sms);
-    }
+    const int64_t c = nt < best_clusters ? nt : best_clusters;
+    pl.grid = static_cast<int>(pl.split * c);
+    pl.cluster = pl.split;
     return pl;
 }
 
