@@ -60,6 +60,25 @@ def dist_env():
     return world, rank, local
 
 
+def max_over_ranks(values, world: int, device=None):
+    """Element-wise maximum of `values` over all ranks: the slowest rank's
+    times, which bound the whole job. Needs an initialised process group when
+    world > 1 (NCCL with CUDA tensors in the bench; gloo on CPU in the tests)."""
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t.cpu()]
+
+
+def job_throughput(world: int, steps: int, work_per_step: float, span_ms: float, scale: float) -> float:
+    """Whole-job rate: the work of all ranks (each ran `steps` steps of
+    `work_per_step` units) over the slowest rank's time span_ms, in units of
+    `scale` per second (1e12 for TFLOP/s, 1e9 for GB/s)."""
+    return world * steps * work_per_step / (span_ms * 1e-3) / scale
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -459,28 +478,22 @@ def run_ours(args):
     clocks = sampler.stop()
 
     # max over ranks of the timed-region time
-    t = torch.tensor([span, eager], dtype=torch.float64, device="cuda")
-    if world > 1:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    span_max, eager_max = float(t[0]), float(t[1])
+    span_max, eager_max = max_over_ranks([span, eager], world, device="cuda")
     avg_max = span_max / args.steps  # average launch duration over the timed region
     if cfg.name == "decode":
         unit = "GB/s"
-        value = world * args.steps * cfg.K * cfg.N * 2 / (span_max * 1e-3) / 1e9
+        value = job_throughput(world, args.steps, cfg.K * cfg.N * 2, span_max, 1e9)
     else:
         unit = "TFLOP/s"
-        value = world * args.steps * cfg.flops / (span_max * 1e-3) / 1e12
+        value = job_throughput(world, args.steps, cfg.flops, span_max, 1e12)
 
     e2e = None
     if not args.no_e2e:
         e2e_steps = max(3, min(args.steps, 20))
         ms, bi, bo = time_e2e(torch, tpd, h, wl, e2e_steps)
-        tt = torch.tensor([ms], dtype=torch.float64, device="cuda")
-        if world > 1:
-            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms = float(tt[0])
-        ev = (world * cfg.K * cfg.N * 2 / (ms * 1e-3) / 1e9) if cfg.name == "decode" else \
-            (world * cfg.flops / (ms * 1e-3) / 1e12)
+        ms = max_over_ranks([ms], world, device="cuda")[0]
+        ev = job_throughput(world, 1, cfg.K * cfg.N * 2, ms, 1e9) if cfg.name == "decode" else \
+            job_throughput(world, 1, cfg.flops, ms, 1e12)
         e2e = {"value": round(ev, 3), "unit": unit, "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo,
                "ms_per_step": round(ms, 4), "steps": e2e_steps,
                "path": "pinned host -> device copies, gemm_run (C ABI), device -> pinned host copy"}
