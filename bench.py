@@ -206,6 +206,38 @@ class Workload:
                             c.alpha, c.beta, self.out_code, stream)
 
 
+class TorchMatmul:
+    """The same workload through torch.matmul (cuBLAS), on the same rotating
+    device buffers: the comparison row of the measurement (not our path)."""
+
+    def __init__(self, wl):
+        self.wl = wl
+
+    def run(self, tpd, h, i, stream):
+        import torch
+        s = self.wl.sets[i % self.wl.nsets]
+        c = self.wl.cfg
+        if s["C"] is not None and c.beta != 0.0:
+            torch.addmm(s["C"], s["A"], s["B"], beta=c.beta, alpha=c.alpha, out=s["D"])
+        elif c.alpha == 1.0:
+            torch.mm(s["A"], s["B"], out=s["D"])
+        else:
+            torch.addmm(s["D"], s["A"], s["B"], beta=0.0, alpha=c.alpha, out=s["D"])
+        return 0
+
+
+def torch_matmul_entry(torch, tpd, h, wl, steps, ours_ms, barrier):
+    span, _ = time_launches(torch, tpd, h, TorchMatmul(wl), steps, 5, barrier)
+    ms = span / steps
+    c = wl.cfg
+    if c.name == "decode":
+        value, unit = c.K * c.N * 2 / (ms * 1e-3) / 1e9, "GB/s"
+    else:
+        value, unit = c.flops / (ms * 1e-3) / 1e12, "TFLOP/s"
+    return {"value": round(value, 2), "unit": unit, "ms_per_step": round(ms, 5), "steps": steps,
+            "ours_over_torch": round(ms / ours_ms, 3)}
+
+
 class MultiWorkload:
     """Batched (bmm) or grouped (mixture-of-experts) GEMM through
     gemm_run_batched / gemm_run_grouped, with rotating device copies."""
@@ -500,7 +532,9 @@ def run_ours(args):
 
     per_config = {}
     launches = args.steps
+    torch_rows = {}
     if not args.no_extra:
+        torch_rows[cfg.name] = torch_matmul_entry(torch, tpd, h, wl, min(args.steps, 400), avg_max, barrier)
         for name in ["qkv", "mlp_down", "decode", "square"]:
             if name == cfg.name:
                 continue
@@ -521,6 +555,7 @@ def run_ours(args):
                                 "eager_ms_per_step": round(eager2 / steps2, 5),
                                 "steps": steps2, "roofline": roofline_entry(c2, k2, avg2, peaks, peak_src),
                                 "config": config_entry(c2, w2, w2.nsets), "plan": p2}
+            torch_rows[name] = torch_matmul_entry(torch, tpd, h, w2, steps2, avg2, barrier)
             launches += steps2
             del w2
             torch.cuda.empty_cache()
@@ -564,6 +599,10 @@ def run_ours(args):
 
     if not args.no_extra:
         per_config["tp_overlay_chunks"] = chunk_tradeoff(torch, tpd, h)
+        per_config["torch_matmul"] = {
+            "note": "torch.matmul / addmm (cuBLAS) on the same shapes and rotating buffers, timed the same way; "
+                    "a comparison row, not this library's path",
+            "rows": torch_rows}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
