@@ -20,8 +20,11 @@
  *  - "cuTile Rust explained", "Ownership crosses the launch boundary" and "The
  *    useful boundary": the mutable output is split into disjoint tiles, each
  *    owned by exactly one tile program; inputs are shared and read-only. Here
- *    every D tile is written by exactly one CTA, with no atomics and no
- *    split-K accumulation in global memory.
+ *    every D tile is written by exactly one CTA (or CTA pair), with no
+ *    atomics and no split-K accumulation in global memory. The small-M
+ *    variant may split a panel's K range over the 2 to 4 CTAs of one cluster;
+ *    the partial sums meet in distributed shared memory and the panel's owner
+ *    adds them in a fixed order.
  *  - Same page, "Why scoped graph capture helps borrowing": only operations
  *    that allocate nothing are safe to capture and replay. gemm_run allocates
  *    nothing and never synchronises.
@@ -250,8 +253,10 @@ int gemm_force_variant(tpgemm_handle *h, int variant);
 /*
  * Reports what gemm_run would launch for this problem, without launching:
  * the variant, the output tile (rows x cols of D), the number of tiles, the
- * grid size in CTAs, the cluster size, the dynamic shared memory per CTA and
- * the number of kernel launches. Any output pointer may be NULL.
+ * grid size in CTAs, the cluster size (2 for CTA pairs; for the streaming
+ * variant the number of CTAs that share a panel's K range, 1 to 4), the
+ * dynamic shared memory per CTA and the number of kernel launches. Any output
+ * pointer may be NULL.
  */
 int gemm_query_plan(tpgemm_handle *h, int64_t M, int64_t N, int64_t K, int out_dtype,
                     int *variant, int *tile_m, int *tile_n, int64_t *num_tiles, int *grid,
