@@ -44,6 +44,11 @@
  * on the host before anything is enqueued. A device-side timeout (a pipeline
  * wait that exceeded its limit) is recorded in the handle's status word and
  * reported by gemm_sync_status. No function aborts, exits or traps.
+ *
+ * Threads: gemm_run, gemm_run_epilogue, gemm_run_batched, gemm_run_grouped,
+ * gemm_run_chunked and gemm_query_plan may be called on one handle from
+ * several host threads at once. gemm_force_variant and gemm_destroy must not
+ * overlap any other call on the handle.
  */
 #ifndef TPGEMM_H
 #define TPGEMM_H

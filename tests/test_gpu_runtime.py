@@ -142,3 +142,44 @@ def test_row_parallel_shards(h, integer):
         assert_bit_exact(bits(got), want, "row shards")
     else:
         assert_within_tolerance(bits(got), want, torch.bfloat16, "row shards")
+
+
+def test_concurrent_host_threads_on_one_fresh_handle():
+    """Four host threads make their first calls on a new handle at once (its
+    occupancy caches start empty), each on its own stream with its own shape
+    and kernel variant; every result is bit-exact."""
+    import threading
+    h2 = tpd.gemm_create(0)
+    shapes = [(300, 520, 256), (16, 4096, 1024), (64, 2048, 512), (1000, 264, 128)]
+    inputs, outs, errors = [], [], []
+    for i, (M, N, K) in enumerate(shapes):
+        A, B, _ = make_inputs(CONFIGS["tiny"], integer=True, M=M, N=N, K=K, seed=40 + i)
+        inputs.append((A, B, to_device(A), to_device(B)))
+        outs.append(torch.full((M, N), float("nan"), device="cuda"))
+    streams = [torch.cuda.Stream() for _ in shapes]
+    torch.cuda.synchronize()
+    barrier = threading.Barrier(len(shapes))
+
+    def work(i):
+        M, N, K = shapes[i]
+        _, _, Ad, Bd = inputs[i]
+        barrier.wait()
+        for _ in range(3):
+            st = tpd.gemm_run(h2, M, N, K, Ad.data_ptr(), K, Bd.data_ptr(), N, None, N, outs[i].data_ptr(), N,
+                              1.0, 0.0, tpd.OUT_F32, streams[i].cuda_stream)
+            if st != tpd.OK:
+                errors.append((i, st))
+
+    threads = [threading.Thread(target=work, args=(i,)) for i in range(len(shapes))]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    torch.cuda.synchronize()
+    try:
+        assert not errors, errors
+        assert tpd.gemm_sync_status(h2, None) == tpd.OK
+        for i, (A, B, _, _) in enumerate(inputs):
+            assert_bit_exact(bits(outs[i]), oracle_out(A, B, None, 1.0, 0.0, torch.float32), f"thread {i}")
+    finally:
+        tpd.gemm_destroy(h2)

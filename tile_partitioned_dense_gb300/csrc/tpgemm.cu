@@ -6,6 +6,7 @@
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cstdint>
 #include <cstdlib>
 #include <cstring>
@@ -56,21 +57,29 @@ struct tpgemm_handle {
     PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
     int forced = TPGEMM_VARIANT_AUTO;
     uint64_t timeout_ns = 2000000000ull;
+    // Occupancy caches, filled on first use. Calls from several host threads
+    // may fill one at the same time; they store the same value, and the
+    // atomics make that well defined.
     // co-resident clusters of the streaming kernel, per [out f32][K split - 2][mt/16 - 1]
-    int stream_clusters[2][3][4] = {};
+    std::atomic<int> stream_clusters[2][3][4] = {};
     // co-resident CTA pairs of the tiled kernel in pair mode, per [out f32]
-    int pair_clusters[2] = {0, 0};
+    std::atomic<int> pair_clusters[2] = {};
 };
 
 namespace {
 
+// Makes `dev` the calling thread's device for the scope of a call, and binds
+// its primary context to the thread. The binding matters: the tensor-map
+// encoder is a driver call that needs a current context, and a fresh host
+// thread has none until some runtime call creates the binding (cudaGetDevice
+// does not), so it is made here on every call, not only on a device switch.
 struct DeviceGuard {
     int prev = -1;
     bool switched = false;
     explicit DeviceGuard(int dev) {
-        if (cudaGetDevice(&prev) == cudaSuccess && prev != dev) {
-            switched = cudaSetDevice(dev) == cudaSuccess;
-        }
+        const bool other = cudaGetDevice(&prev) == cudaSuccess && prev != dev;
+        const bool set = cudaSetDevice(dev) == cudaSuccess;
+        switched = other && set;
     }
     ~DeviceGuard() {
         if (switched) cudaSetDevice(prev);
@@ -213,20 +222,24 @@ int build_tiled(PFN_cuTensorMapEncodeTiled_v12000 encode, const TiledCall &c, CU
 }
 
 int stream_clusters_for(tpgemm_handle *h, bool f32, int mt, int stages, int split) {
-    int &slot = h->stream_clusters[f32 ? 1 : 0][split - 2][mt / 16 - 1];
-    if (slot > 0) return slot;
+    std::atomic<int> &slot = h->stream_clusters[f32 ? 1 : 0][split - 2][mt / 16 - 1];
+    const int cached = slot.load(std::memory_order_relaxed);
+    if (cached > 0) return cached;
     const int n = tpg::stream_split_clusters(f32, h->num_sms,
                                              static_cast<int>(tpg::stream::smem_bytes(mt, stages, split)), split);
-    slot = n > 0 ? n : h->num_sms / split;
-    return slot;
+    const int v = n > 0 ? n : h->num_sms / split;
+    slot.store(v, std::memory_order_relaxed);
+    return v;
 }
 
 int pair_clusters_for(tpgemm_handle *h, bool f32) {
-    int &slot = h->pair_clusters[f32 ? 1 : 0];
-    if (slot > 0) return slot;
+    std::atomic<int> &slot = h->pair_clusters[f32 ? 1 : 0];
+    const int cached = slot.load(std::memory_order_relaxed);
+    if (cached > 0) return cached;
     const int n = tpg::tiled_pair_clusters(f32, h->num_sms);
-    slot = n > 0 ? n : h->num_sms / 2;
-    return slot;
+    const int v = n > 0 ? n : h->num_sms / 2;
+    slot.store(v, std::memory_order_relaxed);
+    return v;
 }
 
 Plan make_plan(tpgemm_handle *h, int64_t M, int64_t N, int64_t K, int out_dtype) {
@@ -893,7 +906,9 @@ extern "C" int gemm_run_noalloc(int64_t M, int64_t N, int64_t K, const void *A, 
     // The scratch this kernel needs is one status word whatever M, N and K are,
     // so the 16-byte array serves every size gemm_check_args accepts.
     int dev = -1;
-    if (cudaGetDevice(&dev) != cudaSuccess) return TPGEMM_ERR_CUDA;
+    // cudaSetDevice on the current device binds its primary context to this
+    // thread, which the tensor-map encoder below needs (see DeviceGuard).
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaSetDevice(dev) != cudaSuccess) return TPGEMM_ERR_CUDA;
     NoallocDevice *nd = nullptr;
     const int st = noalloc_setup(dev, &nd);
     if (st != TPGEMM_OK) return st;
