@@ -674,7 +674,10 @@ def run_ours(args):
             "roofline": roofline_entry(cfg, kernel, avg_max, peaks, peak_src),
             "cpu_baseline": cpu,
             "e2e": e2e,
-            "gpu_launches": launches,
+            # our kernel launches inside the headline timed region (one per step),
+            # and inside every timed region of this run (per_config included)
+            "gpu_launches": args.steps,
+            "gpu_launches_all_timed_regions": launches,
             "clocks": clocks,
             "plan": plan,
             "kernel_avg_ms": round(avg_max, 5),
