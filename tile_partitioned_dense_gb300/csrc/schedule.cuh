@@ -86,10 +86,11 @@ __host__ __device__ __forceinline__ bool work_item(const Schedule &s, int64_t t,
 // `split` column pieces; with fewer tiles than workers every tile is cut, so
 // that more workers have work. split is taken from {1, 2, 4} (up to
 // max_split) to minimise the estimated time of the cut part: its rounds times
-// the cost of one piece. The tiles are bound by operand loads, and a piece
-// 1/f of a tile wide still loads all of the tile's A rows, so a piece costs
-// a_share + (1 - a_share) / f of a whole tile, a_share being A's part of the
-// operand bytes a whole tile loads per k-block.
+// the cost of one piece. A piece 1/f of a tile wide still loads all of the
+// tile's A rows, so it is costed at a_share + (1 - a_share) / f of a whole
+// tile, a_share being A's part of the operand bytes a whole tile loads per
+// k-block. With max_split = 2 the choice is the same for any piece cost
+// between 1/2 and 1 of a tile: halves win exactly when 2 * rest <= cap.
 __host__ __device__ __forceinline__ Schedule make_schedule(int64_t mt, int64_t nt, int32_t group_m, int64_t cap,
                                                            int32_t max_split, double a_share) {
     Schedule s;
