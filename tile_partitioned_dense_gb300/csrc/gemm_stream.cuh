@@ -58,6 +58,9 @@ constexpr uint32_t B_BOX_BYTES = BK * 64 * 2;   // 64 K rows x 64 N
 constexpr uint32_t B_STAGE_BYTES = 2 * B_BOX_BYTES;
 constexpr uint32_t TMEM_COLS = 128;             // two accumulators of up to 64 columns
 constexpr int MAX_SPLIT = 4;
+// K blocks of a CTA's first panel whose B boxes are prefetched into L2 before
+// the wait on the previous grid.
+constexpr int PREFETCH_KB = 16;
 // full, empty; tfull, tempty; red_full (per sending CTA, two slots); red_empty; drain
 constexpr uint32_t NUM_BARS = 2 * MAX_STAGES + 2 + 2 + 2 * (MAX_SPLIT - 1) + 2 + 1;
 constexpr uint32_t BAR_BYTES = NUM_BARS * 8 + 16;
@@ -152,6 +155,20 @@ __global__ void __launch_bounds__(THREADS, 1)
     if (warp == 0 && lane == 0) {
         prefetch_tensormap(&tmA);
         prefetch_tensormap(&tmB);
+        // B is only read, and the prefetch is a hint (see tma_prefetch_2d), so
+        // the first K blocks of this CTA's first panel can start on their way
+        // from HBM while the previous grid in the stream is still finishing:
+        // this CTA runs on an SM that grid has already left, during the
+        // ragged end of its last panels. Only clusters that stream more than
+        // one panel do it. A cluster with a single panel is short, and its
+        // first loads would queue behind the prefetches.
+        const int32_t n0 = cluster_id * BN;
+        const int32_t pf_end =
+            p.nt > num_clusters ? kb_begin + (my_kb < PREFETCH_KB ? my_kb : PREFETCH_KB) : kb_begin;
+        for (int32_t kb = kb_begin; kb < pf_end; ++kb) {
+            tma_prefetch_2d(&tmB, n0, kb * BK);
+            if (n0 + 64 < p.N) tma_prefetch_2d(&tmB, n0 + 64, kb * BK);
+        }
     }
     if (warp == 1) {
         tmem_alloc(tmem_slot, TMEM_COLS);
@@ -311,8 +328,9 @@ __global__ void __launch_bounds__(THREADS, 1)
                         break;
                     }
                     const uint32_t dst = map_to_rank(smem_addr(slot + row_off), 0);
-                    for (int m = 0; m < MT; m += 4)
-                        st_cluster_v4(dst + m * 4, v[m], v[m + 1], v[m + 2], v[m + 3]);
+#pragma unroll
+                    for (int m = 0; m < 64; m += 4)
+                        if (m < MT) st_cluster_v4(dst + m * 4, v[m], v[m + 1], v[m + 2], v[m + 3]);
                     mbar_arrive_cluster(map_to_rank(smem_addr(&red_full[(rank - 1) * 2 + rslot]), 0));
                 } else {
                     // part 0 + part 1 + ... + part SPLIT-1, always in this order
@@ -325,7 +343,9 @@ __global__ void __launch_bounds__(THREADS, 1)
                             break;
                         }
                         const float4 *src = reinterpret_cast<const float4 *>(slot + row_off);
-                        for (int m = 0; m < MT; m += 4) {
+#pragma unroll
+                        for (int m = 0; m < 64; m += 4) {
+                            if (m >= MT) break;
                             const float4 w = src[m / 4];
                             v[m] += w.x;
                             v[m + 1] += w.y;
@@ -344,7 +364,9 @@ __global__ void __launch_bounds__(THREADS, 1)
             }
 
             if (n < p.N) {
-                for (int m = 0; m < p.M; ++m) {
+#pragma unroll
+                for (int m = 0; m < 64; ++m) {
+                    if (m >= p.M) break;
                     float x = p.alpha * v[m];
                     if constexpr (kOutF32) {
                         if (has_beta)

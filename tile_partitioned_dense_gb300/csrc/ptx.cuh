@@ -203,6 +203,17 @@ __device__ __forceinline__ void tma_load_2d(const CUtensorMap *m, uint64_t *bar,
         : "memory");
 }
 
+// L2 prefetch of one box of a 2-D tensor map: a hint that moves no data into
+// shared memory and completes on no barrier. L2 is the point of coherence for
+// every load of this GPU, so a prefetch issued before an earlier grid has
+// finished writing the same bytes can never make a later load see stale data.
+__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap *m, int32_t c0, int32_t c1) {
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                     reinterpret_cast<uint64_t>(m)),
+                 "r"(c0), "r"(c1)
+                 : "memory");
+}
+
 __device__ __forceinline__ void tma_load_2d_hint(const CUtensorMap *m, uint64_t *bar, void *dst,
                                                  int32_t c0, int32_t c1, uint64_t policy) {
     asm volatile(
