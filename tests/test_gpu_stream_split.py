@@ -24,9 +24,11 @@ def h():
     tpd.gemm_destroy(handle)
 
 
-# (M, N, K): on a 152-SM GB300 these plan K splits of 4 (32 panels), 3 (48
-# panels), 2 (224 panels) and 1 (a single K block); a ragged K (65 blocks);
-# 48 and 64 token rows, whose reduction slots leave room for smaller splits.
+# (M, N, K): on a 152-SM GB300 these plan K splits of 4 (32 panels), 2 (48
+# panels: 46 clusters of 3 would leave two panels for a second round; 224
+# panels) and 1 (a single K block); a ragged K (65 blocks); 48 and 64 token
+# rows, whose reduction slots leave room for smaller splits (64 x 512 x 8192
+# plans a split of 3).
 SHAPES = [(16, 4096, 14336), (16, 6144, 4096), (16, 28672, 4096), (32, 1024, 64), (5, 2048, 4100),
           (33, 640, 1000), (64, 512, 8192), (1, 4096, 2048)]
 
@@ -80,3 +82,40 @@ def test_stream_split4_fused_epilogue(h):
     assert tpd.gemm_sync_status(h, None) == tpd.OK
     want, _ = oracle.gemm_rows_epilogue(A, B, None, 1.0, 0.0, oracle.OUT_F32, bias=bias, act=oracle.ACT_RELU, aux=aux)
     assert_bit_exact(bits(D), want, "split-4 stream + fused epilogue")
+
+
+def test_b_written_by_the_previous_gemm(h):
+    """The streaming kernel prefetches the first B blocks of its first panel
+    into L2 before it waits for the previous grid in the stream. Here B is the
+    output of the GEMM launched just before it, and the two overlap through
+    programmatic dependent launch, three times over with new values each time:
+    every second GEMM must read what the first one wrote. Integer inputs keep
+    both products exact (|B| <= 256 is exact in bf16; the sums stay below
+    2^24), so the comparison with the oracle is bit for bit."""
+    K1, M2, N2, K2 = 16, 16, 28672, 4096
+    plan = tpd.gemm_query_plan(h, M2, N2, K2, tpd.OUT_F32)
+    assert plan["variant"] == tpd.VARIANT_STREAM
+    # more panels than clusters: the prefetching case
+    assert plan["num_tiles"] > plan["grid"] // plan["cluster"], plan
+    g = torch.Generator().manual_seed(23)
+    ints = lambda *shape: torch.randint(-4, 5, shape, generator=g).to(torch.bfloat16)
+    B1, A2 = ints(K1, N2), ints(M2, K2)
+    A1s = [ints(K2, K1) for _ in range(3)]
+    B1d, A2d = B1.cuda(), A2.cuda()
+    A1ds = [a.cuda() for a in A1s]
+    B2 = torch.empty((K2, N2), dtype=torch.bfloat16, device="cuda")
+    outs = [torch.full((M2, N2), float("nan"), device="cuda") for _ in range(3)]
+    s = torch.cuda.current_stream().cuda_stream
+    for i in range(3):
+        st = tpd.gemm_run(h, K2, N2, K1, A1ds[i].data_ptr(), K1, B1d.data_ptr(), N2, None, N2, B2.data_ptr(), N2,
+                          1.0, 0.0, tpd.OUT_BF16, s)
+        assert st == tpd.OK
+        st = tpd.gemm_run(h, M2, N2, K2, A2d.data_ptr(), K2, B2.data_ptr(), N2, None, N2, outs[i].data_ptr(), N2,
+                          1.0, 0.0, tpd.OUT_F32, s)
+        assert st == tpd.OK
+    assert tpd.gemm_sync_status(h, None) == tpd.OK
+    for i in range(3):
+        b2 = torch.from_numpy(oracle_out(A1s[i], B1, None, 1.0, 0.0, torch.bfloat16).view(np.int16)).view(
+            torch.bfloat16)
+        want = oracle_out(A2, b2, None, 1.0, 0.0, torch.float32)
+        assert_bit_exact(bits(outs[i]), want, f"chain {i}")

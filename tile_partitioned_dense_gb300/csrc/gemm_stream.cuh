@@ -68,10 +68,10 @@ constexpr uint32_t SMEM_LIMIT = 232448;
 
 __host__ __device__ constexpr uint32_t a_slot_bytes(int mt) { return static_cast<uint32_t>(mt) * 128u; }
 __host__ __device__ constexpr uint32_t stage_bytes(int mt) { return B_STAGE_BYTES + a_slot_bytes(mt); }
-// fp32 partial-sum row of one D column: MT values plus 16 bytes of padding so
-// that consecutive threads' 16-byte stores fall in different bank groups.
-__host__ __device__ constexpr uint32_t red_row_bytes(int mt) { return static_cast<uint32_t>(mt) * 4u + 16u; }
-__host__ __device__ constexpr uint32_t red_slot_bytes(int mt) { return BN * red_row_bytes(mt); }
+// One fp32 partial sum of a panel, laid out [MT / 4][BN][4]: the thread of D
+// column c keeps its token rows 4g .. 4g+3 in the 16 bytes at (g * BN + c) * 16,
+// so a warp's 32 columns fill 512 contiguous bytes (no bank conflicts).
+__host__ __device__ constexpr uint32_t red_slot_bytes(int mt) { return static_cast<uint32_t>(BN) * mt * 4u; }
 
 // Partial-sum slots of the first CTA of a cluster: two per sending CTA.
 __host__ __device__ constexpr uint32_t red_bytes(int mt, int split) {
@@ -317,7 +317,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             }
 
             if (SPLIT > 1) {
-                const uint32_t row_off = col * red_row_bytes(MT);
+                const uint32_t col_off = col * 16u;
                 if (rank != 0) {
                     // Hand this part's partial sum to the first CTA.
                     uint8_t *slot = red + ((rank - 1) * 2 + rslot) * red_slot_bytes(MT);
@@ -327,10 +327,10 @@ __global__ void __launch_bounds__(THREADS, 1)
                         ok = false;
                         break;
                     }
-                    const uint32_t dst = map_to_rank(smem_addr(slot + row_off), 0);
+                    const uint32_t dst = map_to_rank(smem_addr(slot + col_off), 0);
 #pragma unroll
                     for (int m = 0; m < 64; m += 4)
-                        if (m < MT) st_cluster_v4(dst + m * 4, v[m], v[m + 1], v[m + 2], v[m + 3]);
+                        if (m < MT) st_cluster_v4(dst + m * (BN * 4), v[m], v[m + 1], v[m + 2], v[m + 3]);
                     mbar_arrive_cluster(map_to_rank(smem_addr(&red_full[(rank - 1) * 2 + rslot]), 0));
                 } else {
                     // part 0 + part 1 + ... + part SPLIT-1, always in this order
@@ -342,11 +342,11 @@ __global__ void __launch_bounds__(THREADS, 1)
                             ok = false;
                             break;
                         }
-                        const float4 *src = reinterpret_cast<const float4 *>(slot + row_off);
+                        const float4 *src = reinterpret_cast<const float4 *>(slot + col_off);
 #pragma unroll
                         for (int m = 0; m < 64; m += 4) {
                             if (m >= MT) break;
-                            const float4 w = src[m / 4];
+                            const float4 w = src[(m / 4) * BN];
                             v[m] += w.x;
                             v[m + 1] += w.y;
                             v[m + 2] += w.z;
