@@ -283,6 +283,20 @@ int gemm_query_plan(tpgemm_handle *h, int64_t M, int64_t N, int64_t K, int out_d
  * needed.
  */
 int gemm_schedule_workers(int64_t mt, int64_t nt, int cap, int pair, int allow_split);
+
+/*
+ * Host copy of the streaming variant's K-split choice. For nt panels of 128
+ * columns, kb K blocks of 64 and mt_pad token rows (16, 32, 48 or 64),
+ * returns the number s of CTAs (1..4) of a cluster that share each panel's K
+ * range: the s with the least rounds(s) / s * (1 + 0.02 (s - 1)), rounds(s)
+ * being the panels over the clusters of s CTAs that fit at once. s = 1 runs on
+ * num_sms CTAs; clusters[s - 2] (three entries, s = 2..4) gives the clusters of
+ * s CTAs the occupancy API reports (0: not possible). s is also limited to kb
+ * and to splits whose reduction slots leave a ring of at least 4 stages.
+ * gemm_run computes the cluster counts on the device and calls the same
+ * function. Returns TPGEMM_ERR_INVALID_ARG on bad arguments. No GPU is needed.
+ */
+int gemm_stream_split(int64_t nt, int64_t kb, int mt_pad, int num_sms, const int *clusters);
 int64_t gemm_schedule_tiles(int64_t mt, int64_t nt, int group_m, int cap, int pair, int allow_split, int worker,
                             int32_t *out, int64_t cap_items);
 

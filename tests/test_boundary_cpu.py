@@ -215,6 +215,38 @@ def test_schedule_split_choice_follows_the_cost_model():
     assert tpd.gemm_schedule_workers(1, 32, 76, True) == 64
 
 
+# Co-resident clusters of 2, 3 and 4 CTAs of the streaming kernel that the
+# occupancy API reported on a 152-SM GB300 (any ring depth).
+GB300_CLUSTERS = (76, 46, 36)
+
+
+@pytest.mark.parametrize("nt,kb,mt,want", [
+    (224, 64, 16, 2),   # decode 16x28672x4096: 3 rounds of 76 pairs (1.53) beat 2 rounds of 152 CTAs (2.0)
+    (48, 64, 16, 2),    # N = 6144: one round of 48 pairs (0.51); 46 triples would need a second round (0.69)
+    (40, 64, 32, 3),    # N = 5120: one round of triples (0.35) beats pairs (0.51) and quads (2 rounds, 0.53)
+    (32, 224, 16, 4),   # 16x4096x14336: one round of 32 quads (0.27)
+    (112, 64, 16, 1),   # N = 14336: one round of 112 CTAs (1.0) beats 2 rounds of pairs (1.02)
+    (32, 1, 16, 1),     # a single K block cannot be split
+    (32, 2, 16, 2),     # two K blocks: at most two parts
+    (4, 128, 64, 3),    # 64 token rows: four parts leave too small a ring, so three
+])
+def test_stream_split_choice(nt, kb, mt, want):
+    assert tpd.gemm_stream_split(nt, kb, mt, 152, GB300_CLUSTERS) == want
+
+
+def test_stream_split_skips_impossible_cluster_sizes():
+    # no cluster of 3 or 4 fits: 40 panels fall back to pairs
+    assert tpd.gemm_stream_split(40, 64, 16, 152, (76, 0, 0)) == 2
+    # nothing but single CTAs
+    assert tpd.gemm_stream_split(40, 64, 16, 152, (0, 0, 0)) == 1
+    lib = tpd.load_library()
+    arr = (ctypes.c_int32 * 3)(76, 46, 36)
+    for bad in [(0, 64, 16, 152), (40, 0, 16, 152), (40, 64, 8, 152), (40, 64, 80, 152), (40, 64, 24, 152),
+                (40, 64, 16, 0)]:
+        assert lib.gemm_stream_split(*bad, arr) == tpd.ERR_INVALID_ARG, bad
+    assert lib.gemm_stream_split(40, 64, 16, 152, None) == tpd.ERR_INVALID_ARG
+
+
 def test_schedule_grouped_raster_order():
     # the first tiles of a band walk down the band before moving right
     order = tpd.gemm_schedule_tiles(40, 8, 16, 1, 0)

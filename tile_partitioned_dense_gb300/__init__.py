@@ -81,6 +81,7 @@ def load_library() -> ctypes.CDLL:
             "gemm_query_plan": (i32, [vp, i64, i64, i64, i32, pi32, pi32, pi32, pi64, pi32, pi32, pi32, pi32]),
             "gemm_schedule_tiles": (i64, [i64, i64, i32, i32, i32, i32, i32, ctypes.POINTER(ctypes.c_int32), i64]),
             "gemm_schedule_workers": (i32, [i64, i64, i32, i32, i32]),
+            "gemm_stream_split": (i32, [i64, i64, i32, i32, pi32]),
             "gemm_watchdog_selftest": (i32, [vp, ctypes.c_uint64, vp]),
             "gemm_num_sms": (i32, [vp]),
             "gemm_run_noalloc": (i32, [i64, i64, i64, vp, i64, vp, i64, vp, i64, vp, i64, f32, f32, i32, vp,
@@ -171,6 +172,13 @@ def gemm_query_plan(h, M, N, K, out_dtype) -> dict:
 
 def gemm_schedule_workers(mt: int, nt: int, cap: int, pair: bool = False, allow_split: bool = True) -> int:
     return load_library().gemm_schedule_workers(mt, nt, cap, int(pair), int(allow_split))
+
+
+def gemm_stream_split(nt: int, kb: int, mt_pad: int, num_sms: int, clusters) -> int:
+    """K split (1..4) the streaming variant picks for nt panels and kb K blocks,
+    given the co-resident clusters of 2, 3 and 4 CTAs."""
+    arr = (ctypes.c_int32 * 3)(*[int(c) for c in clusters])
+    return load_library().gemm_stream_split(nt, kb, mt_pad, num_sms, arr)
 
 
 def gemm_schedule_tiles(mt: int, nt: int, group_m: int, cap: int, worker: int, pair: bool = False,

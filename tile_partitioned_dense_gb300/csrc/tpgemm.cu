@@ -221,6 +221,33 @@ int build_tiled(PFN_cuTensorMapEncodeTiled_v12000 encode, const TiledCall &c, CU
     return TPGEMM_OK;
 }
 
+// K split of the streaming variant: each panel's K range over s CTAs of a
+// cluster, s from 1 to 4, so that narrow outputs (few panels) still stream B on
+// every SM. Each CTA needs at least one K block and a ring of at least 4
+// stages beside the reduction slots. A panel takes one time unit on one CTA,
+// so s costs rounds(s) / s, rounds(s) being the panels over the co-resident
+// clusters of s CTAs, plus 2% per extra CTA for the reduction. clusters[s - 2]
+// is the number of clusters of s CTAs that fit at once (0: s not possible).
+// Returns s and the cluster count it runs on.
+int stream_split_choice(int64_t nt, int64_t kb, int mt_pad, int num_sms, const int *clusters, int *clusters_used) {
+    int best_s = 1, best_clusters = num_sms;
+    double best_cost = 1e300;
+    for (int sp = 1; sp <= tpg::stream::MAX_SPLIT && sp <= kb; ++sp) {
+        if (tpg::stream::max_stages(mt_pad, sp) < 4) continue;
+        const int c = sp == 1 ? num_sms : clusters[sp - 2];
+        if (c < 1) continue;
+        const int64_t rounds = (nt + c - 1) / c;
+        const double cost = static_cast<double>(rounds) / sp * (1.0 + 0.02 * (sp - 1));
+        if (cost < best_cost - 1e-9) {
+            best_cost = cost;
+            best_s = sp;
+            best_clusters = c;
+        }
+    }
+    if (clusters_used) *clusters_used = best_clusters;
+    return best_s;
+}
+
 int stream_clusters_for(tpgemm_handle *h, bool f32, int mt, int stages, int split) {
     std::atomic<int> &slot = h->stream_clusters[f32 ? 1 : 0][split - 2][mt / 16 - 1];
     const int cached = slot.load(std::memory_order_relaxed);
@@ -286,28 +313,14 @@ Plan make_plan(tpgemm_handle *h, int64_t M, int64_t N, int64_t K, int out_dtype)
     pl.tile_n = tpg::stream::BN;
     pl.num_tiles = nt;
     pl.mt_pad = mt_pad;
-    // K split: each panel's K range over s CTAs of a cluster, s from 1 to 4,
-    // so that narrow outputs (few panels) still stream B on every SM. Each CTA
-    // needs at least one K block and a ring of at least 4 stages beside the
-    // reduction slots. A panel takes one time unit on one CTA, so s costs
-    // rounds(s) / s, rounds(s) being the panels over the co-resident clusters
-    // of s CTAs, plus 2% per extra CTA for the reduction.
     const bool f32 = out_dtype == TPGEMM_OUT_F32;
-    int best_s = 1, best_clusters = h->num_sms;
-    double best_cost = 1e300;
-    for (int sp = 1; sp <= tpg::stream::MAX_SPLIT && sp <= kb; ++sp) {
+    int clusters[tpg::stream::MAX_SPLIT - 1];
+    for (int sp = 2; sp <= tpg::stream::MAX_SPLIT; ++sp) {
         const int st = tpg::stream::max_stages(mt_pad, sp);
-        if (st < 4) continue;
-        const int clusters = sp == 1 ? h->num_sms : stream_clusters_for(h, f32, mt_pad, st, sp);
-        if (clusters < 1) continue;
-        const int64_t rounds = (nt + clusters - 1) / clusters;
-        const double cost = static_cast<double>(rounds) / sp * (1.0 + 0.02 * (sp - 1));
-        if (cost < best_cost - 1e-9) {
-            best_cost = cost;
-            best_s = sp;
-            best_clusters = clusters;
-        }
+        clusters[sp - 2] = st >= 4 && sp <= kb ? stream_clusters_for(h, f32, mt_pad, st, sp) : 0;
     }
+    int best_clusters = h->num_sms;
+    const int best_s = stream_split_choice(nt, kb, mt_pad, h->num_sms, clusters, &best_clusters);
     pl.split = best_s;
     pl.stages = tpg::stream::max_stages(mt_pad, pl.split);
     pl.smem = static_cast<int>(tpg::stream::smem_bytes(mt_pad, pl.stages, pl.split));
@@ -487,6 +500,12 @@ int gemm_query_plan(tpgemm_handle *h, int64_t M, int64_t N, int64_t K, int out_d
     if (smem_bytes) *smem_bytes = pl.smem;
     if (launches) *launches = pl.launches;
     return TPGEMM_OK;
+}
+
+int gemm_stream_split(int64_t nt, int64_t kb, int mt_pad, int num_sms, const int *clusters) {
+    if (nt < 1 || kb < 1 || mt_pad < 16 || mt_pad > 64 || mt_pad % 16 != 0 || num_sms < 1 || !clusters)
+        return TPGEMM_ERR_INVALID_ARG;
+    return stream_split_choice(nt, kb, mt_pad, num_sms, clusters, nullptr);
 }
 
 int gemm_schedule_workers(int64_t mt, int64_t nt, int cap, int pair, int allow_split) {
