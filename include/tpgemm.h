@@ -24,7 +24,10 @@
  *    atomics and no split-K accumulation in global memory. The small-M
  *    variant may split a panel's K range over the 2 to 4 CTAs of one cluster;
  *    the partial sums meet in distributed shared memory and the panel's owner
- *    adds them in a fixed order.
+ *    adds them in a fixed order. So may the tiled kernel when an output has
+ *    few 128 x 256 tiles: the 2 or 4 CTAs of a cluster share a tile's K range,
+ *    each owns a quarter (or half) of the tile's columns, and each adds the
+ *    others' partial sums of its columns in rank order before its epilogue.
  *  - Same page, "Why scoped graph capture helps borrowing": only operations
  *    that allocate nothing are safe to capture and replay. gemm_run allocates
  *    nothing and never synchronises.
@@ -259,7 +262,8 @@ int gemm_force_variant(tpgemm_handle *h, int variant);
  * Reports what gemm_run would launch for this problem, without launching:
  * the variant, the output tile (rows x cols of D), the number of tiles, the
  * grid size in CTAs, the cluster size (2 for CTA pairs; for the streaming
- * variant the number of CTAs that share a panel's K range, 1 to 4), the
+ * variant the number of CTAs that share a panel's K range, 1 to 4; for 1-CTA
+ * tiles the number that share a tile's K range, 1, 2 or 4), the
  * dynamic shared memory per CTA and the number of kernel launches. Any output
  * pointer may be NULL.
  */
@@ -297,6 +301,18 @@ int gemm_schedule_workers(int64_t mt, int64_t nt, int cap, int pair, int allow_s
  * function. Returns TPGEMM_ERR_INVALID_ARG on bad arguments. No GPU is needed.
  */
 int gemm_stream_split(int64_t nt, int64_t kb, int mt_pad, int num_sms, const int *clusters);
+
+/*
+ * Host copy of the tiled kernel's K-split choice, made before the choice
+ * between 1-CTA tiles and CTA pairs. For `tiles` 128 x 256 output tiles of kb
+ * K blocks of 64, returns 4 when kb >= 4 and every tile gets a cluster of four
+ * CTAs at once (tiles <= cap4, the clusters of four the occupancy API
+ * reports), else 2 when kb >= 2 and tiles <= cap2, else 1: no split, the
+ * persistent schedule of gemm_schedule_tiles. gemm_run and gemm_run_noalloc
+ * call the same function (gemm_run only when no variant is forced). Returns
+ * TPGEMM_ERR_INVALID_ARG on bad arguments. No GPU is needed.
+ */
+int gemm_tiled_ksplit(int64_t tiles, int64_t kb, int cap2, int cap4);
 int64_t gemm_schedule_tiles(int64_t mt, int64_t nt, int group_m, int cap, int pair, int allow_split, int worker,
                             int32_t *out, int64_t cap_items);
 

@@ -247,6 +247,29 @@ def test_stream_split_skips_impossible_cluster_sizes():
     assert lib.gemm_stream_split(40, 64, 16, 152, None) == tpd.ERR_INVALID_ARG
 
 
+@pytest.mark.parametrize("tiles,kb,want", [
+    (32, 64, 4),    # 256 x 4096 x 4096: 32 tiles, each on a cluster of four
+    (36, 64, 4),    # as many tiles as clusters of four
+    (37, 64, 2),    # one more: clusters of two
+    (64, 64, 2),    # 512 x 4096: 64 tiles on 64 pairs of CTAs
+    (76, 64, 2),
+    (77, 64, 1),    # more tiles than pairs: the persistent schedule
+    (224, 64, 1),   # 256 x 28672: plenty of tiles
+    (8, 3, 2),      # three K blocks: at most two parts
+    (8, 1, 1),      # a single K block cannot be shared
+])
+def test_tiled_ksplit_choice(tiles, kb, want):
+    assert tpd.gemm_tiled_ksplit(tiles, kb, 76, 36) == want
+
+
+def test_tiled_ksplit_rejects_bad_arguments():
+    lib = tpd.load_library()
+    for bad in [(0, 64, 76, 36), (8, 0, 76, 36), (8, 64, -1, 36), (8, 64, 76, -1)]:
+        assert lib.gemm_tiled_ksplit(*bad) == tpd.ERR_INVALID_ARG, bad
+    # no cluster of either size fits: no split
+    assert tpd.gemm_tiled_ksplit(8, 64, 0, 0) == 1
+
+
 def test_schedule_grouped_raster_order():
     # the first tiles of a band walk down the band before moving right
     order = tpd.gemm_schedule_tiles(40, 8, 16, 1, 0)

@@ -88,13 +88,27 @@ def test_plans_match_the_design(h):
     p = tpd.gemm_query_plan(h, 16, 28672, 4096, tpd.OUT_BF16)
     assert p["variant"] == tpd.VARIANT_STREAM and p["num_tiles"] == 224 and p["cluster"] == 2
     assert p["grid"] % 2 == 0 and p["grid"] <= sms
-    # one tile: cut in two halves on two pairs, or four quarters on four CTAs
+    # few tiles: 1-CTA tiles whose K range is shared by the 4 (or 2) CTAs of a cluster
     p = tpd.gemm_query_plan(h, 256, 256, 256, tpd.OUT_F32)
-    assert p["variant"] == tpd.VARIANT_TILED_PAIR and p["grid"] == 4
+    assert p["variant"] == tpd.VARIANT_TILED and p["num_tiles"] == 2 and p["cluster"] == 4 and p["grid"] == 8
     p = tpd.gemm_query_plan(h, 100, 256, 256, tpd.OUT_F32)
-    assert p["variant"] == tpd.VARIANT_TILED and p["grid"] == 4
-    # a 128-row slice of an 8192-wide output: 32 tiles become 128 quarter tiles
-    p = tpd.gemm_query_plan(h, 128, 8192, 4096, tpd.OUT_BF16)
-    assert p["variant"] == tpd.VARIANT_TILED and p["grid"] == min(128, sms)
+    assert p["variant"] == tpd.VARIANT_TILED and p["cluster"] == 4 and p["grid"] == 4
+    p = tpd.gemm_query_plan(h, 128, 8192, 4096, tpd.OUT_BF16)  # 32 tiles
+    assert p["variant"] == tpd.VARIANT_TILED and p["cluster"] == 4 and p["grid"] == 128
+    p = tpd.gemm_query_plan(h, 512, 4096, 4096, tpd.OUT_BF16)  # 64 tiles: pairs of CTAs
+    assert p["variant"] == tpd.VARIANT_TILED and p["cluster"] == 2 and p["grid"] == 128
+    p = tpd.gemm_query_plan(h, 512, 4096, 64, tpd.OUT_BF16)  # one K block: nothing to share
+    assert p["variant"] == tpd.VARIANT_TILED_PAIR and p["cluster"] == 2
+    p = tpd.gemm_query_plan(h, 1024, 4096, 4096, tpd.OUT_BF16)  # 128 tiles: more than 76 pairs
+    assert p["variant"] == tpd.VARIANT_TILED_PAIR
+    # forced 1-CTA tiles keep the column pieces: one tile cut into four quarters on four CTAs
+    assert tpd.gemm_force_variant(h, tpd.VARIANT_TILED) == tpd.OK
+    try:
+        p = tpd.gemm_query_plan(h, 100, 256, 256, tpd.OUT_F32)
+        assert p["variant"] == tpd.VARIANT_TILED and p["cluster"] == 1 and p["grid"] == 4
+        p = tpd.gemm_query_plan(h, 128, 8192, 4096, tpd.OUT_BF16)  # 32 tiles -> 128 quarter tiles
+        assert p["cluster"] == 1 and p["grid"] == min(128, sms)
+    finally:
+        tpd.gemm_force_variant(h, tpd.VARIANT_AUTO)
     p = tpd.gemm_query_plan(h, 5, 5, 0, tpd.OUT_F32)
     assert p["variant"] == tpd.VARIANT_EPILOGUE_ONLY

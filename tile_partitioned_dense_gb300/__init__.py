@@ -82,6 +82,7 @@ def load_library() -> ctypes.CDLL:
             "gemm_schedule_tiles": (i64, [i64, i64, i32, i32, i32, i32, i32, ctypes.POINTER(ctypes.c_int32), i64]),
             "gemm_schedule_workers": (i32, [i64, i64, i32, i32, i32]),
             "gemm_stream_split": (i32, [i64, i64, i32, i32, pi32]),
+            "gemm_tiled_ksplit": (i32, [i64, i64, i32, i32]),
             "gemm_watchdog_selftest": (i32, [vp, ctypes.c_uint64, vp]),
             "gemm_num_sms": (i32, [vp]),
             "gemm_run_noalloc": (i32, [i64, i64, i64, vp, i64, vp, i64, vp, i64, vp, i64, f32, f32, i32, vp,
@@ -179,6 +180,12 @@ def gemm_stream_split(nt: int, kb: int, mt_pad: int, num_sms: int, clusters) -> 
     given the co-resident clusters of 2, 3 and 4 CTAs."""
     arr = (ctypes.c_int32 * 3)(*[int(c) for c in clusters])
     return load_library().gemm_stream_split(nt, kb, mt_pad, num_sms, arr)
+
+
+def gemm_tiled_ksplit(tiles: int, kb: int, cap2: int, cap4: int) -> int:
+    """K split (1, 2 or 4) the tiled kernel picks for `tiles` 1-CTA tiles of kb K
+    blocks, given the co-resident clusters of 2 and 4 CTAs."""
+    return load_library().gemm_tiled_ksplit(tiles, kb, cap2, cap4)
 
 
 def gemm_schedule_tiles(mt: int, nt: int, group_m: int, cap: int, worker: int, pair: bool = False,

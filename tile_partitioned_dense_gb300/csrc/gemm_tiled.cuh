@@ -63,6 +63,10 @@ struct TiledParams {
     // TMA instruction where the 3-D map needs two); 0: B's map is 3-D,
     // [slice][K][N], loaded one 64 x 64 box at a time.
     int32_t b_grouped;
+    // 1-CTA mode only: the CTAs of a cluster of `ksplit` (2 or 4) share one
+    // tile, each accumulating its own part of the K range; 1 otherwise. See the
+    // kernel's K-split epilogue.
+    int32_t ksplit;
     float alpha, beta;
     const void *C;
     int64_t ldc;
@@ -150,7 +154,8 @@ struct Layout {
     static constexpr uint32_t OFF_B = OFF_A + STAGES * A_STAGE_BYTES;
     static constexpr uint32_t OFF_EPI = OFF_B + STAGES * B_STAGE_BYTES;
     static constexpr uint32_t OFF_BAR = OFF_EPI + 2 * EPI_BUF_BYTES;
-    static constexpr uint32_t NUM_BARS = 2 * STAGES + 2 + 2 + 2 + 1; // full, empty, tfull, tempty, c, drain
+    // full, empty, tfull, tempty, c, drain, K-split: peers' rings free, partials received
+    static constexpr uint32_t NUM_BARS = 2 * STAGES + 2 + 2 + 2 + 1 + 2;
     static constexpr uint32_t OFF_MISC = OFF_BAR + NUM_BARS * 8;
     static constexpr uint32_t SMEM_BYTES = OFF_MISC + 16 + 1024; // + slack to align the base
 };
@@ -179,8 +184,10 @@ __device__ __forceinline__ void settle(uint64_t ns) {
 
 // kEpi: 0 plain alpha*acc + beta*C; 1 + activation for the fused epilogue
 // (bias and aux are runtime options; the activation is compiled in, so each
-// instantiation carries only its own math).
-template <bool kOutF32, bool kPair, int kEpi, bool kGrouped = false>
+// instantiation carries only its own math). kKsplit: the 1-CTA mode's K split
+// (p.ksplit CTAs of a cluster per tile); the other instantiations carry none
+// of its code.
+template <bool kOutF32, bool kPair, int kEpi, bool kGrouped = false, bool kKsplit = false>
 __global__ void __launch_bounds__(THREADS, 1)
     gemm_tiled_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                       const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmD,
@@ -200,14 +207,22 @@ __global__ void __launch_bounds__(THREADS, 1)
     uint64_t *tempty = tfull + 2;
     uint64_t *cbar = tempty + 2;
     uint64_t *drain = cbar + 2;
+    uint64_t *ks_free = drain + 1; // K split: one arrive from each peer whose MMAs are done
+    uint64_t *ks_recv = drain + 2; // K split: the peers' partials have landed here (transaction bytes)
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::OFF_MISC);
     volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(smem + L::OFF_MISC + 4);
 
     const uint32_t warp = threadIdx.x / 32;
     const uint32_t lane = threadIdx.x % 32;
     const uint32_t rank = kPair ? cluster_ctarank() : 0u; // 0 = the even CTA, which issues the MMAs
-    const int64_t worker = static_cast<int64_t>(blockIdx.x) / CL;
-    const int64_t workers = static_cast<int64_t>(gridDim.x) / CL;
+    // K split (1-CTA mode): a cluster of ks CTAs is one worker; CTA krank
+    // accumulates K blocks [kb_lo, kb_hi) of the worker's tile.
+    const int32_t ks = (kPair || !kKsplit) ? 1 : p.ksplit;
+    const int32_t krank = ks > 1 ? static_cast<int32_t>(cluster_ctarank()) : 0;
+    const int32_t kb_lo = krank * p.kb / ks;
+    const int32_t kb_hi = (krank + 1) * p.kb / ks;
+    const int64_t worker = static_cast<int64_t>(blockIdx.x) / (CL * ks);
+    const int64_t workers = static_cast<int64_t>(gridDim.x) / (CL * ks);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
@@ -221,6 +236,10 @@ __global__ void __launch_bounds__(THREADS, 1)
             mbar_init(&cbar[b], 1);
         }
         mbar_init(drain, 1);
+        if (ks > 1) {
+            mbar_init(ks_free, static_cast<uint32_t>(ks - 1));
+            mbar_init(ks_recv, 1);
+        }
         *abort_flag = 0u;
         fence_barrier_init();
     }
@@ -240,8 +259,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
     }
     tc_fence_before();
-    if constexpr (kPair)
-        cluster_sync(); // barriers of both CTAs initialised, TMEM allocated in both
+    if (kPair || ks > 1)
+        cluster_sync(); // every CTA's barriers initialised (and TMEM allocated in both of a pair)
     else
         __syncthreads();
     tc_fence_after();
@@ -274,7 +293,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 const int32_t nload = p.b_grouped ? (cols / 64 + 1) / 2 : cols / 64;
                 const uint32_t bbytes = static_cast<uint32_t>(p.b_grouped ? 2 * nload : nload) * B_BOX_BYTES;
                 const uint32_t tx = CL * (A_STAGE_BYTES + bbytes);
-                for (int32_t kb = 0; kb < p.kb; ++kb) {
+                for (int32_t kb = kb_lo; kb < kb_hi; ++kb) {
                     if (!mbar_wait(&empty[stage], phase ^ 1u, ctl, kStatusTimeoutProducer)) {
                         ok = false;
                         break;
@@ -350,7 +369,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + acc * BN;
-                for (int32_t kb = 0; kb < p.kb; ++kb) {
+                for (int32_t kb = kb_lo; kb < kb_hi; ++kb) {
                     if (!mbar_wait(&full[stage], phase, ctl, kStatusTimeoutMma)) {
                         ok = false;
                         break;
@@ -365,10 +384,11 @@ __global__ void __launch_bounds__(THREADS, 1)
                         // B: N-major, advance 16 K rows = 2048 bytes; 64-wide N blocks are
                         // one 8 KB box apart.
                         const uint64_t bdesc = make_smem_desc_sw128(b_addr + kk * 2048, B_BOX_BYTES, 1024);
+                        const uint32_t accumulate = (kb != kb_lo || kk != 0) ? 1u : 0u;
                         if constexpr (kPair)
-                            tc_mma_f16_pair(d_tmem, adesc, bdesc, idesc, (kb | kk) != 0 ? 1u : 0u);
+                            tc_mma_f16_pair(d_tmem, adesc, bdesc, idesc, accumulate);
                         else
-                            tc_mma_f16(d_tmem, adesc, bdesc, idesc, (kb | kk) != 0 ? 1u : 0u);
+                            tc_mma_f16(d_tmem, adesc, bdesc, idesc, accumulate);
                     }
                     any = true;
                     if constexpr (kPair)
@@ -412,8 +432,56 @@ __global__ void __launch_bounds__(THREADS, 1)
         uint32_t slot = 0;
         uint32_t cphase = 0; // bit b: parity of the next wait on cbar[b]
         bool ok = true;
+        // K split: CTA krank of the cluster owns (and stores) columns
+        // [krank * ks_w, (krank + 1) * ks_w) of the tile. Once its own MMAs are
+        // done its ring is idle, and holds ks - 1 receive slots (the other
+        // CTAs' partial sums of its columns, one slot per sender) followed by
+        // ks - 1 send slots (its partial sums of each peer's columns). A slot
+        // is laid out [column / 4][row][4], so a warp's 32 rows write 512
+        // contiguous bytes; one bulk copy per peer moves a send slot into the
+        // peer's receive slot.
+        const int32_t ks_w = BN / ks;
+        const uint32_t ks_slot_bytes = static_cast<uint32_t>(BM * ks_w * 4);
+        // Columns oc0 .. oc0+31 of this CTA's own window: part 0 + part 1 + ...
+        // + part ks-1, always in that order, this CTA's part taken from r. A
+        // peer's eight cells are loaded together, so their loads overlap.
+        auto ks_combine = [&](uint32_t(&r)[32], int32_t oc0) {
+            const float4 *recv = reinterpret_cast<const float4 *>(smem + L::OFF_A) + (oc0 / 4) * BM + row;
+            const int32_t slot_f4 = static_cast<int32_t>(ks_slot_bytes / 16);
+            float acc[32];
+#pragma unroll
+            for (int rr = 0; rr < 4; ++rr) {
+                if (rr >= ks) break;
+                float part[32];
+                if (rr == krank) {
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) part[e] = __uint_as_float(r[e]);
+                } else {
+                    const float4 *src = recv + (rr < krank ? rr : rr - 1) * slot_f4;
+                    float4 t[8];
+#pragma unroll
+                    for (int g = 0; g < 8; ++g) t[g] = src[g * BM];
+#pragma unroll
+                    for (int g = 0; g < 8; ++g) {
+                        part[4 * g] = t[g].x;
+                        part[4 * g + 1] = t[g].y;
+                        part[4 * g + 2] = t[g].z;
+                        part[4 * g + 3] = t[g].w;
+                    }
+                }
+#pragma unroll
+                for (int e = 0; e < 32; ++e) acc[e] = rr == 0 ? part[e] : acc[e] + part[e];
+            }
+#pragma unroll
+            for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(acc[e]);
+        };
         WorkItem w;
         for (int64_t t = worker; ok && work_item(p.sched, t, BN, w); t += workers) {
+            const int32_t own0 = krank * ks_w; // first TMEM column of this CTA's window
+            if (ks > 1) {
+                w.n += own0;
+                w.width = ks_w;
+            }
             const Segment sg = segment_of<kGrouped>(w.m, BM * CL, p, seg);
             const int32_t m0 = sg.row0 + static_cast<int32_t>(rank) * BM; // first row of this CTA's rows
             int32_t rows_valid = sg.rows_left - static_cast<int32_t>(rank) * BM;
@@ -434,6 +502,56 @@ __global__ void __launch_bounds__(THREADS, 1)
                 break;
             }
             tc_fence_after();
+            if (ks > 1) {
+                uint8_t *ring = smem + L::OFF_A;
+                uint8_t *send = ring + static_cast<uint32_t>(ks - 1) * ks_slot_bytes;
+                // This CTA's MMAs are done, so its ring is idle: stage each peer's
+                // columns of the partial sum in the send slots.
+                for (int32_t j = 0; j < ks; ++j) {
+                    if (j == krank) continue;
+                    uint8_t *slot = send + static_cast<uint32_t>(j < krank ? j : j - 1) * ks_slot_bytes;
+                    for (int32_t g = 0; g < ks_w / 32; g += 2) {
+                        uint32_t r[2][32];
+                        const uint32_t ta = tmem_base + acc * BN + static_cast<uint32_t>(j * ks_w + g * 32) + ((q * 32u) << 16);
+                        tmem_ld32(ta, r[0]);
+                        tmem_ld32(ta + 32, r[1]);
+                        tc_wait_ld();
+#pragma unroll
+                        for (int h = 0; h < 2; ++h)
+#pragma unroll
+                            for (int i = 0; i < 32; i += 4)
+                                *reinterpret_cast<uint4 *>(slot + ((static_cast<uint32_t>((g + h) * 8 + i / 4) * BM + row) << 4)) =
+                                    make_uint4(r[h][i], r[h][i + 1], r[h][i + 2], r[h][i + 3]);
+                    }
+                }
+                fence_proxy_async_smem(); // the bulk copies read what these threads wrote
+                if (leader) {
+                    // the receive slots may be written: tell the peers; expect their bytes
+                    for (int32_t j = 0; j < ks; ++j)
+                        if (j != krank) mbar_arrive_cluster(map_to_rank(smem_addr(ks_free), static_cast<uint32_t>(j)));
+                    mbar_arrive_expect_tx(ks_recv, static_cast<uint32_t>(ks - 1) * ks_slot_bytes);
+                }
+                const bool freed = mbar_wait_cluster(ks_free, 0u, ctl, kStatusTimeoutReduce);
+                if (named_barrier_or(1, EPI_THREADS, !freed)) {
+                    ok = false;
+                    break;
+                }
+                if (leader) {
+                    for (int32_t j = 0; j < ks; ++j) {
+                        if (j == krank) continue;
+                        const uint32_t src = smem_addr(send + static_cast<uint32_t>(j < krank ? j : j - 1) * ks_slot_bytes);
+                        const uint32_t dst = map_to_rank(
+                            smem_addr(ring + static_cast<uint32_t>(krank < j ? krank : krank - 1) * ks_slot_bytes),
+                            static_cast<uint32_t>(j));
+                        bulk_copy_to_peer(dst, src, ks_slot_bytes, map_to_rank(smem_addr(ks_recv), static_cast<uint32_t>(j)));
+                    }
+                }
+                const bool parts = mbar_wait_cluster(ks_recv, 0u, ctl, kStatusTimeoutReduce);
+                if (named_barrier_or(1, EPI_THREADS, !parts)) {
+                    ok = false;
+                    break;
+                }
+            }
             const uint32_t acc_now = acc;
             auto release = [&]() {
                 // Whole accumulator read: hand it back to the MMA warp.
@@ -482,12 +600,17 @@ __global__ void __launch_bounds__(THREADS, 1)
                     }
                     cphase ^= 1u << slot;
                 }
-                const uint32_t taddr = tmem_base + acc * BN + static_cast<uint32_t>(c * CHUNK) + ((q * 32u) << 16);
+                const uint32_t taddr =
+                    tmem_base + acc * BN + static_cast<uint32_t>(own0 + c * CHUNK) + ((q * 32u) << 16);
                 uint32_t r0[32];
                 uint32_t r1[32];
                 tmem_ld32(taddr, r0);
                 if (!kOutF32) tmem_ld32(taddr + 32, r1);
                 tc_wait_ld();
+                if (ks > 1) {
+                    ks_combine(r0, c * CHUNK);
+                    if (!kOutF32) ks_combine(r1, c * CHUNK + 32);
+                }
                 if (c == nchunks - 1) release();
                 uint8_t *rowp = buf + row * 128u;
 #pragma unroll
@@ -579,11 +702,16 @@ __global__ void __launch_bounds__(THREADS, 1)
             }
         }
         if (leader) bulk_wait_group<0>();
+        // K split: a CTA that gave up early must still not exit while a peer's
+        // bulk copy into its ring may be in flight (a no-op once the copies
+        // have landed).
+        if (ks > 1 && leader && !drain_wait(ks_recv, 0u, p.timeout_ns) && p.status)
+            atomicOr(p.status, kStatusTimeoutDrain);
     }
 
     tc_fence_before();
-    if constexpr (kPair)
-        cluster_sync(); // the peer may still arrive on this CTA's barriers until here
+    if (kPair || ks > 1)
+        cluster_sync(); // a peer may still arrive on this CTA's barriers (or write its ring) until here
     else
         __syncthreads();
     if (warp == 1) {

@@ -53,6 +53,7 @@ constexpr int kEpiModes = 5;
 struct TiledLaunch {
     int grid;
     int smem;
+    int cluster; // CTAs per cluster: 2 in pair mode, the K split in 1-CTA mode, else 1
     bool pair;
     bool f32;
     cudaStream_t stream;
@@ -86,8 +87,9 @@ bool tiled_set_limits_e4();
 // grouped GEMM (plain epilogue), from tiled_inst.cu with -DTPG_EPI=0 -DTPG_GROUPED=1
 cudaError_t tiled_launch_g0(const TiledLaunch &l);
 bool tiled_set_limits_g0();
-// co-resident CTA pairs of the pair-mode kernel (plain mode), or -1
-int tiled_pair_clusters(bool f32, int num_sms);
+// co-resident clusters of `cluster` CTAs of the tiled kernel (plain mode; pair
+// mode when `pair`, whose clusters are CTA pairs), or -1
+int tiled_clusters(bool pair, bool f32, int num_sms, int cluster);
 
 // stream_inst.cu
 cudaError_t stream_launch(const StreamLaunch &l);

@@ -38,6 +38,7 @@ tpg::Schedule tiled_schedule(int64_t mt, int64_t nt, int64_t cap, bool pair, boo
 
 struct Plan {
     int variant = TPGEMM_VARIANT_AUTO;
+    int ksplit = 1; // tiled 1-CTA mode: CTAs of a cluster that share one tile's K range
     int tile_m = 0, tile_n = 0;
     int64_t num_tiles = 0;
     int grid = 0;
@@ -64,6 +65,9 @@ struct tpgemm_handle {
     std::atomic<int> stream_clusters[2][3][4] = {};
     // co-resident CTA pairs of the tiled kernel in pair mode, per [out f32]
     std::atomic<int> pair_clusters[2] = {};
+    // co-resident clusters of 2 and 4 CTAs of the tiled kernel in 1-CTA mode (K
+    // split), per [out f32][0: two, 1: four]
+    std::atomic<int> ks_clusters[2][2] = {};
 };
 
 namespace {
@@ -212,6 +216,7 @@ int build_tiled(PFN_cuTensorMapEncodeTiled_v12000 encode, const TiledCall &c, CU
     p->sD = c.sD;
     p->n_tma = static_cast<int32_t>(n_tma);
     p->b_grouped = b_grouped ? 1 : 0;
+    p->ksplit = 1;
     p->alpha = c.alpha;
     p->beta = c.beta;
     p->C = use_c ? c.C : nullptr;
@@ -263,8 +268,31 @@ int pair_clusters_for(tpgemm_handle *h, bool f32) {
     std::atomic<int> &slot = h->pair_clusters[f32 ? 1 : 0];
     const int cached = slot.load(std::memory_order_relaxed);
     if (cached > 0) return cached;
-    const int n = tpg::tiled_pair_clusters(f32, h->num_sms);
+    const int n = tpg::tiled_clusters(true, f32, h->num_sms, 2);
     const int v = n > 0 ? n : h->num_sms / 2;
+    slot.store(v, std::memory_order_relaxed);
+    return v;
+}
+
+// K split of the tiled kernel's 1-CTA mode for `tiles` 128 x 256 tiles of kb K
+// blocks: 4 when every tile gets a cluster of four CTAs at once (cap4 such
+// clusters fit) and kb >= 4, else 2 under the same conditions, else 1 (the
+// persistent schedule). Few tiles for many SMs is a short M with a narrow N;
+// there, rather than cut tiles into narrow column pieces, whose small MMAs run
+// far below the tensor pipe's rate, the CTAs of a cluster share each tile's K
+// range and exchange partial sums through distributed shared memory.
+int tiled_ksplit_choice(int64_t tiles, int64_t kb, int cap2, int cap4) {
+    if (kb >= 4 && tiles <= cap4) return 4;
+    if (kb >= 2 && tiles <= cap2) return 2;
+    return 1;
+}
+
+int ks_clusters_for(tpgemm_handle *h, bool f32, int split) {
+    std::atomic<int> &slot = h->ks_clusters[f32 ? 1 : 0][split == 4 ? 1 : 0];
+    const int cached = slot.load(std::memory_order_relaxed);
+    if (cached > 0) return cached;
+    const int n = tpg::tiled_clusters(false, f32, h->num_sms, split);
+    const int v = n > 0 ? n : h->num_sms / split;
     slot.store(v, std::memory_order_relaxed);
     return v;
 }
@@ -290,6 +318,27 @@ Plan make_plan(tpgemm_handle *h, int64_t M, int64_t N, int64_t K, int out_dtype)
     pl.variant = variant;
     pl.launches = 1;
     if (variant == TPGEMM_VARIANT_TILED || variant == TPGEMM_VARIANT_TILED_PAIR) {
+        const bool f32 = out_dtype == TPGEMM_OUT_F32;
+        // K split of 1-CTA tiles (tiled_ksplit_choice); the automatic choice only.
+        if (h->forced == TPGEMM_VARIANT_AUTO) {
+            const int64_t kbt = (K + tpg::tiled::BK - 1) / tpg::tiled::BK;
+            const int64_t tiles1 = ((M + tpg::tiled::BM - 1) / tpg::tiled::BM) * ((N + tpg::tiled::BN - 1) / tpg::tiled::BN);
+            const int ks = tiled_ksplit_choice(tiles1, kbt, ks_clusters_for(h, f32, 2), ks_clusters_for(h, f32, 4));
+            if (ks > 1) {
+                pl.variant = TPGEMM_VARIANT_TILED;
+                pl.ksplit = ks;
+                pl.tile_m = tpg::tiled::BM;
+                pl.tile_n = tpg::tiled::BN;
+                pl.num_tiles = tiles1;
+                pl.cluster = ks;
+                pl.sched = tiled_schedule((M + tpg::tiled::BM - 1) / tpg::tiled::BM,
+                                          (N + tpg::tiled::BN - 1) / tpg::tiled::BN, tiles1, false, false);
+                pl.grid = static_cast<int>(pl.sched.workers * ks);
+                pl.split = 1;
+                pl.smem = static_cast<int>(tpg::tiled::Layout<false>::SMEM_BYTES);
+                return pl;
+            }
+        }
         const bool pair = variant == TPGEMM_VARIANT_TILED_PAIR;
         const int64_t rows = tpg::tiled::BM * (pair ? 2 : 1);
         const int64_t mt = (M + rows - 1) / rows;
@@ -508,6 +557,11 @@ int gemm_stream_split(int64_t nt, int64_t kb, int mt_pad, int num_sms, const int
     return stream_split_choice(nt, kb, mt_pad, num_sms, clusters, nullptr);
 }
 
+int gemm_tiled_ksplit(int64_t tiles, int64_t kb, int cap2, int cap4) {
+    if (tiles < 1 || kb < 1 || cap2 < 0 || cap4 < 0) return TPGEMM_ERR_INVALID_ARG;
+    return tiled_ksplit_choice(tiles, kb, cap2, cap4);
+}
+
 int gemm_schedule_workers(int64_t mt, int64_t nt, int cap, int pair, int allow_split) {
     if (mt < 0 || nt < 0 || cap < 1) return TPGEMM_ERR_INVALID_ARG;
     return static_cast<int>(tiled_schedule(mt, nt, cap, pair != 0, allow_split != 0).workers);
@@ -619,10 +673,11 @@ int run_impl(tpgemm_handle *h, int64_t M, int64_t N, int64_t K, const void *A, i
         if (build_tiled(h->encode, call, &tmA, &tmB, &tmC, &tmD, &p) != TPGEMM_OK) return TPGEMM_ERR_CUDA;
         p.sched = pl.sched;
         p.mt_batch = static_cast<int32_t>(pl.sched.mt);
+        p.ksplit = pl.ksplit;
         p.status = h->status;
         p.timeout_ns = h->timeout_ns;
         p.epi = ep;
-        const tpg::TiledLaunch l{pl.grid, pl.smem, pl.variant == TPGEMM_VARIANT_TILED_PAIR, f32, stream,
+        const tpg::TiledLaunch l{pl.grid, pl.smem, pl.cluster, pl.variant == TPGEMM_VARIANT_TILED_PAIR, f32, stream,
                                  &tmA, &tmB, &tmC, &tmD, &p, nullptr};
         return launch_tiled(fused ? 1 + ep.act : 0, l);
     }
@@ -717,7 +772,7 @@ int gemm_run_batched(tpgemm_handle *h, int64_t batch, int64_t M, int64_t N, int6
     p.status = h->status;
     p.timeout_ns = h->timeout_ns;
     const int smem = static_cast<int>(pair ? tpg::tiled::Layout<true>::SMEM_BYTES : tpg::tiled::Layout<false>::SMEM_BYTES);
-    const tpg::TiledLaunch l{static_cast<int>(p.sched.workers * (pair ? 2 : 1)), smem, pair, f32, stream,
+    const tpg::TiledLaunch l{static_cast<int>(p.sched.workers * (pair ? 2 : 1)), smem, pair ? 2 : 1, pair, f32, stream,
                              &tmA, &tmB, &tmC, &tmD, &p, nullptr};
     return launch_tiled(0, l);
 }
@@ -783,7 +838,7 @@ int gemm_run_grouped(tpgemm_handle *h, int64_t groups, const int64_t *group_rows
     p.status = h->status;
     p.timeout_ns = h->timeout_ns;
     const int smem = static_cast<int>(pair ? tpg::tiled::Layout<true>::SMEM_BYTES : tpg::tiled::Layout<false>::SMEM_BYTES);
-    const tpg::TiledLaunch l{static_cast<int>(p.sched.workers * (pair ? 2 : 1)), smem, pair, f32, stream,
+    const tpg::TiledLaunch l{static_cast<int>(p.sched.workers * (pair ? 2 : 1)), smem, pair ? 2 : 1, pair, f32, stream,
                              &tmA, &tmB, &tmC, &tmD, &p, &table};
     return tpg::tiled_launch_g0(l) == cudaSuccess ? TPGEMM_OK : TPGEMM_ERR_CUDA;
 }
@@ -873,6 +928,7 @@ struct NoallocDevice {
     bool ready = false;
     uint32_t *status = nullptr; // device address of g_noalloc_scratch on this device
     int num_sms = 0;
+    int ks_clusters[2][2] = {}; // as tpgemm_handle::ks_clusters
     PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
 };
 NoallocDevice g_noalloc_dev[kNoallocMaxDevices];
@@ -908,6 +964,12 @@ int noalloc_setup(int dev, NoallocDevice **out) {
         }
         d.status = static_cast<uint32_t *>(ptr);
         d.num_sms = prop.multiProcessorCount;
+        for (int f = 0; f < 2; ++f)
+            for (int i = 0; i < 2; ++i) {
+                const int split = i ? 4 : 2;
+                const int n = tpg::tiled_clusters(false, f != 0, d.num_sms, split);
+                d.ks_clusters[f][i] = n > 0 ? n : d.num_sms / split;
+            }
         d.encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
         d.ready = true;
     }
@@ -956,12 +1018,15 @@ extern "C" int gemm_run_noalloc(int64_t M, int64_t N, int64_t K, const void *A, 
         if (build_tiled(nd->encode, call, &tmA, &tmB, &tmC, &tmD, &p) != TPGEMM_OK) return TPGEMM_ERR_CUDA;
         const int64_t mt = (M + tpg::tiled::BM - 1) / tpg::tiled::BM;
         const int64_t nt = (N + tpg::tiled::BN - 1) / tpg::tiled::BN;
-        p.sched = tiled_schedule(mt, nt, nd->num_sms, false, true);
-        const int grid = static_cast<int>(p.sched.workers);
+        // the same K split as gemm_run would choose, so the two give the same bits
+        const int ks = tiled_ksplit_choice(mt * nt, p.kb, nd->ks_clusters[f32 ? 1 : 0][0], nd->ks_clusters[f32 ? 1 : 0][1]);
+        p.sched = ks > 1 ? tiled_schedule(mt, nt, mt * nt, false, false) : tiled_schedule(mt, nt, nd->num_sms, false, true);
+        p.ksplit = ks;
+        const int grid = static_cast<int>(p.sched.workers * ks);
         p.mt_batch = static_cast<int32_t>(mt);
         p.status = nd->status;
         p.timeout_ns = 2000000000ull;
-        const tpg::TiledLaunch l{grid, static_cast<int>(tpg::tiled::SMEM_BYTES), false, f32, stream,
+        const tpg::TiledLaunch l{grid, static_cast<int>(tpg::tiled::SMEM_BYTES), ks, false, f32, stream,
                                  &tmA, &tmB, &tmC, &tmD, &p, nullptr};
         rc = tpg::tiled_launch_e0(l) == cudaSuccess ? TPGEMM_OK : TPGEMM_ERR_CUDA;
     }
