@@ -542,10 +542,20 @@ def run_ours(args):
     props = torch.cuda.get_device_properties(local)
     l2 = int(getattr(props, "L2_cache_size", 0) or 129 * 2 ** 20)
     h = tpd.gemm_create(local)
+    # Workspace for the K split of the CTA-pair kernel's last partial round. Every
+    # GEMM below runs on one stream at a time (the e2e loop keeps them on one),
+    # as a handle with a workspace requires.
+    ws_bytes = tpd.gemm_workspace_size(h)
+    ws_buf = torch.empty(ws_bytes + 256, dtype=torch.uint8, device=f"cuda:{local}")
+    st = tpd.gemm_set_workspace(h, (ws_buf.data_ptr() + 255) // 256 * 256, ws_bytes,
+                                torch.cuda.current_stream().cuda_stream)
+    if st != 0:
+        raise RuntimeError("gemm_set_workspace: " + tpd.gemm_status_string(st))
 
     cfg = CONFIGS[args.workload]
     wl = Workload(cfg, torch, l2, pinned=not args.no_e2e)
     plan = tpd.gemm_query_plan(h, cfg.M, cfg.N, cfg.K, wl.out_code)
+    plan["tail_ksplit"] = tpd.gemm_plan_tail_ksplit(h, cfg.M, cfg.N, cfg.K, wl.out_code)
     kernel = "stream" if plan["variant"] == tpd.VARIANT_STREAM else "tiled"
 
     sampler = ClockSampler(local)
@@ -588,6 +598,7 @@ def run_ours(args):
             c2 = CONFIGS[name]
             w2 = Workload(c2, torch, l2, pinned=False)
             p2 = tpd.gemm_query_plan(h, c2.M, c2.N, c2.K, w2.out_code)
+            p2["tail_ksplit"] = tpd.gemm_plan_tail_ksplit(h, c2.M, c2.N, c2.K, w2.out_code)
             k2 = "stream" if p2["variant"] == tpd.VARIANT_STREAM else "tiled"
             steps2 = max(20, min(400, int(0.4 / (c2.flops / 1.5e15 if name != "decode" else 40e-6))))
             span2, eager2 = time_launches(torch, tpd, h, w2, steps2, 10, barrier)

@@ -21,8 +21,10 @@
  *    useful boundary": the mutable output is split into disjoint tiles, each
  *    owned by exactly one tile program; inputs are shared and read-only. Here
  *    every D tile is written by exactly one CTA (or CTA pair), with no
- *    atomics and no split-K accumulation in global memory. The small-M
- *    variant may split a panel's K range over the 2 to 4 CTAs of one cluster;
+ *    atomics. Partial sums reach global memory only in the opt-in K split of
+ *    the last partial round (gemm_set_workspace); each element there is
+ *    still stored once, by its owner. The small-M variant may split a
+ *    panel's K range over the 2 to 4 CTAs of one cluster;
  *    the partial sums meet in distributed shared memory and the panel's owner
  *    adds them in a fixed order. So may the tiled kernel when an output has
  *    few 128 x 256 tiles: the 2 or 4 CTAs of a cluster share a tile's K range,
@@ -50,8 +52,8 @@
  *
  * Threads: gemm_run, gemm_run_epilogue, gemm_run_batched, gemm_run_grouped,
  * gemm_run_chunked and gemm_query_plan may be called on one handle from
- * several host threads at once. gemm_force_variant and gemm_destroy must not
- * overlap any other call on the handle.
+ * several host threads at once. gemm_force_variant, gemm_set_workspace and
+ * gemm_destroy must not overlap any other call on the handle.
  */
 #ifndef TPGEMM_H
 #define TPGEMM_H
@@ -146,7 +148,8 @@ int gemm_create(tpgemm_handle **out, int device);
  * D == C with ldd == ldc (in place) is allowed; any other overlap of D with
  * A, B or C is TPGEMM_ERR_OVERLAP. Argument errors enqueue nothing. Launch
  * failures return TPGEMM_ERR_CUDA. Allocates nothing, so it may be captured
- * into a CUDA graph. Calls on different streams may run concurrently.
+ * into a CUDA graph. Calls on different streams may run concurrently, unless
+ * the handle has a workspace (gemm_set_workspace).
  */
 int gemm_run(tpgemm_handle *h, int64_t M, int64_t N, int64_t K, const void *A, int64_t lda,
              const void *B, int64_t ldb, const void *C, int64_t ldc, void *D, int64_t ldd,
@@ -327,6 +330,53 @@ int gemm_watchdog_selftest(tpgemm_handle *h, uint64_t timeout_ns, void *stream);
 
 /* Number of SMs the handle schedules over, or a negative status. */
 int gemm_num_sms(tpgemm_handle *h);
+
+/*
+ * Optional workspace for the K split of the last partial round of the CTA-pair
+ * kernel. The persistent schedule gives every pair the same number of whole
+ * 256 x 256 tiles; the tiles left over for a last, partial round are cut in
+ * two pieces so that more pairs share them ("cuTile Rust explained",
+ * "Ownership crosses the launch boundary": each piece keeps an exclusive
+ * column half of its tile). Without a workspace a piece is a column half that
+ * runs over all of K, and it costs about as long as a whole tile. With one, a
+ * piece runs over half of K and the full tile width; the two pairs of a tile
+ * trade their fp32 partial sums of each other's column half through the
+ * workspace and each adds the other's part before its epilogue, so a piece
+ * takes about half as long. Each output element is still stored by one CTA,
+ * with no atomics, and the sum of two fp32 parts does not depend on their
+ * order, so results are the same on every run.
+ *   ws, bytes   device memory of the handle's device, 256-byte aligned;
+ *               bytes >= gemm_workspace_size(h) covers every shape (a smaller
+ *               workspace covers the shapes whose tail fits, others run
+ *               without the split). ws == NULL detaches the workspace (bytes
+ *               is then ignored) and restores the behaviour without one.
+ *   stream      the workspace's flags are cleared on this stream; enqueue the
+ *               calls that use it after that point.
+ * Ownership stays with the caller: keep the memory allocated, and do not
+ * touch it, until it is detached and every call that used it has finished.
+ * Each call uses the whole workspace, so while one is attached, calls on the
+ * handle must not overlap on the GPU: issue them on one stream, or order
+ * them with events; two replays of a captured graph that contains such calls
+ * must not overlap either. A call whose workspace wait ran out
+ * (TPGEMM_ERR_TIMEOUT in gemm_sync_status) may leave stale flags: call
+ * gemm_set_workspace again before the next call. Only gemm_run,
+ * gemm_run_epilogue and gemm_run_chunked use it. TPGEMM_ERR_INVALID_ARG for a
+ * null handle or bytes below one tail tile's need, TPGEMM_ERR_ALIGNMENT for a
+ * misaligned ws, TPGEMM_ERR_CUDA if the clearing memset fails to enqueue; a
+ * call whose operands overlap the part of the workspace it would use returns
+ * TPGEMM_ERR_OVERLAP.
+ */
+int gemm_set_workspace(tpgemm_handle *h, void *ws, int64_t bytes, void *stream);
+
+/* Workspace bytes that cover every shape on the handle's device, or a negative status. */
+int64_t gemm_workspace_size(tpgemm_handle *h);
+
+/*
+ * 1 if gemm_run would split the last partial round over K for this problem
+ * (CTA-pair plan, a tail of column halves, K > 64 and a large enough
+ * workspace attached), 0 if not, or a negative status.
+ */
+int gemm_plan_tail_ksplit(tpgemm_handle *h, int64_t M, int64_t N, int64_t K, int out_dtype);
 
 /*
  * Allocation-free GEMM (no counterpart in the paper; it serves callers that

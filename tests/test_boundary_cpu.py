@@ -61,6 +61,9 @@ def test_null_handle_is_rejected_without_gpu():
     assert tpd.gemm_force_variant(None, 0) == tpd.ERR_INVALID_ARG
     assert tpd.gemm_watchdog_selftest(None, 10000, None) == tpd.ERR_INVALID_ARG
     assert tpd.gemm_num_sms(None) == tpd.ERR_INVALID_ARG
+    assert tpd.gemm_set_workspace(None, 0x1000, 1 << 24, None) == tpd.ERR_INVALID_ARG
+    assert tpd.gemm_workspace_size(None) == tpd.ERR_INVALID_ARG
+    assert tpd.gemm_plan_tail_ksplit(None, 4096, 4096, 4096, tpd.OUT_BF16) == tpd.ERR_INVALID_ARG
 
 
 # Fake, well-separated, 16-byte aligned device addresses: gemm_check_args only

@@ -85,6 +85,9 @@ def load_library() -> ctypes.CDLL:
             "gemm_tiled_ksplit": (i32, [i64, i64, i32, i32]),
             "gemm_watchdog_selftest": (i32, [vp, ctypes.c_uint64, vp]),
             "gemm_num_sms": (i32, [vp]),
+            "gemm_set_workspace": (i32, [vp, vp, i64, vp]),
+            "gemm_workspace_size": (i64, [vp]),
+            "gemm_plan_tail_ksplit": (i32, [vp, i64, i64, i64, i32]),
             "gemm_run_noalloc": (i32, [i64, i64, i64, vp, i64, vp, i64, vp, i64, vp, i64, f32, f32, i32, vp,
                                        i32]),
         }
@@ -206,6 +209,20 @@ def gemm_watchdog_selftest(h, timeout_ns: int, stream=None) -> int:
 
 def gemm_num_sms(h) -> int:
     return load_library().gemm_num_sms(h)
+
+
+def gemm_set_workspace(h, ws, nbytes: int, stream=None) -> int:
+    """Attach (ws = device pointer) or detach (ws = None) the workspace of the
+    K split of the last partial round (see include/tpgemm.h)."""
+    return load_library().gemm_set_workspace(h, ws, int(nbytes), stream)
+
+
+def gemm_workspace_size(h) -> int:
+    return load_library().gemm_workspace_size(h)
+
+
+def gemm_plan_tail_ksplit(h, M, N, K, out_dtype) -> int:
+    return load_library().gemm_plan_tail_ksplit(h, M, N, K, out_dtype)
 
 
 def gemm_run_noalloc(M, N, K, A, lda, B, ldb, C, ldc, D, ldd, alpha, beta, out_dtype, stream,

@@ -11,10 +11,11 @@
 // Inside a CTA three roles run concurrently, connected by mbarriers:
 //   warp 0      TMA producer: per 64-wide K block, one A box (128 rows x 64 K,
 //               K-major) and the B boxes (64 K rows x 64 N each, N-major, two
-//               per instruction when N is a multiple of 64), all 128-byte
-//               swizzled, into the shared-memory ring. The TMA unit's cost
-//               grows with the number of instructions, not only with bytes, so
-//               fewer, larger boxes keep the ring fuller.
+//               per instruction when N is a multiple of 64; an odd last one,
+//               of a 64-column piece, alone), all 128-byte swizzled, into the
+//               shared-memory ring. The TMA unit's cost grows with the number
+//               of instructions, not only with bytes, so fewer, larger boxes
+//               keep the ring fuller.
 //   warp 1      allocates all 512 TMEM columns (two 128 x 256 fp32
 //               accumulators); one lane (of the even CTA, in pair mode) issues
 //               the MMAs, K = 16 each, four per K block, and frees each ring
@@ -60,13 +61,23 @@ struct TiledParams {
     int32_t n_tma;
     // 1: B's tensor map is 4-D, [slice][N/64 groups][K][64 columns] (N a multiple
     // of 64), and each load brings two 64-column groups of one K block (one
-    // TMA instruction where the 3-D map needs two); 0: B's map is 3-D,
-    // [slice][K][N], loaded one 64 x 64 box at a time.
+    // TMA instruction where the 3-D map needs two); 0: B is loaded one 64 x 64
+    // box at a time. The second map of B is always the 3-D one, [slice][K][N]:
+    // it carries every box when this is 0 and the odd last 64-column group of a
+    // narrow piece when it is 1.
     int32_t b_grouped;
     // 1-CTA mode only: the CTAs of a cluster of `ksplit` (2 or 4) share one
     // tile, each accumulating its own part of the K range; 1 otherwise. See the
     // kernel's K-split epilogue.
     int32_t ksplit;
+    // Pair mode only, 1 or 0: the K split of the last partial round. Its tiles
+    // are cut into two pieces as column halves, and each piece accumulates
+    // half of the K range over the whole tile width instead of all of K over
+    // half the width. The two pairs of a tile then trade, through `ws`, the
+    // fp32 partial sums of each other's columns (see the epilogue).
+    int32_t ktail;
+    uint32_t epoch; // nonzero tag of this call in the workspace flags
+    void *ws;       // workspace (caller-owned; flags, then 64 KB partial-sum slots)
     float alpha, beta;
     const void *C;
     int64_t ldc;
@@ -175,6 +186,38 @@ __device__ __forceinline__ bool drain_wait(uint64_t *bar, uint32_t parity, uint6
     return false;
 }
 
+// The K blocks [lo, hi) a work item accumulates, and the columns its MMAs
+// cover: all of K over the item's own columns, except for a piece of the K
+// split tail, which covers its tile's full width over half of K.
+struct KRange {
+    int32_t lo, hi, n, width;
+};
+__device__ __forceinline__ KRange item_krange(const WorkItem &w, int32_t kb_lo, int32_t kb_hi, const TiledParams &p) {
+    KRange r{kb_lo, kb_hi, w.n, w.width};
+    if (p.ktail && w.width < BN) {
+        const int32_t piece = (w.n % BN) / w.width; // 0 or 1
+        r.lo = piece * p.kb / 2;
+        r.hi = (piece + 1) * p.kb / 2;
+        r.n = w.n - w.n % BN;
+        r.width = BN;
+    }
+    return r;
+}
+
+// Workspace of the K split tail: 4 KB of flags, then one slot of 128 rows x
+// 128 fp32 columns (64 KB) per (tail tile, CTA of the pair, piece). A slot is
+// laid out [column / 4][row][4], so that the 32 rows of a warp write and read
+// 512 contiguous bytes per column quad.
+constexpr uint32_t kTailFlagBytes = 4096;
+constexpr uint32_t kTailSlotBytes = 128u * 128u * 4u;
+__device__ __forceinline__ uint32_t *tail_flag(const TiledParams &p, int64_t tile, uint32_t cta, uint32_t piece) {
+    return static_cast<uint32_t *>(p.ws) + (tile * 2 + cta) * 2 + piece;
+}
+__device__ __forceinline__ float4 *tail_slot(const TiledParams &p, int64_t tile, uint32_t cta, uint32_t piece) {
+    return reinterpret_cast<float4 *>(static_cast<uint8_t *>(p.ws) + kTailFlagBytes +
+                                      static_cast<uint64_t>((tile * 2 + cta) * 2 + piece) * kTailSlotBytes);
+}
+
 // Busy-waits `ns` nanoseconds (abort path only).
 __device__ __forceinline__ void settle(uint64_t ns) {
     const uint64_t t0 = globaltimer_ns();
@@ -190,7 +233,7 @@ __device__ __forceinline__ void settle(uint64_t ns) {
 template <bool kOutF32, bool kPair, int kEpi, bool kGrouped = false, bool kKsplit = false>
 __global__ void __launch_bounds__(THREADS, 1)
     gemm_tiled_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                      const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmD,
+                      const __grid_constant__ CUtensorMap tmB1, const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmD,
                       const TiledParams p, const __grid_constant__ SegArg<kGrouped> seg) {
     using L = Layout<kPair>;
     constexpr int STAGES = L::STAGES;
@@ -208,7 +251,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     uint64_t *cbar = tempty + 2;
     uint64_t *drain = cbar + 2;
     uint64_t *ks_free = drain + 1; // K split: one arrive from each peer whose MMAs are done
-    uint64_t *ks_recv = drain + 2; // K split: the peers' partials have landed here (transaction bytes)
+    uint64_t *ks_recv = drain + 2; // K split (and its tail form in pair mode): the peers' partials have landed here
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::OFF_MISC);
     volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(smem + L::OFF_MISC + 4);
 
@@ -240,12 +283,14 @@ __global__ void __launch_bounds__(THREADS, 1)
             mbar_init(ks_free, static_cast<uint32_t>(ks - 1));
             mbar_init(ks_recv, 1);
         }
+        if (kPair && p.ktail) mbar_init(ks_recv, 1); // the K split tail's partner partial sums
         *abort_flag = 0u;
         fence_barrier_init();
     }
     if (warp == 0 && lane == 0) {
         prefetch_tensormap(&tmA);
         prefetch_tensormap(&tmB);
+        if (p.b_grouped) prefetch_tensormap(&tmB1);
         prefetch_tensormap(&tmD);
         if (p.beta != 0.0f) prefetch_tensormap(&tmC);
     }
@@ -281,19 +326,23 @@ __global__ void __launch_bounds__(THREADS, 1)
             bool ok = true;
             WorkItem w;
             for (int64_t t = worker; ok && work_item(p.sched, t, BN, w); t += workers) {
+                const KRange kr = item_krange(w, kb_lo, kb_hi, p);
                 const Segment sg = segment_of<kGrouped>(w.m, BM * CL, p, seg);
                 const int32_t m0 = sg.row0 + static_cast<int32_t>(rank) * BM;
                 const int32_t ab = p.a_bcast ? 0 : sg.ab;
                 const int32_t bb = p.b_bcast ? 0 : sg.bb;
-                const int32_t cols = w.width / CL; // B columns this CTA stages
-                const int32_t nb = w.n + static_cast<int32_t>(rank) * cols;
-                // Grouped B: boxes of two 64-column groups. A piece 64 columns wide
-                // still loads two (the second one's columns are not used; the
-                // stage has room for them), so the byte count is whole boxes.
-                const int32_t nload = p.b_grouped ? (cols / 64 + 1) / 2 : cols / 64;
-                const uint32_t bbytes = static_cast<uint32_t>(p.b_grouped ? 2 * nload : nload) * B_BOX_BYTES;
+                const int32_t cols = kr.width / CL; // B columns this CTA stages
+                const int32_t nb = kr.n + static_cast<int32_t>(rank) * cols;
+                // The CTA stages `groups` 64-column groups of B per K block: two
+                // per instruction through the 4-D view while at least two remain,
+                // and an odd last one (a 64-column piece of a split tile) through
+                // the 3-D view, so that a narrow piece loads only the columns it
+                // uses.
+                const int32_t groups = cols / 64;
+                const int32_t npair = p.b_grouped ? groups / 2 : 0;
+                const uint32_t bbytes = static_cast<uint32_t>(groups) * B_BOX_BYTES;
                 const uint32_t tx = CL * (A_STAGE_BYTES + bbytes);
-                for (int32_t kb = kb_lo; kb < kb_hi; ++kb) {
+                for (int32_t kb = kr.lo; kb < kr.hi; ++kb) {
                     if (!mbar_wait(&empty[stage], phase ^ 1u, ctl, kStatusTimeoutProducer)) {
                         ok = false;
                         break;
@@ -305,24 +354,17 @@ __global__ void __launch_bounds__(THREADS, 1)
                         if (rank == 0) mbar_arrive_expect_tx(&full[stage], tx);
                         const uint32_t fb = full0 + stage * 8u;
                         tma_load_3d_pair(&tmA, fb, adst, k0, m0, ab);
-                        if (p.b_grouped) {
-                            for (int c = 0; c < nload; ++c)
-                                tma_load_4d_pair(&tmB, fb, bdst + 2 * c * B_BOX_BYTES, 0, k0, (nb >> 6) + 2 * c, bb);
-                        } else {
-                            for (int c = 0; c < nload; ++c)
-                                tma_load_3d_pair(&tmB, fb, bdst + c * B_BOX_BYTES, nb + c * 64, k0, bb);
-                        }
+                        for (int c = 0; c < npair; ++c)
+                            tma_load_4d_pair(&tmB, fb, bdst + 2 * c * B_BOX_BYTES, 0, k0, (nb >> 6) + 2 * c, bb);
+                        for (int c = 2 * npair; c < groups; ++c)
+                            tma_load_3d_pair(&tmB1, fb, bdst + c * B_BOX_BYTES, nb + c * 64, k0, bb);
                     } else {
                         mbar_arrive_expect_tx(&full[stage], tx);
                         tma_load_3d(&tmA, &full[stage], adst, k0, m0, ab);
-                        if (p.b_grouped) {
-                            for (int c = 0; c < nload; ++c)
-                                tma_load_4d(&tmB, &full[stage], bdst + 2 * c * B_BOX_BYTES, 0, k0, (nb >> 6) + 2 * c,
-                                            bb);
-                        } else {
-                            for (int c = 0; c < nload; ++c)
-                                tma_load_3d(&tmB, &full[stage], bdst + c * B_BOX_BYTES, nb + c * 64, k0, bb);
-                        }
+                        for (int c = 0; c < npair; ++c)
+                            tma_load_4d(&tmB, &full[stage], bdst + 2 * c * B_BOX_BYTES, 0, k0, (nb >> 6) + 2 * c, bb);
+                        for (int c = 2 * npair; c < groups; ++c)
+                            tma_load_3d(&tmB1, &full[stage], bdst + c * B_BOX_BYTES, nb + c * 64, k0, bb);
                     }
                     ++issued;
                     if (++stage == STAGES) {
@@ -362,14 +404,15 @@ __global__ void __launch_bounds__(THREADS, 1)
             bool any = false;
             WorkItem w;
             for (int64_t t = worker; ok && work_item(p.sched, t, BN, w); t += workers) {
-                const uint32_t idesc = make_idesc_bf16_f32(BM * CL, static_cast<uint32_t>(w.width), false, true);
+                const KRange kr = item_krange(w, kb_lo, kb_hi, p);
+                const uint32_t idesc = make_idesc_bf16_f32(BM * CL, static_cast<uint32_t>(kr.width), false, true);
                 if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, ctl, kStatusTimeoutMma)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + acc * BN;
-                for (int32_t kb = kb_lo; kb < kb_hi; ++kb) {
+                for (int32_t kb = kr.lo; kb < kr.hi; ++kb) {
                     if (!mbar_wait(&full[stage], phase, ctl, kStatusTimeoutMma)) {
                         ok = false;
                         break;
@@ -384,7 +427,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                         // B: N-major, advance 16 K rows = 2048 bytes; 64-wide N blocks are
                         // one 8 KB box apart.
                         const uint64_t bdesc = make_smem_desc_sw128(b_addr + kk * 2048, B_BOX_BYTES, 1024);
-                        const uint32_t accumulate = (kb != kb_lo || kk != 0) ? 1u : 0u;
+                        const uint32_t accumulate = (kb != kr.lo || kk != 0) ? 1u : 0u;
                         if constexpr (kPair)
                             tc_mma_f16_pair(d_tmem, adesc, bdesc, idesc, accumulate);
                         else
@@ -432,6 +475,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         uint32_t slot = 0;
         uint32_t cphase = 0; // bit b: parity of the next wait on cbar[b]
         bool ok = true;
+        bool tail_loading = false; // the leader issued the bulk load of the partner's partial sums
         // K split: CTA krank of the cluster owns (and stores) columns
         // [krank * ks_w, (krank + 1) * ks_w) of the tile. Once its own MMAs are
         // done its ring is idle, and holds ks - 1 receive slots (the other
@@ -552,6 +596,78 @@ __global__ void __launch_bounds__(THREADS, 1)
                     break;
                 }
             }
+            // K split tail: this pair accumulated half of K over the whole tile,
+            // and owns (stores) the column half given by its piece. It hands the
+            // partner pair its partial sums of the partner's columns through the
+            // workspace, flags them with this call's epoch, and takes the
+            // partner's partial sums of its own columns in return; the chunk loop
+            // below adds them. Every element is still written by one CTA, and the
+            // sum of two fp32 parts is the same in either order.
+            const bool tail_piece = kPair && p.ktail && w.width < BN;
+            // The partner's partial sums land in this CTA's ring, idle now: the
+            // pair's MMAs are done and a tail piece is a worker's last item.
+            const float4 *partner = reinterpret_cast<const float4 *>(smem + L::OFF_A) + row;
+            if (tail_piece) {
+                const int64_t tile_i = (t - p.sched.whole) / 2;
+                const uint32_t piece = static_cast<uint32_t>((w.n % BN) / w.width);
+                float4 *mine = tail_slot(p, tile_i, rank, piece);
+                const uint32_t other0 = (1u - piece) * 128u; // TMEM column of the partner's half
+                for (int32_t g = 0; g < 4; g += 2) {
+                    uint32_t r[2][32];
+                    const uint32_t ta = tmem_base + acc * BN + other0 + static_cast<uint32_t>(g * 32) + ((q * 32u) << 16);
+                    tmem_ld32(ta, r[0]);
+                    tmem_ld32(ta + 32, r[1]);
+                    tc_wait_ld();
+#pragma unroll
+                    for (int h = 0; h < 2; ++h)
+#pragma unroll
+                        for (int i = 0; i < 32; i += 4)
+                            __stcg(mine + static_cast<uint32_t>((g + h) * 8 + i / 4) * BM + row,
+                                   make_float4(__uint_as_float(r[h][i]), __uint_as_float(r[h][i + 1]),
+                                               __uint_as_float(r[h][i + 2]), __uint_as_float(r[h][i + 3])));
+                }
+                __threadfence();
+                named_barrier_sync(1, EPI_THREADS);
+                bool have = true;
+                if (leader) {
+                    st_release_gpu(tail_flag(p, tile_i, rank, piece), p.epoch);
+                    uint32_t *theirs = tail_flag(p, tile_i, rank, 1u - piece);
+                    have = flag_wait(theirs, p.epoch, ctl, kStatusTimeoutReduce);
+                    if (have) {
+                        *theirs = 0u; // consumed: the next call starts from a clear flag
+                        // one bulk copy brings the partner's 64 KB into the ring
+                        fence_proxy_async_global();
+                        mbar_arrive_expect_tx(ks_recv, kTailSlotBytes);
+                        bulk_load_g2s(smem + L::OFF_A, tail_slot(p, tile_i, rank, 1u - piece), kTailSlotBytes, ks_recv);
+                        tail_loading = true;
+                    }
+                }
+                if (named_barrier_or(1, EPI_THREADS, !have)) {
+                    ok = false;
+                    break;
+                }
+                const bool landed = mbar_wait(ks_recv, 0u, ctl, kStatusTimeoutReduce);
+                if (named_barrier_or(1, EPI_THREADS, !landed)) {
+                    ok = false;
+                    break;
+                }
+            }
+            // Adds the partner's partial sums of columns col0 .. col0+31 of this
+            // CTA's column half, from the ring ([column / 4][row][4] layout).
+            auto tail_add = [&](uint32_t(&r)[32], int32_t col0) {
+                float4 v[8];
+#pragma unroll
+                for (int g = 0; g < 8; ++g) v[g] = partner[static_cast<uint32_t>(col0 / 4 + g) * BM];
+#pragma unroll
+                for (int g = 0; g < 8; ++g) {
+                    r[4 * g] = __float_as_uint(__uint_as_float(r[4 * g]) + v[g].x);
+                    r[4 * g + 1] = __float_as_uint(__uint_as_float(r[4 * g + 1]) + v[g].y);
+                    r[4 * g + 2] = __float_as_uint(__uint_as_float(r[4 * g + 2]) + v[g].z);
+                    r[4 * g + 3] = __float_as_uint(__uint_as_float(r[4 * g + 3]) + v[g].w);
+                }
+            };
+            // first TMEM column of the columns this CTA stores
+            const int32_t tcol0 = tail_piece ? (w.n % BN) : own0;
             const uint32_t acc_now = acc;
             auto release = [&]() {
                 // Whole accumulator read: hand it back to the MMA warp.
@@ -601,7 +717,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                     cphase ^= 1u << slot;
                 }
                 const uint32_t taddr =
-                    tmem_base + acc * BN + static_cast<uint32_t>(own0 + c * CHUNK) + ((q * 32u) << 16);
+                    tmem_base + acc * BN + static_cast<uint32_t>(tcol0 + c * CHUNK) + ((q * 32u) << 16);
                 uint32_t r0[32];
                 uint32_t r1[32];
                 tmem_ld32(taddr, r0);
@@ -610,6 +726,10 @@ __global__ void __launch_bounds__(THREADS, 1)
                 if (ks > 1) {
                     ks_combine(r0, c * CHUNK);
                     if (!kOutF32) ks_combine(r1, c * CHUNK + 32);
+                }
+                if (tail_piece) {
+                    tail_add(r0, c * CHUNK);
+                    if (!kOutF32) tail_add(r1, c * CHUNK + 32);
                 }
                 if (c == nchunks - 1) release();
                 uint8_t *rowp = buf + row * 128u;
@@ -704,8 +824,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (leader) bulk_wait_group<0>();
         // K split: a CTA that gave up early must still not exit while a peer's
         // bulk copy into its ring may be in flight (a no-op once the copies
-        // have landed).
-        if (ks > 1 && leader && !drain_wait(ks_recv, 0u, p.timeout_ns) && p.status)
+        // have landed). The same holds for the tail's bulk load.
+        if ((ks > 1 || tail_loading) && leader && !drain_wait(ks_recv, 0u, p.timeout_ns) && p.status)
             atomicOr(p.status, kStatusTimeoutDrain);
     }
 

@@ -57,7 +57,7 @@ struct TiledLaunch {
     bool pair;
     bool f32;
     cudaStream_t stream;
-    const CUtensorMap *a, *b, *c, *d;
+    const CUtensorMap *a, *b, *b1, *c, *d; // b: B's 4-D map (or its 3-D one); b1: the 3-D map
     const TiledParams *p;
     const GroupTable *groups; // grouped GEMM only (tiled_launch_g0)
 };

@@ -146,6 +146,34 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint64_t *bar, uint32_t parity
     return mbar_wait_slow<true>(a, parity, ctl, code);
 }
 
+// ---------------------------------------------------------------- flags in global memory
+// A flag another CTA of the grid sets after writing data that this CTA then
+// reads (release store / acquire load at GPU scope).
+__device__ __forceinline__ void st_release_gpu(uint32_t *p, uint32_t v) {
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t *p) {
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// Bounded wait until *flag == want, with the same give-up rules as the
+// mbarrier waits (time limit, another role's abort, a hard poll cap).
+static __device__ __noinline__ bool flag_wait(const uint32_t *flag, uint32_t want, WaitCtl ctl, uint32_t code) {
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t i = 1; i < (1u << 31); ++i) {
+        if (ld_acquire_gpu(flag) == want) return true;
+        if ((i & 15u) == 0) {
+            if (*ctl.abort_flag) return false;
+            if (globaltimer_ns() - t0 > ctl.timeout_ns) break;
+        }
+    }
+    *ctl.abort_flag = 1u;
+    if (ctl.status) atomicOr(ctl.status, code);
+    return false;
+}
+
 // ---------------------------------------------------------------- programmatic dependent launch
 // A kernel launched with programmatic stream serialisation may start while the
 // previous kernel in the stream is still running. It does its prologue (barrier
@@ -309,6 +337,23 @@ __device__ __forceinline__ void bulk_copy_to_peer(uint32_t dst_cluster, uint32_t
 
 __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// Orders this thread's generic-proxy view of global memory (e.g. an acquire
+// load of a flag) before the async-proxy operations it issues next (a bulk
+// copy that reads what the flag guards).
+__device__ __forceinline__ void fence_proxy_async_global() {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+// Bulk copy (TMA, no tensor map) of `bytes` (a multiple of 16, both addresses
+// 16-byte aligned) from global memory into this CTA's shared memory; the bytes
+// complete as transactions on `bar`.
+__device__ __forceinline__ void bulk_load_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     smem_addr(dst)),
+                 "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_addr(bar))
+                 : "memory");
 }
 
 __device__ __forceinline__ void named_barrier_sync(uint32_t id, uint32_t threads) {

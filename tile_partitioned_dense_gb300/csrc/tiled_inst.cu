@@ -43,10 +43,10 @@ cudaError_t launch_one(const TiledLaunch &l) {
     if constexpr (!kPair && !kGrouped) {
         if (l.cluster > 1)
             return launch_ex(tiled::gemm_tiled_kernel<kOutF32, false, TPG_EPI, false, true>, l.grid, tiled::THREADS,
-                             l.smem, l.cluster, true, l.stream, *l.a, *l.b, *l.c, *l.d, *l.p, seg);
+                             l.smem, l.cluster, true, l.stream, *l.a, *l.b, *l.b1, *l.c, *l.d, *l.p, seg);
     }
     return launch_ex(tiled::gemm_tiled_kernel<kOutF32, kPair, TPG_EPI, kGrouped>, l.grid, tiled::THREADS, l.smem,
-                     l.cluster, true, l.stream, *l.a, *l.b, *l.c, *l.d, *l.p, seg);
+                     l.cluster, true, l.stream, *l.a, *l.b, *l.b1, *l.c, *l.d, *l.p, seg);
 }
 } // namespace
 

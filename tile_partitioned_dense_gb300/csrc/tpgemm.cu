@@ -46,8 +46,15 @@ struct Plan {
     int smem = 0;
     int launches = 0;
     int mt_pad = 0, stages = 0, split = 1;
+    int ktail = 0; // CTA-pair mode: the last partial round's tiles split over K (workspace)
     tpg::Schedule sched{};
 };
+
+// Workspace bytes of the K split tail for `tail_tiles` tiles: the flags, then
+// four 64 KB partial-sum slots per tile (two CTAs of each of two pairs).
+int64_t tail_ws_bytes(int64_t tail_tiles) {
+    return tpg::tiled::kTailFlagBytes + tail_tiles * 4 * static_cast<int64_t>(tpg::tiled::kTailSlotBytes);
+}
 
 } // namespace
 
@@ -68,6 +75,11 @@ struct tpgemm_handle {
     // co-resident clusters of 2 and 4 CTAs of the tiled kernel in 1-CTA mode (K
     // split), per [out f32][0: two, 1: four]
     std::atomic<int> ks_clusters[2][2] = {};
+    // Caller-owned workspace (gemm_set_workspace), or null, and the tag of the
+    // latest call that may use it.
+    void *ws = nullptr;
+    int64_t ws_bytes = 0;
+    std::atomic<uint32_t> epoch{0};
 };
 
 namespace {
@@ -180,7 +192,7 @@ struct TiledCall {
 };
 
 int build_tiled(PFN_cuTensorMapEncodeTiled_v12000 encode, const TiledCall &c, CUtensorMap *tmA, CUtensorMap *tmB,
-                CUtensorMap *tmC, CUtensorMap *tmD, tpg::TiledParams *p) {
+                CUtensorMap *tmB1, CUtensorMap *tmC, CUtensorMap *tmD, tpg::TiledParams *p) {
     const int64_t elt = c.f32 ? 4 : 2;
     const bool use_c = c.beta != 0.0f;
     const CUtensorMapDataType out_dt = c.f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
@@ -195,9 +207,9 @@ int build_tiled(PFN_cuTensorMapEncodeTiled_v12000 encode, const TiledCall &c, CU
     const bool b_grouped = c.N % 64 == 0;
     if (encode_3d(encode, tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, c.A, c.K, c.rows, tma_stride(c.rows, c.K, c.lda, 2),
                   aslices, c.sA, 2, 64, tpg::tiled::BM) ||
-        (b_grouped ? encode_b_grouped(encode, tmB, c.B, c.N, c.K, c.ldb, bslices, c.sB)
-                   : encode_3d(encode, tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, c.B, c.N, c.K,
-                               tma_stride(c.K, c.N, c.ldb, 2), bslices, c.sB, 2, 64, 64)) ||
+        encode_3d(encode, tmB1, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, c.B, c.N, c.K, tma_stride(c.K, c.N, c.ldb, 2),
+                  bslices, c.sB, 2, 64, 64) ||
+        (b_grouped ? encode_b_grouped(encode, tmB, c.B, c.N, c.K, c.ldb, bslices, c.sB) : (*tmB = *tmB1, 0)) ||
         encode_3d(encode, tmD, out_dt, c.D, map_n, c.rows, tma_stride(c.rows, c.N, c.ldd, elt), c.batch, c.sD, elt,
                   chunk, tpg::tiled::BM) ||
         encode_3d(encode, tmC, out_dt, use_c ? c.C : c.D, map_n, c.rows,
@@ -352,6 +364,12 @@ Plan make_plan(tpgemm_handle *h, int64_t M, int64_t N, int64_t K, int out_dtype)
         pl.grid = static_cast<int>(pl.sched.workers * pl.cluster);
         pl.split = pl.sched.split;
         pl.smem = static_cast<int>(pair ? tpg::tiled::Layout<true>::SMEM_BYTES : tpg::tiled::Layout<false>::SMEM_BYTES);
+        // With a workspace, the halves of the last partial round become K halves
+        // over the whole tile width (tiled::item_krange): a piece then takes half
+        // of a tile's K blocks, where a column half takes all of them.
+        const int64_t kbt = (K + tpg::tiled::BK - 1) / tpg::tiled::BK;
+        if (pair && pl.sched.split == 2 && kbt >= 2 && h->ws && tail_ws_bytes(pl.sched.pieces / 2) <= h->ws_bytes)
+            pl.ktail = 1;
         return pl;
     }
     // weight-streaming variant
@@ -523,6 +541,38 @@ int gemm_destroy(tpgemm_handle *h) {
 
 int gemm_num_sms(tpgemm_handle *h) { return h ? h->num_sms : TPGEMM_ERR_INVALID_ARG; }
 
+int64_t gemm_workspace_size(tpgemm_handle *h) {
+    if (!h) return TPGEMM_ERR_INVALID_ARG;
+    // at most one tail tile per two CTA pairs
+    return tail_ws_bytes(h->num_sms / 4);
+}
+
+int gemm_set_workspace(tpgemm_handle *h, void *ws, int64_t bytes, void *stream_ptr) {
+    if (!h) return TPGEMM_ERR_INVALID_ARG;
+    if (!ws) {
+        h->ws = nullptr;
+        h->ws_bytes = 0;
+        return TPGEMM_OK;
+    }
+    if (bytes < tail_ws_bytes(1)) return TPGEMM_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return TPGEMM_ERR_ALIGNMENT;
+    DeviceGuard guard(h->device);
+    // every flag starts clear; calls enqueued after this on the same stream see it
+    if (cudaMemsetAsync(ws, 0, tpg::tiled::kTailFlagBytes, static_cast<cudaStream_t>(stream_ptr)) != cudaSuccess)
+        return TPGEMM_ERR_CUDA;
+    h->ws = ws;
+    h->ws_bytes = bytes;
+    return TPGEMM_OK;
+}
+
+int gemm_plan_tail_ksplit(tpgemm_handle *h, int64_t M, int64_t N, int64_t K, int out_dtype) {
+    if (!h || M < 0 || N < 0 || K < 0) return TPGEMM_ERR_INVALID_ARG;
+    if (out_dtype != TPGEMM_OUT_BF16 && out_dtype != TPGEMM_OUT_F32) return TPGEMM_ERR_INVALID_ARG;
+    if (M > kMaxDim || N > kMaxDim || K > kMaxDim) return TPGEMM_ERR_TOO_LARGE;
+    DeviceGuard guard(h->device);
+    return make_plan(h, M, N, K, out_dtype).ktail;
+}
+
 int gemm_force_variant(tpgemm_handle *h, int variant) {
     if (!h) return TPGEMM_ERR_INVALID_ARG;
     if (variant != TPGEMM_VARIANT_AUTO && variant != TPGEMM_VARIANT_TILED && variant != TPGEMM_VARIANT_STREAM &&
@@ -667,18 +717,33 @@ int run_impl(tpgemm_handle *h, int64_t M, int64_t N, int64_t K, const void *A, i
 
     CUtensorMap tmA, tmB;
     if (pl.variant == TPGEMM_VARIANT_TILED || pl.variant == TPGEMM_VARIANT_TILED_PAIR) {
-        CUtensorMap tmC, tmD;
+        CUtensorMap tmB1, tmC, tmD;
         tpg::TiledParams p;
         const TiledCall call{M, N, K, 1, 1, A, lda, 0, B, ldb, 0, C, ldc, 0, D, ldd, 0, alpha, beta, f32};
-        if (build_tiled(h->encode, call, &tmA, &tmB, &tmC, &tmD, &p) != TPGEMM_OK) return TPGEMM_ERR_CUDA;
+        if (build_tiled(h->encode, call, &tmA, &tmB, &tmB1, &tmC, &tmD, &p) != TPGEMM_OK) return TPGEMM_ERR_CUDA;
         p.sched = pl.sched;
         p.mt_batch = static_cast<int32_t>(pl.sched.mt);
         p.ksplit = pl.ksplit;
         p.status = h->status;
         p.timeout_ns = h->timeout_ns;
         p.epi = ep;
+        if (pl.ktail) {
+            // The kernel writes the workspace: it may not share bytes with an operand.
+            const Range rw{reinterpret_cast<uintptr_t>(h->ws), reinterpret_cast<uintptr_t>(h->ws) +
+                                                                   static_cast<uintptr_t>(tail_ws_bytes(pl.sched.pieces / 2))};
+            if (overlaps(rw, byte_range(A, M, K, lda, 2)) || overlaps(rw, byte_range(B, K, N, ldb, 2)) ||
+                overlaps(rw, byte_range(D, M, N, ldd, elt)) || (use_c && overlaps(rw, byte_range(C, M, N, ldc, elt))) ||
+                (epi && epi->aux && overlaps(rw, byte_range(epi->aux, M, N, epi->ldaux, elt))) ||
+                (epi && epi->bias && overlaps(rw, byte_range(epi->bias, 1, N, N, epi->bias_dtype == TPGEMM_OUT_F32 ? 4 : 2))))
+                return TPGEMM_ERR_OVERLAP;
+            uint32_t e = h->epoch.fetch_add(1u, std::memory_order_relaxed) + 1u;
+            if (e == 0u) e = h->epoch.fetch_add(1u, std::memory_order_relaxed) + 1u;
+            p.ktail = 1;
+            p.epoch = e;
+            p.ws = h->ws;
+        }
         const tpg::TiledLaunch l{pl.grid, pl.smem, pl.cluster, pl.variant == TPGEMM_VARIANT_TILED_PAIR, f32, stream,
-                                 &tmA, &tmB, &tmC, &tmD, &p, nullptr};
+                                 &tmA, &tmB, &tmB1, &tmC, &tmD, &p, nullptr};
         return launch_tiled(fused ? 1 + ep.act : 0, l);
     }
 
@@ -763,17 +828,17 @@ int gemm_run_batched(tpgemm_handle *h, int64_t batch, int64_t M, int64_t N, int6
     const int64_t mt = (M + rows_per_tile - 1) / rows_per_tile;
     const int64_t nt = (N + tpg::tiled::BN - 1) / tpg::tiled::BN;
     const int64_t cap = pair ? pair_clusters_for(h, f32) : h->num_sms;
-    CUtensorMap tmA, tmB, tmC, tmD;
+    CUtensorMap tmA, tmB, tmB1, tmC, tmD;
     tpg::TiledParams p;
     const TiledCall call{M, N, K, batch, batch, A, lda, sA, B, ldb, sB, C, ldc, sC, D, ldd, sD, alpha, beta, f32};
-    if (build_tiled(h->encode, call, &tmA, &tmB, &tmC, &tmD, &p) != TPGEMM_OK) return TPGEMM_ERR_CUDA;
+    if (build_tiled(h->encode, call, &tmA, &tmB, &tmB1, &tmC, &tmD, &p) != TPGEMM_OK) return TPGEMM_ERR_CUDA;
     p.sched = tiled_schedule(mt * batch, nt, cap, pair, true);
     p.mt_batch = static_cast<int32_t>(mt);
     p.status = h->status;
     p.timeout_ns = h->timeout_ns;
     const int smem = static_cast<int>(pair ? tpg::tiled::Layout<true>::SMEM_BYTES : tpg::tiled::Layout<false>::SMEM_BYTES);
     const tpg::TiledLaunch l{static_cast<int>(p.sched.workers * (pair ? 2 : 1)), smem, pair ? 2 : 1, pair, f32, stream,
-                             &tmA, &tmB, &tmC, &tmD, &p, nullptr};
+                             &tmA, &tmB, &tmB1, &tmC, &tmD, &p, nullptr};
     return launch_tiled(0, l);
 }
 
@@ -828,18 +893,18 @@ int gemm_run_grouped(tpgemm_handle *h, int64_t groups, const int64_t *group_rows
     table.tile_prefix[groups] = static_cast<int32_t>(tiles);
     const int64_t nt = (N + tpg::tiled::BN - 1) / tpg::tiled::BN;
     const int64_t cap = pair ? pair_clusters_for(h, f32) : h->num_sms;
-    CUtensorMap tmA, tmB, tmC, tmD;
+    CUtensorMap tmA, tmB, tmB1, tmC, tmD;
     tpg::TiledParams p;
     const TiledCall call{total, N, K, 1, groups, A, lda, 0, B, ldb, groups > 1 ? sB : 0, C, ldc, 0, D, ldd, 0,
                          alpha, beta, f32};
-    if (build_tiled(h->encode, call, &tmA, &tmB, &tmC, &tmD, &p) != TPGEMM_OK) return TPGEMM_ERR_CUDA;
+    if (build_tiled(h->encode, call, &tmA, &tmB, &tmB1, &tmC, &tmD, &p) != TPGEMM_OK) return TPGEMM_ERR_CUDA;
     p.sched = tiled_schedule(tiles, nt, cap, pair, true);
     p.mt_batch = 1;
     p.status = h->status;
     p.timeout_ns = h->timeout_ns;
     const int smem = static_cast<int>(pair ? tpg::tiled::Layout<true>::SMEM_BYTES : tpg::tiled::Layout<false>::SMEM_BYTES);
     const tpg::TiledLaunch l{static_cast<int>(p.sched.workers * (pair ? 2 : 1)), smem, pair ? 2 : 1, pair, f32, stream,
-                             &tmA, &tmB, &tmC, &tmD, &p, &table};
+                             &tmA, &tmB, &tmB1, &tmC, &tmD, &p, &table};
     return tpg::tiled_launch_g0(l) == cudaSuccess ? TPGEMM_OK : TPGEMM_ERR_CUDA;
 }
 
@@ -1012,10 +1077,10 @@ extern "C" int gemm_run_noalloc(int64_t M, int64_t N, int64_t K, const void *A, 
     } else {
         // The status word must start at zero: every call shares it.
         if (cudaMemsetAsync(nd->status, 0, sizeof(uint32_t), stream) != cudaSuccess) return TPGEMM_ERR_CUDA;
-        CUtensorMap tmA, tmB, tmC, tmD;
+        CUtensorMap tmA, tmB, tmB1, tmC, tmD;
         tpg::TiledParams p;
         const TiledCall call{M, N, K, 1, 1, A, lda, 0, B, ldb, 0, C, ldc, 0, D, ldd, 0, alpha, beta, f32};
-        if (build_tiled(nd->encode, call, &tmA, &tmB, &tmC, &tmD, &p) != TPGEMM_OK) return TPGEMM_ERR_CUDA;
+        if (build_tiled(nd->encode, call, &tmA, &tmB, &tmB1, &tmC, &tmD, &p) != TPGEMM_OK) return TPGEMM_ERR_CUDA;
         const int64_t mt = (M + tpg::tiled::BM - 1) / tpg::tiled::BM;
         const int64_t nt = (N + tpg::tiled::BN - 1) / tpg::tiled::BN;
         // the same K split as gemm_run would choose, so the two give the same bits
@@ -1027,7 +1092,7 @@ extern "C" int gemm_run_noalloc(int64_t M, int64_t N, int64_t K, const void *A, 
         p.status = nd->status;
         p.timeout_ns = 2000000000ull;
         const tpg::TiledLaunch l{grid, static_cast<int>(tpg::tiled::SMEM_BYTES), ks, false, f32, stream,
-                                 &tmA, &tmB, &tmC, &tmD, &p, nullptr};
+                                 &tmA, &tmB, &tmB1, &tmC, &tmD, &p, nullptr};
         rc = tpg::tiled_launch_e0(l) == cudaSuccess ? TPGEMM_OK : TPGEMM_ERR_CUDA;
     }
     if (rc != TPGEMM_OK || !check_status) return rc;
