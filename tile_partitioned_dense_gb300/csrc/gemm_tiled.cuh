@@ -626,7 +626,9 @@ __global__ void __launch_bounds__(THREADS, 1)
                                    make_float4(__uint_as_float(r[h][i]), __uint_as_float(r[h][i + 1]),
                                                __uint_as_float(r[h][i + 2]), __uint_as_float(r[h][i + 3])));
                 }
-                __threadfence();
+                // Every thread's stores come before the barrier, and the leader's
+                // release store after it is cumulative over them: a reader that
+                // acquires the flag sees the whole slot.
                 named_barrier_sync(1, EPI_THREADS);
                 bool have = true;
                 if (leader) {
@@ -821,7 +823,9 @@ __global__ void __launch_bounds__(THREADS, 1)
                 acc_phase ^= 1u;
             }
         }
-        if (leader) bulk_wait_group<0>();
+        // The stores must have read the staging buffers before the CTA exits;
+        // their global writes are complete when the grid is.
+        if (leader) bulk_wait_group_read<0>();
         // K split: a CTA that gave up early must still not exit while a peer's
         // bulk copy into its ring may be in flight (a no-op once the copies
         // have landed). The same holds for the tail's bulk load.
