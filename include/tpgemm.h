@@ -338,11 +338,11 @@ int gemm_num_sms(tpgemm_handle *h);
  * two pieces so that more pairs share them ("cuTile Rust explained",
  * "Ownership crosses the launch boundary": each piece keeps an exclusive
  * column half of its tile). Without a workspace a piece is a column half that
- * runs over all of K, and it costs about as long as a whole tile. With one, a
- * piece runs over half of K and the full tile width; the two pairs of a tile
- * trade their fp32 partial sums of each other's column half through the
- * workspace and each adds the other's part before its epilogue, so a piece
- * takes about half as long. Each output element is still stored by one CTA,
+ * runs over all of K, and it costs about as long as a whole tile. With one,
+ * and K of at least 2048, a piece runs over half of K and the full tile
+ * width; the two pairs of a tile trade their fp32 partial sums of each
+ * other's column half through the workspace and each adds the other's part
+ * before its epilogue, so a piece takes about half as long. Each output element is still stored by one CTA,
  * with no atomics, and the sum of two fp32 parts does not depend on their
  * order, so results are the same on every run.
  *   ws, bytes   device memory of the handle's device, 256-byte aligned;
@@ -373,7 +373,7 @@ int64_t gemm_workspace_size(tpgemm_handle *h);
 
 /*
  * 1 if gemm_run would split the last partial round over K for this problem
- * (CTA-pair plan, a tail of column halves, K > 64 and a large enough
+ * (CTA-pair plan, a tail of column halves, K >= 2048 and a large enough
  * workspace attached), 0 if not, or a negative status.
  */
 int gemm_plan_tail_ksplit(tpgemm_handle *h, int64_t M, int64_t N, int64_t K, int out_dtype);

@@ -56,6 +56,12 @@ int64_t tail_ws_bytes(int64_t tail_tiles) {
     return tpg::tiled::kTailFlagBytes + tail_tiles * 4 * static_cast<int64_t>(tpg::tiled::kTailSlotBytes);
 }
 
+// Fewest K blocks for which the K split tail is used. On square 4096^3 the
+// exchange of partial sums costs about 4.5 us more than a column half's plain
+// epilogue, and a K half saves 0.168 us per K block of the tile (half of a
+// 256 x 256 K block's 0.336 us): the split pays from about 27 K blocks.
+constexpr int64_t kTailMinKb = 32;
+
 } // namespace
 
 struct tpgemm_handle {
@@ -366,9 +372,11 @@ Plan make_plan(tpgemm_handle *h, int64_t M, int64_t N, int64_t K, int out_dtype)
         pl.smem = static_cast<int>(pair ? tpg::tiled::Layout<true>::SMEM_BYTES : tpg::tiled::Layout<false>::SMEM_BYTES);
         // With a workspace, the halves of the last partial round become K halves
         // over the whole tile width (tiled::item_krange): a piece then takes half
-        // of a tile's K blocks, where a column half takes all of them.
+        // of a tile's K blocks, where a column half takes all of them. Only for
+        // K of at least kTailMinKb blocks, where that outweighs the exchange.
         const int64_t kbt = (K + tpg::tiled::BK - 1) / tpg::tiled::BK;
-        if (pair && pl.sched.split == 2 && kbt >= 2 && h->ws && tail_ws_bytes(pl.sched.pieces / 2) <= h->ws_bytes)
+        if (pair && pl.sched.split == 2 && kbt >= kTailMinKb && h->ws &&
+            tail_ws_bytes(pl.sched.pieces / 2) <= h->ws_bytes)
             pl.ktail = 1;
         return pl;
     }
