@@ -398,6 +398,15 @@ __global__ void __launch_bounds__(THREADS, 1)
     } else if (warp == 1) {
         // ------------------------------------------------ MMA issuer (even CTA only in pair mode)
         if (lane == 0 && rank == 0) {
+            // The issuing thread's instructions per K block bound the tensor pipe:
+            // each tcgen05.mma costs it about 107 cycles to issue, four of them
+            // about 430 of the 512 cycles a 256-wide K block computes for. So the
+            // stage-0 descriptors and barrier addresses are built once, and a
+            // stage only adds offsets.
+            const uint64_t adesc0 = make_smem_desc_sw128(smem_addr(smem + L::OFF_A), 16, 1024);
+            // 64-wide N blocks of B are one 8 KB box apart
+            const uint64_t bdesc0 = make_smem_desc_sw128(smem_addr(smem + L::OFF_B), B_BOX_BYTES, 1024);
+            const uint32_t full_a = smem_addr(full), empty_a = smem_addr(empty);
             uint32_t stage = 0, phase = 0;
             uint32_t acc = 0, acc_phase = 0;
             bool ok = true;
@@ -413,31 +422,31 @@ __global__ void __launch_bounds__(THREADS, 1)
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + acc * BN;
                 for (int32_t kb = kr.lo; kb < kr.hi; ++kb) {
-                    if (!mbar_wait(&full[stage], phase, ctl, kStatusTimeoutMma)) {
+                    if (!mbar_try_wait(full_a + stage * 8u, phase) &&
+                        !mbar_wait(&full[stage], phase, ctl, kStatusTimeoutMma)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t a_addr = smem_addr(smem + L::OFF_A + stage * A_STAGE_BYTES);
-                    const uint32_t b_addr = smem_addr(smem + L::OFF_B + stage * L::B_STAGE_BYTES);
+                    // The stage's descriptors: stage 0's plus the stage's byte offset >> 4
+                    // in the start-address field.
+                    const uint64_t ad = adesc0 + stage * (A_STAGE_BYTES >> 4);
+                    const uint64_t bd = bdesc0 + stage * (L::B_STAGE_BYTES >> 4);
 #pragma unroll
                     for (int kk = 0; kk < BK / 16; ++kk) {
                         // A: K-major, advance 16 bf16 = 32 bytes inside the swizzle atom.
-                        const uint64_t adesc = make_smem_desc_sw128(a_addr + kk * 32, 16, 1024);
-                        // B: N-major, advance 16 K rows = 2048 bytes; 64-wide N blocks are
-                        // one 8 KB box apart.
-                        const uint64_t bdesc = make_smem_desc_sw128(b_addr + kk * 2048, B_BOX_BYTES, 1024);
+                        // B: N-major, advance 16 K rows = 2048 bytes.
                         const uint32_t accumulate = (kb != kr.lo || kk != 0) ? 1u : 0u;
                         if constexpr (kPair)
-                            tc_mma_f16_pair(d_tmem, adesc, bdesc, idesc, accumulate);
+                            tc_mma_f16_pair(d_tmem, ad + kk * (32 >> 4), bd + kk * (2048 >> 4), idesc, accumulate);
                         else
-                            tc_mma_f16(d_tmem, adesc, bdesc, idesc, accumulate);
+                            tc_mma_f16(d_tmem, ad + kk * (32 >> 4), bd + kk * (2048 >> 4), idesc, accumulate);
                     }
                     any = true;
                     if constexpr (kPair)
-                        tc_commit_pair_mc(&empty[stage], 0x3);
+                        tc_commit_pair_mc_addr(empty_a + stage * 8u, 0x3);
                     else
-                        tc_commit(&empty[stage]);
+                        tc_commit_addr(empty_a + stage * 8u);
                     if (++stage == STAGES) {
                         stage = 0;
                         phase ^= 1u;
