@@ -379,6 +379,19 @@ int64_t gemm_workspace_size(tpgemm_handle *h);
 int gemm_plan_tail_ksplit(tpgemm_handle *h, int64_t M, int64_t N, int64_t K, int out_dtype);
 
 /*
+ * Host copies of the K split tail's rules (no GPU needed). gemm_tail_ksplit
+ * returns 1 when a CTA-pair schedule whose left-over tiles are cut into
+ * `split` column pieces (the split only applies to halves, split == 2), with
+ * kb K blocks of 64 and `tail_tiles` left-over tiles, is split over K with a
+ * workspace of ws_bytes bytes: kb >= 32 and ws_bytes >=
+ * gemm_tail_workspace_bytes(tail_tiles); else 0. gemm_tail_workspace_bytes
+ * is 4096 bytes of flags plus four 64 KB slots per left-over tile. gemm_run
+ * calls the same rule. TPGEMM_ERR_INVALID_ARG on bad arguments.
+ */
+int gemm_tail_ksplit(int split, int64_t kb, int64_t tail_tiles, int64_t ws_bytes);
+int64_t gemm_tail_workspace_bytes(int64_t tail_tiles);
+
+/*
  * Allocation-free GEMM (no counterpart in the paper; it serves callers that
  * cannot allocate device memory). Some callers cannot call cudaMalloc: code
  * whose device memory must all come from a pool or arena owned by an outer

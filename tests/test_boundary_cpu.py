@@ -289,3 +289,30 @@ def test_schedule_rejects_bad_arguments():
     assert lib.gemm_schedule_tiles(4, 4, 8, 2, 0, 1, -1, None, 0) == tpd.ERR_INVALID_ARG
     assert lib.gemm_schedule_tiles(4, 4, 8, 2, 0, 1, 0, None, 3) == tpd.ERR_INVALID_ARG
     assert lib.gemm_schedule_workers(4, 4, 0, 0, 1) == tpd.ERR_INVALID_ARG
+
+
+# The K split tail's rule for CTA-pair schedules (gemm_run applies the same
+# function): column halves only, at least 32 K blocks, and a workspace that
+# holds 4 KB of flags plus four 64 KB partial-sum slots per left-over tile.
+def test_tail_workspace_bytes():
+    assert tpd.gemm_tail_workspace_bytes(0) == 4096
+    assert tpd.gemm_tail_workspace_bytes(28) == 4096 + 28 * 4 * 65536
+    assert tpd.gemm_tail_workspace_bytes(-1) == tpd.ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("split,kb,tiles,ws_mult,want", [
+    (2, 64, 28, 1, 1),    # square 4096^3: 28 left over, 64 K blocks
+    (2, 32, 28, 1, 1),    # the threshold itself
+    (2, 31, 28, 1, 0),    # one K block short: the exchange would not pay
+    (1, 64, 28, 1, 0),    # no halves (mlp_down: 56 left over on 76 pairs)
+    (2, 64, 28, 0, 0),    # workspace one byte too small
+    (2, 64, 0, 1, 0),     # no partial round
+])
+def test_tail_ksplit_choice(split, kb, tiles, ws_mult, want):
+    ws = tpd.gemm_tail_workspace_bytes(tiles) - (0 if ws_mult else 1)
+    assert tpd.gemm_tail_ksplit(split, kb, tiles, ws) == want
+
+
+def test_tail_ksplit_rejects_bad_arguments():
+    for bad in [(0, 64, 1, 1 << 24), (2, 0, 1, 1 << 24), (2, 64, -1, 1 << 24), (2, 64, 1, -1)]:
+        assert tpd.gemm_tail_ksplit(*bad) == tpd.ERR_INVALID_ARG, bad

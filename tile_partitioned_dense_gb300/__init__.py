@@ -88,6 +88,8 @@ def load_library() -> ctypes.CDLL:
             "gemm_set_workspace": (i32, [vp, vp, i64, vp]),
             "gemm_workspace_size": (i64, [vp]),
             "gemm_plan_tail_ksplit": (i32, [vp, i64, i64, i64, i32]),
+            "gemm_tail_ksplit": (i32, [i32, i64, i64, i64]),
+            "gemm_tail_workspace_bytes": (i64, [i64]),
             "gemm_run_noalloc": (i32, [i64, i64, i64, vp, i64, vp, i64, vp, i64, vp, i64, f32, f32, i32, vp,
                                        i32]),
         }
@@ -223,6 +225,14 @@ def gemm_workspace_size(h) -> int:
 
 def gemm_plan_tail_ksplit(h, M, N, K, out_dtype) -> int:
     return load_library().gemm_plan_tail_ksplit(h, M, N, K, out_dtype)
+
+
+def gemm_tail_ksplit(split: int, kb: int, tail_tiles: int, ws_bytes: int) -> int:
+    return load_library().gemm_tail_ksplit(split, kb, tail_tiles, ws_bytes)
+
+
+def gemm_tail_workspace_bytes(tail_tiles: int) -> int:
+    return load_library().gemm_tail_workspace_bytes(tail_tiles)
 
 
 def gemm_run_noalloc(M, N, K, A, lda, B, ldb, C, ldc, D, ldd, alpha, beta, out_dtype, stream,

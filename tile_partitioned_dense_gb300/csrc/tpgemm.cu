@@ -62,6 +62,13 @@ int64_t tail_ws_bytes(int64_t tail_tiles) {
 // 256 x 256 K block's 0.336 us): the split pays from about 27 K blocks.
 constexpr int64_t kTailMinKb = 32;
 
+// Whether the last partial round of a CTA-pair schedule is split over K: its
+// tiles are cut into column halves (split == 2), K has at least kTailMinKb
+// blocks, and the workspace holds the tail's flags and partial sums.
+bool tail_ksplit_choice(int split, int64_t kb, int64_t tail_tiles, int64_t ws_bytes) {
+    return split == 2 && kb >= kTailMinKb && tail_tiles > 0 && tail_ws_bytes(tail_tiles) <= ws_bytes;
+}
+
 } // namespace
 
 struct tpgemm_handle {
@@ -375,8 +382,7 @@ Plan make_plan(tpgemm_handle *h, int64_t M, int64_t N, int64_t K, int out_dtype)
         // of a tile's K blocks, where a column half takes all of them. Only for
         // K of at least kTailMinKb blocks, where that outweighs the exchange.
         const int64_t kbt = (K + tpg::tiled::BK - 1) / tpg::tiled::BK;
-        if (pair && pl.sched.split == 2 && kbt >= kTailMinKb && h->ws &&
-            tail_ws_bytes(pl.sched.pieces / 2) <= h->ws_bytes)
+        if (pair && h->ws && tail_ksplit_choice(pl.sched.split, kbt, pl.sched.pieces / 2, h->ws_bytes))
             pl.ktail = 1;
         return pl;
     }
@@ -613,6 +619,16 @@ int gemm_stream_split(int64_t nt, int64_t kb, int mt_pad, int num_sms, const int
     if (nt < 1 || kb < 1 || mt_pad < 16 || mt_pad > 64 || mt_pad % 16 != 0 || num_sms < 1 || !clusters)
         return TPGEMM_ERR_INVALID_ARG;
     return stream_split_choice(nt, kb, mt_pad, num_sms, clusters, nullptr);
+}
+
+int gemm_tail_ksplit(int split, int64_t kb, int64_t tail_tiles, int64_t ws_bytes) {
+    if (split < 1 || kb < 1 || tail_tiles < 0 || ws_bytes < 0) return TPGEMM_ERR_INVALID_ARG;
+    return tail_ksplit_choice(split, kb, tail_tiles, ws_bytes) ? 1 : 0;
+}
+
+int64_t gemm_tail_workspace_bytes(int64_t tail_tiles) {
+    if (tail_tiles < 0) return TPGEMM_ERR_INVALID_ARG;
+    return tail_ws_bytes(tail_tiles);
 }
 
 int gemm_tiled_ksplit(int64_t tiles, int64_t kb, int cap2, int cap4) {
