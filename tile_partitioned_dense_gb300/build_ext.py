@@ -1,10 +1,10 @@
 """Builds libtpgemm.so in-tree with nvcc for sm_103a.
 
-Eight translation units compiled in parallel: the host library (tpgemm.cu),
+Nine translation units compiled in parallel: the host library (tpgemm.cu),
 the streaming-kernel instantiations (stream_inst.cu), the tiled-kernel
 instantiations, one per fused-epilogue mode (tiled_inst.cu with
--DTPG_EPI=0..4), and the grouped tiled kernel (-DTPG_GROUPED=1); then one
-link.
+-DTPG_EPI=0..5, 5 being the plain epilogue for alpha == 1), and the grouped
+tiled kernel (-DTPG_GROUPED=1); then one link.
 """
 from __future__ import annotations
 
@@ -23,7 +23,7 @@ FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-std=c++17", "-li
          f"-I{INCLUDE}", f"-I{CSRC}"]
 
 UNITS = [("tpgemm.o", "tpgemm.cu", []), ("stream_inst.o", "stream_inst.cu", [])] + [
-    (f"tiled_e{e}.o", "tiled_inst.cu", [f"-DTPG_EPI={e}"]) for e in range(5)] + [
+    (f"tiled_e{e}.o", "tiled_inst.cu", [f"-DTPG_EPI={e}"]) for e in range(6)] + [
     ("tiled_g0.o", "tiled_inst.cu", ["-DTPG_EPI=0", "-DTPG_GROUPED=1"])]
 
 

@@ -144,6 +144,8 @@ __device__ __forceinline__ Segment segment_of(int32_t tile_row, int32_t rows_per
 
 namespace tiled {
 
+constexpr int kEpiUnitAlpha = 5; // see gemm_tiled_kernel's kEpi
+
 constexpr int BM = 128;  // rows per CTA
 constexpr int BN = 256;  // columns per tile
 constexpr int BK = 64;
@@ -225,7 +227,10 @@ __device__ __forceinline__ void settle(uint64_t ns) {
     }
 }
 
-// kEpi: 0 plain alpha*acc + beta*C; 1 + activation for the fused epilogue
+// kEpi: 0 plain alpha*acc + beta*C; 1 + activation for the fused epilogue;
+// kEpiUnitAlpha the plain epilogue for alpha == 1, without the multiply (the
+// epilogue's instructions share an SM sub-partition with the thread that
+// issues the MMAs, which they slow down).
 // (bias and aux are runtime options; the activation is compiled in, so each
 // instantiation carries only its own math). kKsplit: the 1-CTA mode's K split
 // (p.ksplit CTAs of a cluster per tile); the other instantiations carry none
@@ -237,6 +242,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                       const TiledParams p, const __grid_constant__ SegArg<kGrouped> seg) {
     using L = Layout<kPair>;
     constexpr int STAGES = L::STAGES;
+    constexpr bool kFused = kEpi > 0 && kEpi != kEpiUnitAlpha; // bias / activation / aux
     constexpr int CHUNK = kOutF32 ? 32 : 64; // output columns per 128-byte staging row
     constexpr int CL = kPair ? 2 : 1;        // CTAs per worker
 
@@ -707,7 +713,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 // Fused epilogue: this row's aux cells for the chunk, all in flight at once,
                 // while the staging buffer frees up and C arrives.
                 uint4 auxq[8];
-                if constexpr (kEpi > 0) {
+                if constexpr (kFused) {
 #pragma unroll
                     for (int j = 0; j < 8; ++j)
                         auxq[j] = load_aux_cell<kOutF32>(p.epi, p.N, grow, row_ok, cb + j * (kOutF32 ? 4 : 8));
@@ -751,7 +757,9 @@ __global__ void __launch_bounds__(THREADS, 1)
                     if constexpr (kOutF32) {
                         float v[4];
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) v[e] = p.alpha * __uint_as_float(r0[j * 4 + e]);
+                        for (int e = 0; e < 4; ++e)
+                            v[e] = kEpi == kEpiUnitAlpha ? __uint_as_float(r0[j * 4 + e])
+                                                         : p.alpha * __uint_as_float(r0[j * 4 + e]);
                         if (tail) {
                             // ragged last columns: plain loads and stores of this row
 #pragma unroll
@@ -760,7 +768,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                                 if (has_beta && row_ok && col < p.N)
                                     v[e] = fmaf(p.beta, static_cast<const float *>(p.C)[crow + col], v[e]);
                             }
-                            if constexpr (kEpi > 0) epilogue_cell<4, true, kEpi - 1>(p.epi, p.N, grow, row_ok, cb + j * 4, v, auxq[j]);
+                            if constexpr (kFused) epilogue_cell<4, true, kFused ? kEpi - 1 : 0>(p.epi, p.N, grow, row_ok, cb + j * 4, v, auxq[j]);
 #pragma unroll
                             for (int e = 0; e < 4; ++e) {
                                 const int32_t col = cb + j * 4 + e;
@@ -775,7 +783,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                             v[2] = fmaf(p.beta, __uint_as_float(cv.z), v[2]);
                             v[3] = fmaf(p.beta, __uint_as_float(cv.w), v[3]);
                         }
-                        if constexpr (kEpi > 0) epilogue_cell<4, true, kEpi - 1>(p.epi, p.N, grow, row_ok, cb + j * 4, v, auxq[j]);
+                        if constexpr (kFused) epilogue_cell<4, true, kFused ? kEpi - 1 : 0>(p.epi, p.N, grow, row_ok, cb + j * 4, v, auxq[j]);
                         *cell = make_uint4(__float_as_uint(v[0]), __float_as_uint(v[1]), __float_as_uint(v[2]),
                                            __float_as_uint(v[3]));
                     } else {
@@ -783,7 +791,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
                         for (int e = 0; e < 8; ++e) {
                             const uint32_t bits = (j < 4) ? r0[j * 8 + e] : r1[(j - 4) * 8 + e];
-                            v[e] = p.alpha * __uint_as_float(bits);
+                            v[e] = kEpi == kEpiUnitAlpha ? __uint_as_float(bits) : p.alpha * __uint_as_float(bits);
                         }
                         if (tail) {
 #pragma unroll
@@ -794,7 +802,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                                     v[e] = fmaf(p.beta, __uint_as_float(static_cast<uint32_t>(cbits) << 16), v[e]);
                                 }
                             }
-                            if constexpr (kEpi > 0) epilogue_cell<8, false, kEpi - 1>(p.epi, p.N, grow, row_ok, cb + j * 8, v, auxq[j]);
+                            if constexpr (kFused) epilogue_cell<8, false, kFused ? kEpi - 1 : 0>(p.epi, p.N, grow, row_ok, cb + j * 8, v, auxq[j]);
 #pragma unroll
                             for (int e = 0; e < 8; ++e) {
                                 const int32_t col = cb + j * 8 + e;
@@ -813,7 +821,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                                 v[2 * e + 1] = fmaf(p.beta, bf16hi_to_f32(cw[e]), v[2 * e + 1]);
                             }
                         }
-                        if constexpr (kEpi > 0) epilogue_cell<8, false, kEpi - 1>(p.epi, p.N, grow, row_ok, cb + j * 8, v, auxq[j]);
+                        if constexpr (kFused) epilogue_cell<8, false, kFused ? kEpi - 1 : 0>(p.epi, p.N, grow, row_ok, cb + j * 8, v, auxq[j]);
                         *cell = make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]), pack_bf16x2(v[4], v[5]),
                                            pack_bf16x2(v[6], v[7]));
                     }

@@ -47,8 +47,9 @@ cudaError_t launch_ex(Kernel kernel, int grid, int block, int smem, int cluster,
 
 // Fused-epilogue modes of the tiled kernel (its kEpi template argument):
 // 0 plain alpha*acc + beta*C; 1 + activation otherwise (bias and aux are
-// runtime options inside every fused mode).
-constexpr int kEpiModes = 5;
+// runtime options inside every fused mode); 5 (tiled::kEpiUnitAlpha) the
+// plain epilogue for alpha == 1.
+constexpr int kEpiModes = 6;
 
 struct TiledLaunch {
     int grid;
@@ -79,11 +80,13 @@ cudaError_t tiled_launch_e1(const TiledLaunch &l);
 cudaError_t tiled_launch_e2(const TiledLaunch &l);
 cudaError_t tiled_launch_e3(const TiledLaunch &l);
 cudaError_t tiled_launch_e4(const TiledLaunch &l);
+cudaError_t tiled_launch_e5(const TiledLaunch &l);
 bool tiled_set_limits_e0();
 bool tiled_set_limits_e1();
 bool tiled_set_limits_e2();
 bool tiled_set_limits_e3();
 bool tiled_set_limits_e4();
+bool tiled_set_limits_e5();
 // grouped GEMM (plain epilogue), from tiled_inst.cu with -DTPG_EPI=0 -DTPG_GROUPED=1
 cudaError_t tiled_launch_g0(const TiledLaunch &l);
 bool tiled_set_limits_g0();

@@ -5,7 +5,7 @@
 #include "launch.cuh"
 
 #ifndef TPG_EPI
-#error "compile with -DTPG_EPI=<0..4>"
+#error "compile with -DTPG_EPI=<0..5>"
 #endif
 #ifndef TPG_GROUPED
 #define TPG_GROUPED 0

@@ -427,6 +427,7 @@ bool set_smem_limits() {
     ok = tpg::tiled_set_limits_e2() && ok;
     ok = tpg::tiled_set_limits_e3() && ok;
     ok = tpg::tiled_set_limits_e4() && ok;
+    ok = tpg::tiled_set_limits_e5() && ok;
     ok = tpg::stream_set_limits() && ok;
     return ok;
 }
@@ -472,6 +473,7 @@ int launch_tiled(int mode, const tpg::TiledLaunch &l) {
     case 2: e = tpg::tiled_launch_e2(l); break;
     case 3: e = tpg::tiled_launch_e3(l); break;
     case 4: e = tpg::tiled_launch_e4(l); break;
+    case tpg::tiled::kEpiUnitAlpha: e = tpg::tiled_launch_e5(l); break;
     default: e = tpg::tiled_launch_e0(l); break;
     }
     return e == cudaSuccess ? TPGEMM_OK : TPGEMM_ERR_CUDA;
@@ -768,7 +770,7 @@ int run_impl(tpgemm_handle *h, int64_t M, int64_t N, int64_t K, const void *A, i
         }
         const tpg::TiledLaunch l{pl.grid, pl.smem, pl.cluster, pl.variant == TPGEMM_VARIANT_TILED_PAIR, f32, stream,
                                  &tmA, &tmB, &tmB1, &tmC, &tmD, &p, nullptr};
-        return launch_tiled(fused ? 1 + ep.act : 0, l);
+        return launch_tiled(fused ? 1 + ep.act : (alpha == 1.0f ? tpg::tiled::kEpiUnitAlpha : 0), l);
     }
 
     // weight-streaming variant
@@ -863,7 +865,7 @@ int gemm_run_batched(tpgemm_handle *h, int64_t batch, int64_t M, int64_t N, int6
     const int smem = static_cast<int>(pair ? tpg::tiled::Layout<true>::SMEM_BYTES : tpg::tiled::Layout<false>::SMEM_BYTES);
     const tpg::TiledLaunch l{static_cast<int>(p.sched.workers * (pair ? 2 : 1)), smem, pair ? 2 : 1, pair, f32, stream,
                              &tmA, &tmB, &tmB1, &tmC, &tmD, &p, nullptr};
-    return launch_tiled(0, l);
+    return launch_tiled(p.alpha == 1.0f ? tpg::tiled::kEpiUnitAlpha : 0, l);
 }
 
 int gemm_run_grouped(tpgemm_handle *h, int64_t groups, const int64_t *group_rows, int64_t N, int64_t K,
