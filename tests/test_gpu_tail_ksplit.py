@@ -279,3 +279,21 @@ def test_small_workspace_falls_back():
         torch.cuda.synchronize()
     finally:
         tpd.gemm_destroy(h)
+
+
+def test_gemm_object_with_a_workspace():
+    """The torch convenience class attaches its own workspace when asked, uses
+    the K split tail, and detaches it on close."""
+    g = tpd.Gemm(0, workspace=True)
+    try:
+        M, N, K = 2560, 2048, 2048
+        if _full_size_gpu(g.handle):
+            assert tpd.gemm_plan_tail_ksplit(g.handle, M, N, K, tpd.OUT_BF16) == 1
+        A, B, _ = make_inputs(CONFIGS["square"], integer=True, M=M, N=N, K=K, seed=61)
+        D = g(to_device(A), to_device(B), out_dtype=torch.bfloat16)
+        torch.cuda.synchronize()
+        assert tpd.gemm_sync_status(g.handle, None) == tpd.OK
+        assert_bit_exact(bits(D), oracle_out(A, B, None, 1.0, 0.0, torch.bfloat16), "Gemm(workspace=True)")
+    finally:
+        g.close()
+    assert g.handle is None

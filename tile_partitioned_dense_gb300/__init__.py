@@ -246,14 +246,38 @@ def gemm_run_noalloc(M, N, K, A, lda, B, ldb, C, ldc, D, ldd, alpha, beta, out_d
 # ------------------------------------------------------------------ torch convenience
 
 class Gemm:
-    """Owns one handle; ``__call__`` runs D = alpha*A*B + beta*C on torch tensors."""
+    """Owns one handle; ``__call__`` runs D = alpha*A*B + beta*C on torch tensors.
 
-    def __init__(self, device: int = 0):
+    workspace=True allocates the handle's workspace (gemm_workspace_size bytes,
+    through torch) and attaches it, so that the CTA-pair kernel may split the
+    last partial round over K; calls through this object must then not overlap
+    on the GPU (issue them on one stream, or order them with events).
+    """
+
+    def __init__(self, device: int = 0, workspace: bool = False):
         self.device = int(device)
         self.handle = gemm_create(self.device)
+        self._ws = None
+        if workspace:
+            import torch
+            nbytes = gemm_workspace_size(self.handle)
+            if nbytes < 0:
+                raise TpgemmError(int(nbytes), "gemm_workspace_size")
+            buf = torch.empty(nbytes + 256, dtype=torch.uint8, device=f"cuda:{self.device}")
+            ptr = (buf.data_ptr() + 255) // 256 * 256
+            st = gemm_set_workspace(self.handle, ptr, nbytes,
+                                    torch.cuda.current_stream(self.device).cuda_stream)
+            if st != OK:
+                raise TpgemmError(st, "gemm_set_workspace")
+            self._ws = buf
 
     def close(self):
         if self.handle is not None:
+            if self._ws is not None:
+                import torch
+                torch.cuda.synchronize(self.device)  # every call that used the workspace has finished
+                gemm_set_workspace(self.handle, None, 0, None)
+                self._ws = None
             gemm_destroy(self.handle)
             self.handle = None
 
