@@ -230,10 +230,10 @@ __device__ __forceinline__ void settle(uint64_t ns) {
 // kEpi: 0 plain alpha*acc + beta*C; 1 + activation for the fused epilogue
 // (bias and aux are runtime options; the activation is compiled in, so each
 // instantiation carries only its own math); kEpiUnitAlpha the plain epilogue
-// for alpha == 1, without the multiply (the epilogue's instructions share an
-// SM sub-partition with the thread that issues the MMAs, which they slow
-// down). kKsplit: the 1-CTA mode's K split (p.ksplit CTAs of a cluster per
-// tile); the other instantiations carry none of its code.
+// for alpha == 1, without the multiply (the epilogue's work runs beside the
+// next tile's MMAs and slows them, in proportion to how much of it there is).
+// kKsplit: the 1-CTA mode's K split (p.ksplit CTAs of a cluster per tile);
+// the other instantiations carry none of its code.
 template <bool kOutF32, bool kPair, int kEpi, bool kGrouped = false, bool kKsplit = false>
 __global__ void __launch_bounds__(THREADS, 1)
     gemm_tiled_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
