@@ -128,6 +128,11 @@ typedef struct tpgemm_epilogue {
  * tensor-map encoder, sets the kernels' shared-memory limits and allocates
  * the 8-byte device status word (the only allocation the library makes).
  * *out is set to NULL on failure. Not called on a hot path.
+ * Everything that allocates or queries the device happens here, once, so
+ * that the calls made per GEMM allocate nothing and can be captured into a
+ * graph and replayed ("cuTile Rust explained", "Why scoped graph capture
+ * helps borrowing": only operations that allocate nothing are safe to
+ * capture). The handle owns its status word; the caller owns the handle.
  */
 int gemm_create(tpgemm_handle **out, int device);
 
@@ -232,7 +237,12 @@ int gemm_run_chunked(tpgemm_handle *h, int chunks, int64_t M, int64_t N, int64_t
  * Synchronises `stream`, then reads and clears the handle's device status
  * word. Returns TPGEMM_OK, TPGEMM_ERR_TIMEOUT if any kernel since the last
  * call gave up on a pipeline wait (its output is then incomplete), or
- * TPGEMM_ERR_CUDA if the synchronisation failed.
+ * TPGEMM_ERR_CUDA if the synchronisation failed. A wait that cannot finish
+ * must end in a reported error rather than a hang, and the error must reach
+ * the host so that the caller can recover ("Implementing Tensor Parallelism
+ * Communication Overlays ...", "Real-world Failure Modes: Deadlocks,
+ * Timeouts, and Error Recovery"): every pipeline wait in the kernels has a
+ * time limit, and this call is where its expiry is read.
  */
 int gemm_sync_status(tpgemm_handle *h, void *stream);
 
@@ -246,7 +256,14 @@ int gemm_check_args(int64_t M, int64_t N, int64_t K, const void *A, int64_t lda,
                     int64_t ldb, const void *C, int64_t ldc, const void *D, int64_t ldd, float beta,
                     int out_dtype);
 
-/* Frees the handle and its status word. NULL is accepted. */
+/*
+ * Frees the handle and its status word. NULL is accepted. Work is
+ * asynchronous, so the handle (like every buffer a call reads or writes)
+ * must outlive the calls enqueued with it: destroy it only after the streams
+ * of those calls have passed them ("Implementing Tensor Parallelism
+ * Communication Overlays ...", "Preventing Rust Lifetime Pitfalls in Async
+ * GPU Operations").
+ */
 int gemm_destroy(tpgemm_handle *h);
 
 /* Static, human-readable name of a tpgemm_status value. */
@@ -352,6 +369,18 @@ int gemm_num_sms(tpgemm_handle *h);
  *               is then ignored) and restores the behaviour without one.
  *   stream      the workspace's flags are cleared on this stream; enqueue the
  *               calls that use it after that point.
+ * Co-residency: the two pairs that share a tail tile wait for each other's
+ * partial sums, so the split assumes every CTA pair of the launch is resident
+ * at once. The grid is sized to the number of CTA pairs the occupancy API
+ * reports for the whole device, so that holds when the GPU runs this launch
+ * alone or beside kernels that leave it room. Where fewer SMs are available
+ * than the device reports (an MPS client limited to part of the GPU, a green
+ * context, kernels on other streams holding SMs for a long time), a pair may
+ * wait for a partner that cannot start until it exits: the wait then runs out
+ * after the handle's time limit and gemm_sync_status reports
+ * TPGEMM_ERR_TIMEOUT with the output incomplete. Such callers detach the
+ * workspace (ws == NULL), which restores the plan without waits between
+ * pairs.
  * Ownership stays with the caller: keep the memory allocated, and do not
  * touch it, until it is detached and every call that used it has finished.
  * Each call uses the whole workspace, so while one is attached, calls on the

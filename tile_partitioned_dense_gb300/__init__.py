@@ -250,8 +250,10 @@ class Gemm:
 
     workspace=True allocates the handle's workspace (gemm_workspace_size bytes,
     through torch) and attaches it, so that the CTA-pair kernel may split the
-    last partial round over K; calls through this object must then not overlap
-    on the GPU (issue them on one stream, or order them with events).
+    last partial round over K; the constructor waits until the workspace's
+    flags are clear, so the first call may go to any stream, but calls through
+    this object must then not overlap on the GPU (issue them on one stream, or
+    order them with events).
     """
 
     def __init__(self, device: int = 0, workspace: bool = False):
@@ -269,6 +271,9 @@ class Gemm:
                                     torch.cuda.current_stream(self.device).cuda_stream)
             if st != OK:
                 raise TpgemmError(st, "gemm_set_workspace")
+            # The flags are cleared on the current stream; wait for that here so
+            # that calls on any stream are ordered after it.
+            torch.cuda.current_stream(self.device).synchronize()
             self._ws = buf
 
     def close(self):
