@@ -26,9 +26,14 @@ ACT_NONE = 0
 ACT_RELU = 1
 ACT_SIGMOID = 2
 ACT_TANH = 3
+FP8_E4M3 = 0
+FP8_E5M2 = 1
+SCALE_E8M0 = 2
+MX_BLOCK = 32
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "oracle.c")
+_SRCS = [_SRC, os.path.join(_HERE, "oracle_mx.c")]
 _LIB = os.path.join(_HERE, "liboracle.so")
 _lock = threading.Lock()
 _lib = None
@@ -37,11 +42,11 @@ _lib = None
 def build(force: bool = False) -> str:
     """Compile oracle.c into liboracle.so (plain gcc, no contraction, no fast-math)."""
     with _lock:
-        stale = (not os.path.exists(_LIB)) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC)
+        stale = (not os.path.exists(_LIB)) or any(os.path.getmtime(_LIB) < os.path.getmtime(f) for f in _SRCS)
         if force or stale:
             tmp = _LIB + f".tmp{os.getpid()}"
             cmd = ["gcc", "-O2", "-ffp-contract=off", "-fno-fast-math", "-fPIC", "-shared",
-                   "-pthread", "-std=c11", "-Wall", "-o", tmp, _SRC, "-lm"]
+                   "-pthread", "-std=c11", "-Wall", "-o", tmp, *_SRCS, "-lm"]
             subprocess.run(cmd, check=True)
             os.replace(tmp, _LIB)
     return _LIB
@@ -70,6 +75,12 @@ def _load():
         lib.oracle_round_bf16_from_f32_bits.argtypes = [vp, vp, i64]
         lib.oracle_round_bf16_array.restype = None
         lib.oracle_round_bf16_array.argtypes = [vp, vp, i64]
+        lib.oracle_mx_gemm_rows.restype = ctypes.c_int
+        lib.oracle_mx_gemm_rows.argtypes = [i64, i64, i64, vp, i64, ctypes.c_int, vp, i64, vp, i64, ctypes.c_int,
+                                            vp, i64, vp, i64, dbl, dbl, ctypes.c_int, vp, i64, vp, i64, vp, i64,
+                                            ctypes.c_int]
+        lib.oracle_decode_mx_array.restype = None
+        lib.oracle_decode_mx_array.argtypes = [ctypes.c_int, vp, vp, i64]
         _lib = lib
     return _lib
 
@@ -202,3 +213,63 @@ def round_bf16_from_f32_bits(u: np.ndarray) -> np.ndarray:
 
 def round_f32(x: float) -> float:
     return float(_load().oracle_round_f32(float(x)))
+
+
+# ------------------------------------------------------------------ block-scaled (MX) GEMM
+
+def decode_mx(codes, fmt: int) -> np.ndarray:
+    """Values of 8-bit codes: fmt FP8_E4M3, FP8_E5M2 or SCALE_E8M0 (see oracle_mx.c)."""
+    c = np.ascontiguousarray(np.asarray(codes, dtype=np.uint8))
+    out = np.empty(c.shape, dtype=np.float64)
+    _load().oracle_decode_mx_array(int(fmt), c.ctypes.data, out.ctypes.data, c.size)
+    return out
+
+
+def _u8_view(t, name):
+    a = t.numpy() if isinstance(t, torch.Tensor) else t
+    if a.dtype != np.uint8 or a.ndim != 2:
+        raise ValueError(f"{name}: need a 2-D uint8 array")
+    if a.size and a.strides[1] != 1:
+        raise ValueError(f"{name}: need unit column stride")
+    return a, a.ctypes.data, (a.strides[0] if a.size else max(a.shape[1], 1))
+
+
+def mx_gemm_rows(A, SA, Bt, SB, C, alpha: float, beta: float, out_dtype: int, fmt_a: int = FP8_E4M3,
+                 fmt_b: int = FP8_E4M3, rows=None, want_pre: bool = False, nthreads: int | None = None):
+    """Rows `rows` (default: all) of the block-scaled GEMM
+        D = alpha * sum_b SA[:, b] SB[:, b]^T * (A_b Bt_b^T) + beta * C
+    on the CPU. A [M, K] and Bt [N, K] hold FP8 codes (uint8, row-major, any
+    row stride), SA [M, K/32] and SB [N, K/32] E8M0 scale codes; C is [M, N] of
+    the output dtype or None when beta == 0. Returns (D, pre) like gemm_rows."""
+    lib = _load()
+    A, a_ptr, lda = _u8_view(A, "A")
+    SA, sa_ptr, ldsa = _u8_view(SA, "SA")
+    Bt, b_ptr, ldb = _u8_view(Bt, "Bt")
+    SB, sb_ptr, ldsb = _u8_view(SB, "SB")
+    M, K = A.shape
+    N = Bt.shape[0]
+    if Bt.shape[1] != K or K % MX_BLOCK or SA.shape != (M, K // MX_BLOCK) or SB.shape != (N, K // MX_BLOCK):
+        raise ValueError("shapes of A, SA, Bt, SB do not agree")
+    alpha = float(np.float32(alpha))
+    beta = float(np.float32(beta))
+    if rows is None:
+        rows = np.arange(M, dtype=np.int64)
+    rows = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+    c_ptr, ldc = 0, max(N, 1)
+    if beta != 0.0:
+        want = torch.bfloat16 if out_dtype == OUT_BF16 else torch.float32
+        if C is None or C.dtype != want or tuple(C.shape) != (M, N):
+            raise ValueError("C must be [M,N] of the output dtype when beta != 0")
+        c_ptr, ldc = _bits_view(C, "C")
+    out_np = np.uint16 if out_dtype == OUT_BF16 else np.float32
+    D = np.zeros((len(rows), N), dtype=out_np)
+    pre = np.zeros((len(rows), N), dtype=np.float64) if want_pre else None
+    if nthreads is None:
+        nthreads = len(os.sched_getaffinity(0))
+    rc = lib.oracle_mx_gemm_rows(M, N, K, a_ptr, lda, int(fmt_a), sa_ptr, ldsa, b_ptr, ldb, int(fmt_b), sb_ptr,
+                                 ldsb, c_ptr, ldc, alpha, beta, out_dtype, rows.ctypes.data, len(rows),
+                                 D.ctypes.data, max(N, 1), pre.ctypes.data if pre is not None else None,
+                                 max(N, 1), int(nthreads))
+    if rc != 0:
+        raise RuntimeError("oracle_mx_gemm_rows rejected its arguments")
+    return D, pre
