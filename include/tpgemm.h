@@ -420,6 +420,66 @@ int gemm_plan_tail_ksplit(tpgemm_handle *h, int64_t M, int64_t N, int64_t K, int
 int gemm_tail_ksplit(int split, int64_t kb, int64_t tail_tiles, int64_t ws_bytes);
 int64_t gemm_tail_workspace_bytes(int64_t tail_tiles);
 
+/* FP8 element formats of the block-scaled GEMM (OCP Microscaling v1.0). */
+enum tpgemm_fp8_format {
+    TPGEMM_FP8_E4M3 = 0, /* bias 7, no infinities, largest finite 448 */
+    TPGEMM_FP8_E5M2 = 1  /* bias 15, IEEE-style infinities and NaNs, largest finite 57344 */
+};
+
+/*
+ * Block-scaled GEMM, MXFP8 (scaled_mm): "TorchInductor ganha suporte a GEMMs de
+ * alta performance com CuteDSL" lists scaled_mm among the GEMMs its backend
+ * covers (the enablement paragraph) and reports MXFP8 results (the results
+ * paragraph). The page defines no format; the formats are those of the OCP
+ * Microscaling (MX) v1.0 specification: every 32 consecutive elements along K
+ * share one E8M0 scale (2^(e - 127), e = 255 is NaN), per row of A and per
+ * column of B. With A_b, B_b the b-th 32-wide K block:
+ *     D = alpha * sum_b (SA[:, b] SB[:, b]^T) .* (A_b * B_b) + beta * C
+ * accumulated in fp32 on the tensor cores (tcgen05.mma kind::mxf8f6f4 applies
+ * the scales), then alpha, beta*C and one rounding as in gemm_run.
+ *   M, N, K     >= 0, each <= 2^31 - 1; K a multiple of 32.
+ *   A, lda      FP8 codes (a_format), row-major [M, K], lda >= K bytes, a
+ *               multiple of 16 (not checked for M == 1).
+ *   B, ldb      FP8 codes (b_format) of B TRANSPOSED: row-major [N, K] (B in
+ *               column-major order, as fp8 scaled_mm takes it), ldb >= K
+ *               bytes, a multiple of 16 (not checked for N == 1).
+ *   SA, SB      E8M0 scale codes of A's M rows and B's N columns, each in the
+ *               blocked layout: 512-byte chunks of 128 rows x 4 scale columns,
+ *               chunk (row block rb, column block cb) at byte
+ *               (rb * ceil(K/128) + cb) * 512, and inside it the scale of row
+ *               r, scale column c at byte (r % 32) * 16 + (r / 32) * 4 + c;
+ *               gemm_mx_scale_bytes(M, K) and (N, K) bytes, 16-byte aligned.
+ *               This is the layout NVIDIA's libraries take for MX scales, so
+ *               scales prepared for them can be passed as they are. Bytes of
+ *               rows past M (N) or scale columns past K/32 are read and must
+ *               hold finite scales (any code but 255; zero is fine).
+ *   C, ldc, D, ldd, alpha, beta, out_dtype   as gemm_run.
+ * K == 0 gives D = beta*C. D may equal C (same stride); any other overlap of
+ * D with A, B, SA, SB or C is TPGEMM_ERR_OVERLAP. Errors as gemm_run, plus
+ * TPGEMM_ERR_INVALID_ARG for a bad format or K not a multiple of 32.
+ * Allocates nothing and never synchronises. Runs a persistent 1-CTA kernel of
+ * 128 x 192 tiles (128 x 128 when N <= 128).
+ */
+int gemm_run_mx(tpgemm_handle *h, int64_t M, int64_t N, int64_t K, const void *A, int64_t lda, int a_format,
+                const void *SA, const void *B, int64_t ldb, int b_format, const void *SB, const void *C,
+                int64_t ldc, void *D, int64_t ldd, float alpha, float beta, int out_dtype, void *stream);
+
+/* Bytes of one operand's scales in gemm_run_mx's blocked layout:
+ * ceil(rows / 128) * ceil(K / 128) * 512; TPGEMM_ERR_INVALID_ARG for negative sizes. */
+int64_t gemm_mx_scale_bytes(int64_t rows, int64_t K);
+
+/* The argument checks of gemm_run_mx alone (no handle, no GPU; pointers are
+ * only compared and tested for alignment). */
+int gemm_mx_check_args(int64_t M, int64_t N, int64_t K, const void *A, int64_t lda, int a_format, const void *SA,
+                       const void *B, int64_t ldb, int b_format, const void *SB, const void *C, int64_t ldc,
+                       const void *D, int64_t ldd, float beta, int out_dtype);
+
+/* What gemm_run_mx launches for this shape: tile rows and columns, tiles, grid
+ * (CTAs, one per SM at most) and dynamic shared memory per CTA. Any output
+ * pointer may be NULL. */
+int gemm_mx_query_plan(tpgemm_handle *h, int64_t M, int64_t N, int64_t K, int *tile_m, int *tile_n,
+                       int64_t *num_tiles, int *grid, int *smem_bytes);
+
 /*
  * Allocation-free GEMM (no counterpart in the paper; it serves callers that
  * cannot allocate device memory). Some callers cannot call cudaMalloc: code

@@ -316,3 +316,50 @@ def test_tail_ksplit_choice(split, kb, tiles, ws_mult, want):
 def test_tail_ksplit_rejects_bad_arguments():
     for bad in [(0, 64, 1, 1 << 24), (2, 0, 1, 1 << 24), (2, 64, -1, 1 << 24), (2, 64, 1, -1)]:
         assert tpd.gemm_tail_ksplit(*bad) == tpd.ERR_INVALID_ARG, bad
+
+
+# ---------------------------------------------------------------- block-scaled (MX) argument checks
+
+def mx_chk(M=128, N=128, K=256, A=A0, lda=None, fa=0, SA=0x50000000, B=B0, ldb=None, fb=0, SB=0x60000000, C=None,
+           ldc=None, D=D0, ldd=None, beta=0.0, out=tpd.OUT_BF16):
+    lda = K if lda is None else lda
+    ldb = K if ldb is None else ldb
+    ldc = N if ldc is None else ldc
+    ldd = N if ldd is None else ldd
+    return tpd.gemm_mx_check_args(M, N, K, A, lda, fa, SA, B, ldb, fb, SB, C, ldc, D, ldd, beta, out)
+
+
+def test_mx_scale_bytes():
+    assert tpd.gemm_mx_scale_bytes(128, 128) == 512
+    assert tpd.gemm_mx_scale_bytes(129, 128) == 1024
+    assert tpd.gemm_mx_scale_bytes(128, 160) == 1024
+    assert tpd.gemm_mx_scale_bytes(8192, 4096) == 64 * 32 * 512
+    assert tpd.gemm_mx_scale_bytes(0, 4096) == 0
+    assert tpd.gemm_mx_scale_bytes(-1, 32) == tpd.ERR_INVALID_ARG
+
+
+def test_mx_check_args():
+    assert mx_chk() == tpd.OK
+    assert mx_chk(K=96) == tpd.OK
+    assert mx_chk(K=100) == tpd.ERR_INVALID_ARG
+    assert mx_chk(fa=2) == tpd.ERR_INVALID_ARG and mx_chk(fb=-1) == tpd.ERR_INVALID_ARG
+    assert mx_chk(out=5) == tpd.ERR_INVALID_ARG
+    assert mx_chk(lda=128) == tpd.ERR_INVALID_ARG and mx_chk(ldb=255) == tpd.ERR_INVALID_ARG
+    assert mx_chk(lda=264) == tpd.ERR_ALIGNMENT and mx_chk(ldb=264) == tpd.ERR_ALIGNMENT
+    assert mx_chk(M=1, lda=264) == tpd.OK  # one row: its stride is not used
+    assert mx_chk(SA=0x50000008) == tpd.ERR_ALIGNMENT and mx_chk(SB=0x60000004) == tpd.ERR_ALIGNMENT
+    assert mx_chk(SA=None) == tpd.ERR_INVALID_ARG
+    assert mx_chk(M=2 ** 31) == tpd.ERR_TOO_LARGE
+    assert mx_chk(M=0) == tpd.OK and mx_chk(N=0, D=None) == tpd.OK
+    assert mx_chk(K=0, A=None, B=None, SA=None, SB=None) == tpd.OK
+    assert mx_chk(beta=1.0) == tpd.ERR_INVALID_ARG  # C missing
+    assert mx_chk(beta=1.0, C=D0) == tpd.OK          # in place
+    assert mx_chk(beta=1.0, C=D0 + 16) == tpd.ERR_OVERLAP
+    assert mx_chk(D=0x50000000 + 256) == tpd.ERR_OVERLAP  # D inside A's scales
+    assert mx_chk(D=A0 + 64) == tpd.ERR_OVERLAP
+    assert mx_chk(D=B0) == tpd.ERR_OVERLAP
+
+
+def test_mx_null_handle():
+    assert tpd.gemm_run_mx(None, 8, 8, 32, A0, 32, 0, 0x50000000, B0, 32, 0, 0x60000000, None, 8, D0, 8, 1.0, 0.0,
+                           tpd.OUT_F32, None) == tpd.ERR_INVALID_ARG

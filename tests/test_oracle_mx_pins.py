@@ -257,3 +257,19 @@ def test_bad_arguments_are_rejected():
                             oracle.OUT_F32)
     with pytest.raises(RuntimeError):
         oracle.mx_gemm_rows(z, s, z, s, None, 1.0, 0.0, oracle.OUT_F32, fmt_a=3)
+
+
+def test_blocked_scale_layout_helper_matches_its_definition():
+    """The test harness's rearrangement of row-major scales into the kernel's
+    blocked layout, checked byte by byte against the layout's definition."""
+    from _gpu import mx_blocked
+    rng = np.random.default_rng(9)
+    for R, nb in [(128, 4), (130, 5), (300, 3), (1, 1)]:
+        S = rng.integers(0, 255, size=(R, nb), dtype=np.uint8)
+        got = mx_blocked(S)
+        kc = -(-nb // 4)
+        assert got.size == -(-R // 128) * kc * 512
+        for r in range(R):
+            for c in range(nb):
+                off = ((r // 128) * kc + c // 4) * 512 + (r % 32) * 16 + ((r % 128) // 32) * 4 + c % 4
+                assert got[off] == S[r, c]

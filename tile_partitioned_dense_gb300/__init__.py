@@ -28,6 +28,9 @@ ACT_RELU = 1
 ACT_SIGMOID = 2
 ACT_TANH = 3
 
+FP8_E4M3 = 0
+FP8_E5M2 = 1
+
 OK = 0
 ERR_INVALID_ARG = -1
 ERR_ALIGNMENT = -2
@@ -92,6 +95,12 @@ def load_library() -> ctypes.CDLL:
             "gemm_tail_workspace_bytes": (i64, [i64]),
             "gemm_run_noalloc": (i32, [i64, i64, i64, vp, i64, vp, i64, vp, i64, vp, i64, f32, f32, i32, vp,
                                        i32]),
+            "gemm_run_mx": (i32, [vp, i64, i64, i64, vp, i64, i32, vp, vp, i64, i32, vp, vp, i64, vp, i64, f32, f32,
+                                  i32, vp]),
+            "gemm_mx_scale_bytes": (i64, [i64, i64]),
+            "gemm_mx_check_args": (i32, [i64, i64, i64, vp, i64, i32, vp, vp, i64, i32, vp, vp, i64, vp, i64, f32,
+                                         i32]),
+            "gemm_mx_query_plan": (i32, [vp, i64, i64, i64, pi32, pi32, pi64, pi32, pi32]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -241,6 +250,34 @@ def gemm_run_noalloc(M, N, K, A, lda, B, ldb, C, ldc, D, ldd, alpha, beta, out_d
     that cannot call cudaMalloc (see include/tpgemm.h)."""
     return load_library().gemm_run_noalloc(M, N, K, A, lda, B, ldb, C, ldc, D, ldd, alpha, beta,
                                            out_dtype, stream, int(check_status))
+
+
+def gemm_run_mx(h, M, N, K, A, lda, a_format, SA, B, ldb, b_format, SB, C, ldc, D, ldd, alpha, beta, out_dtype,
+                stream) -> int:
+    """Block-scaled (MXFP8) GEMM; B is passed transposed ([N, K] row-major) and
+    the scales in the blocked layout (see include/tpgemm.h)."""
+    return load_library().gemm_run_mx(h, M, N, K, A, lda, a_format, SA, B, ldb, b_format, SB, C, ldc, D, ldd,
+                                      alpha, beta, out_dtype, stream)
+
+
+def gemm_mx_scale_bytes(rows: int, K: int) -> int:
+    return load_library().gemm_mx_scale_bytes(rows, K)
+
+
+def gemm_mx_check_args(M, N, K, A, lda, a_format, SA, B, ldb, b_format, SB, C, ldc, D, ldd, beta, out_dtype) -> int:
+    return load_library().gemm_mx_check_args(M, N, K, A, lda, a_format, SA, B, ldb, b_format, SB, C, ldc, D, ldd,
+                                             beta, out_dtype)
+
+
+def gemm_mx_query_plan(h, M, N, K) -> dict:
+    tm, tn, grid, smem = (ctypes.c_int() for _ in range(4))
+    tiles = ctypes.c_int64()
+    st = load_library().gemm_mx_query_plan(h, M, N, K, ctypes.byref(tm), ctypes.byref(tn), ctypes.byref(tiles),
+                                           ctypes.byref(grid), ctypes.byref(smem))
+    if st != OK:
+        raise TpgemmError(st, "gemm_mx_query_plan")
+    return {"tile_m": tm.value, "tile_n": tn.value, "num_tiles": tiles.value, "grid": grid.value,
+            "smem_bytes": smem.value}
 
 
 # ------------------------------------------------------------------ torch convenience

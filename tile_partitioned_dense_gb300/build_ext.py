@@ -1,7 +1,8 @@
 """Builds libtpgemm.so in-tree with nvcc for sm_103a.
 
-Nine translation units compiled in parallel: the host library (tpgemm.cu),
-the streaming-kernel instantiations (stream_inst.cu), the tiled-kernel
+Ten translation units compiled in parallel: the host library (tpgemm.cu),
+the streaming-kernel instantiations (stream_inst.cu), the block-scaled (MX)
+kernel's (mx_inst.cu), the tiled-kernel
 instantiations, one per fused-epilogue mode (tiled_inst.cu with
 -DTPG_EPI=0..5, 5 being the plain epilogue for alpha == 1), and the grouped
 tiled kernel (-DTPG_GROUPED=1); then one link.
@@ -22,7 +23,7 @@ INCLUDE = os.path.join(ROOT, "include")
 FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC",
          f"-I{INCLUDE}", f"-I{CSRC}"]
 
-UNITS = [("tpgemm.o", "tpgemm.cu", []), ("stream_inst.o", "stream_inst.cu", [])] + [
+UNITS = [("tpgemm.o", "tpgemm.cu", []), ("stream_inst.o", "stream_inst.cu", []), ("mx_inst.o", "mx_inst.cu", [])] + [
     (f"tiled_e{e}.o", "tiled_inst.cu", [f"-DTPG_EPI={e}"]) for e in range(6)] + [
     ("tiled_g0.o", "tiled_inst.cu", ["-DTPG_EPI=0", "-DTPG_GROUPED=1"])]
 

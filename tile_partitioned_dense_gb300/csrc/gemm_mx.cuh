@@ -1,0 +1,440 @@
+// Persistent, warp-specialised block-scaled (MX) GEMM for sm_103a:
+//
+//     D = alpha * sum over K blocks b of (SA[:, b] SB[:, b]^T) .* (A_b * B_b) + beta * C
+//
+// the scaled_mm of "TorchInductor ganha suporte a GEMMs de alta performance
+// com CuteDSL" (the enablement paragraph names scaled_mm; the results paragraph
+// measures MXFP8). A and B hold FP8 elements (E4M3 or E5M2) and every 32
+// consecutive elements along K share one E8M0 scale per row of A and per
+// column of B, the MX formats of the OCP Microscaling specification. The
+// tensor cores apply the scales themselves: tcgen05.mma kind::mxf8f6f4 with
+// scale_vec::1X reads one scale byte per row (of A) and per column (of B) from
+// TMEM for each K = 32 instruction.
+//
+// One CTA per SM owns 128 x kBN output tiles (kBN = 128 or 192) of the same
+// grouped-raster persistent schedule as the bf16 kernel; each tile has one
+// owner ("cuTile Rust explained", "Ownership crosses the launch boundary").
+// Roles, connected by mbarriers:
+//   warp 0      TMA producer: per 128-wide K block, one A box (128 rows x 128
+//               bytes) and one B box (kBN rows of B's transpose x 128 bytes),
+//               both K-major with 128-byte swizzle, plus the K block's scale
+//               chunks: 512 bytes for A's 128 rows and one or two for B's rows,
+//               copied as they are from the caller's blocked scale layout.
+//   warp 1      allocates TMEM (two fp32 accumulators of kBN columns and, per
+//               ring stage, 4 scale columns for A and 8 for B); one lane copies
+//               each stage's scale chunks into TMEM (tcgen05.cp, 32 lanes x 16
+//               bytes, repeated in all four lane quarters) and issues the four
+//               K = 32 MMAs of the stage, scale byte j of each TMEM cell going
+//               with MMA j; tcgen05.commit frees the stage.
+//   warps 2-5   epilogue, as in the bf16 kernel: TMEM -> registers -> alpha,
+//               beta*C -> one rounding -> swizzled staging -> TMA store.
+//
+// The scale layout, per operand of R rows and K/32 scale columns: chunks of 128
+// rows x 4 scale columns (512 bytes), chunk (row block rb, column block cb)
+// at byte (rb * ceil(K/128) + cb) * 512, and inside a chunk the scale of row r,
+// column c at byte (r % 32) * 16 + (r / 32) * 4 + c. A chunk is therefore the
+// 32 x 16-byte matrix that tcgen05.cp places so that TMEM lane r % 32, column
+// r / 32, byte c holds scale (r, c): row r's scale for MMA c of the K block.
+// For B tiles of 192 columns a tile may start 64 rows into a chunk; its scale
+// columns then start two TMEM columns into the copied pair of chunks.
+#pragma once
+
+#include <cuda_bf16.h>
+
+#include "ptx.cuh"
+#include "schedule.cuh"
+
+namespace tpg {
+
+struct MxParams {
+    int32_t M, N, K;
+    int32_t kb;       // K blocks of 128
+    Schedule sched;   // 128 x kBN tiles, no column pieces
+    int32_t n_tma;    // columns [0, n_tma) of C and D go through the tensor maps (see TiledParams)
+    int32_t sfb_rows; // row blocks of 128 in B's scales: chunks past the last are not loaded
+    int64_t sf_kc;    // scale chunks per row block: ceil(K / 128)
+    const uint8_t *SA;
+    const uint8_t *SB;
+    uint32_t idesc;   // instruction descriptor without the scale-factor IDs
+    float alpha, beta;
+    const void *C;
+    int64_t ldc;
+    void *D;
+    int64_t ldd;
+    uint32_t *status;
+    uint64_t timeout_ns;
+};
+
+namespace mx {
+
+constexpr int BM = 128;
+constexpr int BK = 128; // K elements (bytes) per stage: four MMAs of K = 32, four scale columns
+constexpr int THREADS = 192;
+constexpr int EPI_THREADS = 128;
+constexpr uint32_t SF_CHUNK = 512;
+constexpr uint32_t EPI_BUF_BYTES = BM * 128;
+constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t SF_TMEM_STRIDE = 16; // TMEM columns per stage: A at +0 (4), B at +4 (8)
+
+template <int kBN>
+struct Layout {
+    static_assert(kBN == 128 || kBN == 192, "tile width");
+    static constexpr int STAGES = kBN == 192 ? 4 : 5;
+    static constexpr uint32_t A_BYTES = BM * BK;
+    static constexpr uint32_t B_BYTES = kBN * BK;
+    static constexpr uint32_t SF_BYTES = 2048; // A chunk at 0, B chunks at 512 and 1024
+    static constexpr uint32_t OFF_A = 0;
+    static constexpr uint32_t OFF_B = OFF_A + STAGES * A_BYTES;
+    static constexpr uint32_t OFF_SF = OFF_B + STAGES * B_BYTES;
+    static constexpr uint32_t OFF_EPI = OFF_SF + STAGES * SF_BYTES;
+    static constexpr uint32_t OFF_BAR = OFF_EPI + 2 * EPI_BUF_BYTES;
+    // full, empty, tfull, tempty, c, drain
+    static constexpr uint32_t NUM_BARS = 2 * STAGES + 2 + 2 + 2 + 1;
+    static constexpr uint32_t OFF_MISC = OFF_BAR + NUM_BARS * 8;
+    static constexpr uint32_t SMEM_BYTES = OFF_MISC + 16 + 1024;
+    static constexpr uint32_t SF_COL0 = 2 * kBN; // first TMEM column of the scale region
+    static_assert(SF_COL0 + STAGES * SF_TMEM_STRIDE <= TMEM_COLS, "TMEM overflow");
+    static_assert(SMEM_BYTES <= 232448, "exceeds the 227 KB shared-memory limit per CTA");
+};
+
+__device__ __forceinline__ bool mx_drain_wait(uint64_t *bar, uint32_t parity, uint64_t limit_ns) {
+    const uint32_t a = smem_addr(bar);
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t i = 0; i < (1u << 28); ++i) {
+        if (mbar_try_wait(a, parity)) return true;
+        if ((i & 63u) == 63u && globaltimer_ns() - t0 > limit_ns) return false;
+    }
+    return false;
+}
+
+template <bool kOutF32, int kBN>
+__global__ void __launch_bounds__(THREADS, 1)
+    gemm_mx_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmD,
+                   const MxParams p) {
+    using L = Layout<kBN>;
+    constexpr int STAGES = L::STAGES;
+    constexpr int CHUNK = kOutF32 ? 32 : 64; // output columns per 128-byte staging row
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                                ~static_cast<uintptr_t>(1023));
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::OFF_BAR);
+    uint64_t *full = bars;
+    uint64_t *empty = bars + STAGES;
+    uint64_t *tfull = bars + 2 * STAGES;
+    uint64_t *tempty = tfull + 2;
+    uint64_t *cbar = tempty + 2;
+    uint64_t *drain = cbar + 2;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::OFF_MISC);
+    volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(smem + L::OFF_MISC + 4);
+
+    const uint32_t warp = threadIdx.x / 32;
+    const uint32_t lane = threadIdx.x % 32;
+    const int64_t worker = blockIdx.x;
+    const int64_t workers = gridDim.x;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&tfull[b], 1);
+            mbar_init(&tempty[b], EPI_THREADS / 32);
+            mbar_init(&cbar[b], 1);
+        }
+        mbar_init(drain, 1);
+        *abort_flag = 0u;
+        fence_barrier_init();
+    }
+    if (warp == 0 && lane == 0) {
+        prefetch_tensormap(&tmA);
+        prefetch_tensormap(&tmB);
+        prefetch_tensormap(&tmD);
+        if (p.beta != 0.0f) prefetch_tensormap(&tmC);
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+    grid_dependency_wait();
+    grid_launch_dependents();
+
+    const WaitCtl ctl{abort_flag, p.status, p.timeout_ns};
+
+    if (warp == 0) {
+        // ------------------------------------------------ TMA producer
+        if (lane == 0) {
+            uint32_t stage = 0, phase = 0;
+            int64_t issued = 0;
+            bool ok = true;
+            WorkItem w;
+            for (int64_t t = worker; ok && work_item(p.sched, t, kBN, w); t += workers) {
+                const int32_t m0 = w.m * BM;
+                const int32_t rb = w.n / 128; // B's first scale row block
+                // a 192-wide tile may reach into the next row block of B's scales
+                const bool two = kBN + (w.n % 128) > 128 && rb + 1 < p.sfb_rows;
+                const uint8_t *sfa = p.SA + static_cast<int64_t>(w.m) * p.sf_kc * SF_CHUNK;
+                const uint8_t *sfb = p.SB + static_cast<int64_t>(rb) * p.sf_kc * SF_CHUNK;
+                const uint32_t tx = L::A_BYTES + L::B_BYTES + SF_CHUNK * (two ? 3u : 2u);
+                for (int32_t kb = 0; kb < p.kb; ++kb) {
+                    if (!mbar_wait(&empty[stage], phase ^ 1u, ctl, kStatusTimeoutProducer)) {
+                        ok = false;
+                        break;
+                    }
+                    uint8_t *sf = smem + L::OFF_SF + stage * L::SF_BYTES;
+                    mbar_arrive_expect_tx(&full[stage], tx);
+                    tma_load_2d(&tmA, &full[stage], smem + L::OFF_A + stage * L::A_BYTES, kb * BK, m0);
+                    tma_load_2d(&tmB, &full[stage], smem + L::OFF_B + stage * L::B_BYTES, kb * BK, w.n);
+                    bulk_load_g2s(sf, sfa + static_cast<int64_t>(kb) * SF_CHUNK, SF_CHUNK, &full[stage]);
+                    bulk_load_g2s(sf + SF_CHUNK, sfb + static_cast<int64_t>(kb) * SF_CHUNK, SF_CHUNK, &full[stage]);
+                    if (two)
+                        bulk_load_g2s(sf + 2 * SF_CHUNK, sfb + (p.sf_kc + kb) * static_cast<int64_t>(SF_CHUNK), SF_CHUNK,
+                                      &full[stage]);
+                    ++issued;
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            if (!ok) {
+                // Let the loads already issued land before the CTA exits.
+                const int64_t pending = issued < STAGES ? issued : STAGES;
+                uint32_t s = stage, ph = phase;
+                for (int64_t i = 0; i < pending; ++i) {
+                    if (s == 0) {
+                        s = STAGES - 1;
+                        ph ^= 1u;
+                    } else {
+                        --s;
+                    }
+                    if (!mx_drain_wait(&full[s], ph, p.timeout_ns) && p.status) atomicOr(p.status, kStatusTimeoutDrain);
+                }
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------ scale copies and MMA issue
+        if (lane == 0) {
+            const uint64_t adesc0 = make_smem_desc_sw128(smem_addr(smem + L::OFF_A), 16, 1024);
+            const uint64_t bdesc0 = make_smem_desc_sw128(smem_addr(smem + L::OFF_B), 16, 1024);
+            // a scale chunk: 32 rows of 16 bytes, groups of 8 rows 128 bytes apart
+            const uint64_t sdesc0 = make_smem_desc_plain(smem_addr(smem + L::OFF_SF), 512, 128);
+            const uint32_t full_a = smem_addr(full), empty_a = smem_addr(empty);
+            uint32_t stage = 0, phase = 0;
+            uint32_t acc = 0, acc_phase = 0;
+            bool ok = true;
+            bool any = false;
+            WorkItem w;
+            for (int64_t t = worker; ok && work_item(p.sched, t, kBN, w); t += workers) {
+                // B's scale columns start (w.n % 128) / 32 TMEM columns into the copied chunks
+                const uint32_t sfb_skip = static_cast<uint32_t>((w.n % 128) / 32);
+                if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, ctl, kStatusTimeoutMma)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + acc * kBN;
+                for (int32_t kb = 0; kb < p.kb; ++kb) {
+                    if (!mbar_try_wait(full_a + stage * 8u, phase) &&
+                        !mbar_wait(&full[stage], phase, ctl, kStatusTimeoutMma)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t sfa_t = tmem_base + L::SF_COL0 + stage * SF_TMEM_STRIDE;
+                    const uint32_t sfb_t = sfa_t + 4;
+                    const uint64_t sd = sdesc0 + stage * (L::SF_BYTES >> 4);
+                    tc_cp_32x128b_x4(sfa_t, sd);
+                    tc_cp_32x128b_x4(sfb_t, sd + (SF_CHUNK >> 4));
+                    if constexpr (kBN > 128) tc_cp_32x128b_x4(sfb_t + 4, sd + (2 * SF_CHUNK >> 4));
+                    const uint64_t ad = adesc0 + stage * (L::A_BYTES >> 4);
+                    const uint64_t bd = bdesc0 + stage * (L::B_BYTES >> 4);
+#pragma unroll
+                    for (int kk = 0; kk < BK / 32; ++kk) {
+                        // K = 32 FP8 elements are 32 bytes: +2 in the descriptors' address field
+                        const uint32_t accumulate = (kb != 0 || kk != 0) ? 1u : 0u;
+                        tc_mma_mxf8(d_tmem, ad + kk * 2, bd + kk * 2, p.idesc | idesc_mx_sf_ids(kk, kk), sfa_t,
+                                    sfb_t + sfb_skip, accumulate);
+                    }
+                    any = true;
+                    tc_commit_addr(empty_a + stage * 8u);
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                tc_commit(&tfull[acc]);
+                if (++acc == 2) {
+                    acc = 0;
+                    acc_phase ^= 1u;
+                }
+            }
+            if (!ok && any) {
+                // Wait for every MMA and copy issued so far before TMEM is freed.
+                tc_commit(drain);
+                if (!mx_drain_wait(drain, 0, p.timeout_ns) && p.status) atomicOr(p.status, kStatusTimeoutDrain);
+            }
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------ epilogue (warps 2..5)
+        const uint32_t q = warp & 3u;        // TMEM lane quarter this warp may read
+        const uint32_t row = q * 32u + lane; // row of the tile held by this thread
+        const bool leader = threadIdx.x == 64;
+        const bool has_beta = p.beta != 0.0f;
+        uint8_t *epi = smem + L::OFF_EPI;
+        uint32_t acc = 0, acc_phase = 0;
+        uint32_t slot = 0;
+        uint32_t cphase = 0;
+        bool ok = true;
+        WorkItem w;
+        for (int64_t t = worker; ok && work_item(p.sched, t, kBN, w); t += workers) {
+            const int32_t m0 = w.m * BM;
+            int32_t rows_valid = p.M - m0;
+            rows_valid = rows_valid > BM ? BM : rows_valid;
+            int nchunks = (p.N - w.n + CHUNK - 1) / CHUNK;
+            if (nchunks > kBN / CHUNK) nchunks = kBN / CHUNK;
+            const bool got = mbar_wait(&tfull[acc], acc_phase, ctl, kStatusTimeoutEpilogue);
+            if (named_barrier_or(1, EPI_THREADS, !got)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const uint32_t acc_now = acc;
+            auto release = [&]() {
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&tempty[acc_now]);
+            };
+            for (int c = 0; c < nchunks; ++c) {
+                uint8_t *buf = epi + slot * EPI_BUF_BYTES;
+                const int32_t cb = w.n + c * CHUNK;
+                const bool chunk_tma = cb < p.n_tma;
+                const int tail_cell = (p.N > p.n_tma && cb <= p.n_tma && p.n_tma < cb + CHUNK)
+                                          ? (p.n_tma - cb) / (16 / (kOutF32 ? 4 : 2))
+                                          : -1;
+                const int32_t grow = m0 + static_cast<int32_t>(row);
+                const bool row_ok = static_cast<int32_t>(row) < rows_valid;
+                const int64_t crow = static_cast<int64_t>(grow) * p.ldc;
+                const int64_t drow = static_cast<int64_t>(grow) * p.ldd;
+                if (leader) bulk_wait_group_read<1>();
+                named_barrier_sync(1, EPI_THREADS);
+                if (has_beta && chunk_tma) {
+                    if (leader) {
+                        mbar_arrive_expect_tx(&cbar[slot], EPI_BUF_BYTES);
+                        tma_load_2d(&tmC, &cbar[slot], buf, cb, m0);
+                    }
+                    const bool gotc = mbar_wait(&cbar[slot], (cphase >> slot) & 1u, ctl, kStatusTimeoutEpilogue);
+                    if (named_barrier_or(1, EPI_THREADS, !gotc)) {
+                        ok = false;
+                        break;
+                    }
+                    cphase ^= 1u << slot;
+                }
+                const uint32_t taddr = tmem_base + acc * kBN + static_cast<uint32_t>(c * CHUNK) + ((q * 32u) << 16);
+                uint32_t r0[32];
+                uint32_t r1[32];
+                tmem_ld32(taddr, r0);
+                if (!kOutF32) tmem_ld32(taddr + 32, r1);
+                tc_wait_ld();
+                if (c == nchunks - 1) release();
+                uint8_t *rowp = buf + row * 128u;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    uint4 *cell = reinterpret_cast<uint4 *>(rowp + ((j ^ (row & 7u)) << 4));
+                    const bool tail = j == tail_cell;
+                    if constexpr (kOutF32) {
+                        float v[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) v[e] = p.alpha * __uint_as_float(r0[j * 4 + e]);
+                        if (tail) {
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                const int32_t col = cb + j * 4 + e;
+                                if (row_ok && col < p.N) {
+                                    if (has_beta) v[e] = fmaf(p.beta, static_cast<const float *>(p.C)[crow + col], v[e]);
+                                    static_cast<float *>(p.D)[drow + col] = v[e];
+                                }
+                            }
+                            continue;
+                        }
+                        if (has_beta) {
+                            const uint4 cv = *cell;
+                            v[0] = fmaf(p.beta, __uint_as_float(cv.x), v[0]);
+                            v[1] = fmaf(p.beta, __uint_as_float(cv.y), v[1]);
+                            v[2] = fmaf(p.beta, __uint_as_float(cv.z), v[2]);
+                            v[3] = fmaf(p.beta, __uint_as_float(cv.w), v[3]);
+                        }
+                        *cell = make_uint4(__float_as_uint(v[0]), __float_as_uint(v[1]), __float_as_uint(v[2]),
+                                           __float_as_uint(v[3]));
+                    } else {
+                        float v[8];
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) {
+                            const uint32_t bits = (j < 4) ? r0[j * 8 + e] : r1[(j - 4) * 8 + e];
+                            v[e] = p.alpha * __uint_as_float(bits);
+                        }
+                        if (tail) {
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) {
+                                const int32_t col = cb + j * 8 + e;
+                                if (row_ok && col < p.N) {
+                                    if (has_beta) {
+                                        const uint16_t cbits = static_cast<const uint16_t *>(p.C)[crow + col];
+                                        v[e] = fmaf(p.beta, __uint_as_float(static_cast<uint32_t>(cbits) << 16), v[e]);
+                                    }
+                                    static_cast<uint16_t *>(p.D)[drow + col] =
+                                        static_cast<uint16_t>(pack_bf16x2(v[e], 0.0f) & 0xFFFFu);
+                                }
+                            }
+                            continue;
+                        }
+                        if (has_beta) {
+                            const uint4 cv = *cell;
+                            const uint32_t cw[4] = {cv.x, cv.y, cv.z, cv.w};
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                v[2 * e] = fmaf(p.beta, bf16lo_to_f32(cw[e]), v[2 * e]);
+                                v[2 * e + 1] = fmaf(p.beta, bf16hi_to_f32(cw[e]), v[2 * e + 1]);
+                            }
+                        }
+                        *cell = make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]), pack_bf16x2(v[4], v[5]),
+                                           pack_bf16x2(v[6], v[7]));
+                    }
+                }
+                fence_proxy_async_smem();
+                named_barrier_sync(1, EPI_THREADS);
+                if (leader && chunk_tma) {
+                    tma_store_2d(&tmD, buf, cb, m0);
+                    bulk_commit_group();
+                }
+                slot ^= 1u;
+            }
+            if (!ok) break;
+            if (nchunks == 0) release();
+            if (++acc == 2) {
+                acc = 0;
+                acc_phase ^= 1u;
+            }
+        }
+        if (leader) bulk_wait_group_read<0>();
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, TMEM_COLS);
+    }
+}
+
+} // namespace mx
+} // namespace tpg

@@ -8,6 +8,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include "gemm_mx.cuh"
 #include "gemm_stream.cuh"
 #include "gemm_tiled.cuh"
 
@@ -73,6 +74,20 @@ struct StreamLaunch {
     const CUtensorMap *a, *b;
     const StreamParams *p;
 };
+
+struct MxLaunch {
+    int grid;
+    int tile_n; // 128 or 192
+    bool f32;
+    cudaStream_t stream;
+    const CUtensorMap *a, *b, *c, *d;
+    const MxParams *p;
+};
+
+// mx_inst.cu: the block-scaled (MX) kernel
+cudaError_t mx_launch(const MxLaunch &l);
+bool mx_set_limits();
+int mx_smem_bytes(int tile_n);
 
 // tiled_inst.cu, one definition per mode E (compiled with -DTPG_EPI=E).
 cudaError_t tiled_launch_e0(const TiledLaunch &l);

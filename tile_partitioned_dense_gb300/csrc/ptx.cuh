@@ -564,6 +564,55 @@ __host__ __device__ constexpr uint32_t make_idesc_bf16_f32(uint32_t m, uint32_t 
            (static_cast<uint32_t>(b_mn_major) << 16) | ((n >> 3) << 17) | ((m >> 4) << 24);
 }
 
+// ---------------------------------------------------------------- tcgen05, block-scaled (MX) operands
+// Shared-memory matrix descriptor without swizzling: rows of 16 bytes, groups
+// of 8 rows `sbo` bytes apart (the leading offset is not used by a matrix
+// one 16-byte column wide).
+__device__ __forceinline__ uint64_t make_smem_desc_plain(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);
+    d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
+    d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
+    d |= 1ull << 46;
+    return d;
+}
+
+// Copies a 32-row x 16-byte shared-memory matrix into TMEM: row i lands in
+// lane i, columns taddr .. taddr+3 (bytes 4j .. 4j+3 of the row in column
+// taddr + j), and the same 32 lanes are written in each of the four lane
+// quarters (warpx4). Asynchronous; ordered before later tcgen05.mma of the
+// same thread, and tracked by tcgen05.commit like an MMA.
+__device__ __forceinline__ void tc_cp_32x128b_x4(uint32_t taddr, uint64_t sdesc) {
+    asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+
+// D[tmem] (+)= (A scaled) * (B scaled), kind::mxf8f6f4 with one E8M0 scale per
+// 32 K elements (scale_vec::1X): FP8 A and B from shared-memory descriptors,
+// the scales of A's rows and B's columns in TMEM at sfa / sfb (the byte of
+// each 32-bit TMEM cell is chosen by the scale-factor IDs of idesc).
+__device__ __forceinline__ void tc_mma_mxf8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                            uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}\n" ::"r"(
+            d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+        : "memory");
+}
+
+// Instruction descriptor of a block-scaled MMA, kind::mxf8f6f4, both operands
+// K-major, E8M0 scales:
+//   bits 4-5 B scale-factor ID, bits 7-9 A format and 10-12 B format (0 E4M3,
+//   1 E5M2), bits 17-22 N >> 3, bit 23 scale type (1 = E8M0), bits 24-28
+//   M >> 4, bits 29-30 A scale-factor ID.
+__host__ __device__ constexpr uint32_t make_idesc_mxf8(uint32_t m, uint32_t n, uint32_t a_fmt, uint32_t b_fmt) {
+    return (a_fmt << 7) | (b_fmt << 10) | ((n >> 3) << 17) | (1u << 23) | ((m >> 4) << 24);
+}
+__host__ __device__ constexpr uint32_t idesc_mx_sf_ids(uint32_t a_id, uint32_t b_id) {
+    return (b_id << 4) | (a_id << 29);
+}
+
 // ---------------------------------------------------------------- conversions
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     // cvt.rn.bf16x2.f32 takes the high half first.

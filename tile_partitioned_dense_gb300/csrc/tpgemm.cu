@@ -429,6 +429,7 @@ bool set_smem_limits() {
     ok = tpg::tiled_set_limits_e4() && ok;
     ok = tpg::tiled_set_limits_e5() && ok;
     ok = tpg::stream_set_limits() && ok;
+    ok = tpg::mx_set_limits() && ok;
     return ok;
 }
 
@@ -992,6 +993,150 @@ int gemm_watchdog_selftest(tpgemm_handle *h, uint64_t timeout_ns, void *stream_p
     if (cudaMemcpy(&word, h->status, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess) return TPGEMM_ERR_CUDA;
     if (cudaMemset(h->status, 0, sizeof(uint64_t)) != cudaSuccess) return TPGEMM_ERR_CUDA;
     return (word & tpg::kStatusSelftest) ? TPGEMM_ERR_TIMEOUT : TPGEMM_OK;
+}
+
+} // extern "C"
+
+// ---------------------------------------------------------------------------
+// Block-scaled (MX) GEMM (gemm_run_mx).
+namespace {
+
+constexpr int64_t kMxBlock = 32;
+
+// Bytes of one operand's scales in the blocked layout: 512-byte chunks of 128
+// rows x 4 scale columns, ceil(rows / 128) x ceil(K / 128) of them.
+int64_t mx_scale_bytes(int64_t rows, int64_t K) {
+    return ((rows + 127) / 128) * ((K + 127) / 128) * 512;
+}
+
+// Tile width of the MX kernel: 192 columns (fewer MMAs per output, each long
+// enough to hide its issue cost) unless the output is at most 128 wide.
+int mx_tile_n(int64_t N) { return N > 128 ? 192 : 128; }
+
+} // namespace
+
+extern "C" {
+
+int64_t gemm_mx_scale_bytes(int64_t rows, int64_t K) {
+    if (rows < 0 || K < 0) return TPGEMM_ERR_INVALID_ARG;
+    return mx_scale_bytes(rows, K);
+}
+
+int gemm_mx_check_args(int64_t M, int64_t N, int64_t K, const void *A, int64_t lda, int a_format, const void *SA,
+                       const void *B, int64_t ldb, int b_format, const void *SB, const void *C, int64_t ldc,
+                       const void *D, int64_t ldd, float beta, int out_dtype) {
+    if (out_dtype != TPGEMM_OUT_BF16 && out_dtype != TPGEMM_OUT_F32) return TPGEMM_ERR_INVALID_ARG;
+    if ((a_format != TPGEMM_FP8_E4M3 && a_format != TPGEMM_FP8_E5M2) ||
+        (b_format != TPGEMM_FP8_E4M3 && b_format != TPGEMM_FP8_E5M2))
+        return TPGEMM_ERR_INVALID_ARG;
+    if (M < 0 || N < 0 || K < 0 || K % kMxBlock != 0) return TPGEMM_ERR_INVALID_ARG;
+    if (M > kMaxDim || N > kMaxDim || K > kMaxDim) return TPGEMM_ERR_TOO_LARGE;
+    if (M == 0 || N == 0) return TPGEMM_OK;
+    const int64_t elt = out_dtype == TPGEMM_OUT_F32 ? 4 : 2;
+    const bool use_c = beta != 0.0f;
+    if (!D || ldd < N) return TPGEMM_ERR_INVALID_ARG;
+    if (K > 0 && (!A || !B || !SA || !SB || lda < K || ldb < K)) return TPGEMM_ERR_INVALID_ARG;
+    if (use_c && (!C || ldc < N)) return TPGEMM_ERR_INVALID_ARG;
+    if (ldd > kMaxDim * 8 || (K > 0 && (lda > kMaxDim * 16 || ldb > kMaxDim * 16)) || (use_c && ldc > kMaxDim * 8))
+        return TPGEMM_ERR_TOO_LARGE;
+    if (!aligned16(D) || (M > 1 && (ldd * elt) % 16 != 0)) return TPGEMM_ERR_ALIGNMENT;
+    if (K > 0) {
+        if (!aligned16(A) || !aligned16(B) || !aligned16(SA) || !aligned16(SB)) return TPGEMM_ERR_ALIGNMENT;
+        if ((M > 1 && lda % 16 != 0) || (N > 1 && ldb % 16 != 0)) return TPGEMM_ERR_ALIGNMENT;
+    }
+    if (use_c && (!aligned16(C) || (M > 1 && (ldc * elt) % 16 != 0))) return TPGEMM_ERR_ALIGNMENT;
+    const Range rd = byte_range(D, M, N, ldd, elt);
+    if (K > 0) {
+        const Range rsa{reinterpret_cast<uintptr_t>(SA), reinterpret_cast<uintptr_t>(SA) +
+                                                             static_cast<uintptr_t>(mx_scale_bytes(M, K))};
+        const Range rsb{reinterpret_cast<uintptr_t>(SB), reinterpret_cast<uintptr_t>(SB) +
+                                                             static_cast<uintptr_t>(mx_scale_bytes(N, K))};
+        if (overlaps(rd, byte_range(A, M, K, lda, 1)) || overlaps(rd, byte_range(B, N, K, ldb, 1)) ||
+            overlaps(rd, rsa) || overlaps(rd, rsb))
+            return TPGEMM_ERR_OVERLAP;
+    }
+    if (use_c && !(C == D && ldc == ldd) && overlaps(rd, byte_range(C, M, N, ldc, elt))) return TPGEMM_ERR_OVERLAP;
+    return TPGEMM_OK;
+}
+
+int gemm_run_mx(tpgemm_handle *h, int64_t M, int64_t N, int64_t K, const void *A, int64_t lda, int a_format,
+                const void *SA, const void *B, int64_t ldb, int b_format, const void *SB, const void *C,
+                int64_t ldc, void *D, int64_t ldd, float alpha, float beta, int out_dtype, void *stream_ptr) {
+    if (!h) return TPGEMM_ERR_INVALID_ARG;
+    const int chk = gemm_mx_check_args(M, N, K, A, lda, a_format, SA, B, ldb, b_format, SB, C, ldc, D, ldd, beta,
+                                       out_dtype);
+    if (chk != TPGEMM_OK || M == 0 || N == 0) return chk;
+    const bool f32 = out_dtype == TPGEMM_OUT_F32;
+    const int64_t elt = f32 ? 4 : 2;
+    const bool use_c = beta != 0.0f;
+    DeviceGuard guard(h->device);
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+    if (K == 0) {
+        int64_t blocks = (M * N + 1023) / 1024;
+        if (blocks > 8LL * h->num_sms) blocks = 8LL * h->num_sms;
+        const int32_t m = static_cast<int32_t>(M), n = static_cast<int32_t>(N);
+        const tpg::EpiParams none{};
+        const void *c = use_c ? C : nullptr;
+        return f32 ? launch(tpg::epilogue_only_kernel<true, false>, static_cast<int>(blocks), 256, 0, 1, stream, m, n,
+                            beta, c, ldc, D, ldd, none)
+                   : launch(tpg::epilogue_only_kernel<false, false>, static_cast<int>(blocks), 256, 0, 1, stream, m,
+                            n, beta, c, ldc, D, ldd, none);
+    }
+    const int tile_n = mx_tile_n(N);
+    const uint32_t chunk = f32 ? 32u : 64u;
+    const int64_t cell = 16 / elt;
+    const int64_t n_tma = N / cell * cell;
+    const uint64_t map_n = static_cast<uint64_t>(n_tma > 0 ? n_tma : N);
+    const CUtensorMapDataType out_dt = f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    CUtensorMap tmA, tmB, tmC, tmD;
+    if (encode_2d(h, &tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, A, K, M, tma_stride(M, K, lda, 1), 128, 128) ||
+        encode_2d(h, &tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, B, K, N, tma_stride(N, K, ldb, 1), 128,
+                  static_cast<uint32_t>(tile_n)) ||
+        encode_2d(h, &tmD, out_dt, D, map_n, M, tma_stride(M, N, ldd, elt), chunk, 128) ||
+        encode_2d(h, &tmC, out_dt, use_c ? C : D, map_n, M,
+                  use_c ? tma_stride(M, N, ldc, elt) : tma_stride(M, N, ldd, elt), chunk, 128))
+        return TPGEMM_ERR_CUDA;
+    tpg::MxParams p{};
+    p.M = static_cast<int32_t>(M);
+    p.N = static_cast<int32_t>(N);
+    p.K = static_cast<int32_t>(K);
+    p.kb = static_cast<int32_t>((K + tpg::mx::BK - 1) / tpg::mx::BK);
+    const int64_t mt = (M + tpg::mx::BM - 1) / tpg::mx::BM;
+    const int64_t nt = (N + tile_n - 1) / tile_n;
+    p.sched = tpg::make_schedule(mt, nt, kGroupM, h->num_sms, 1, 0.5);
+    p.n_tma = static_cast<int32_t>(n_tma);
+    p.sfb_rows = static_cast<int32_t>((N + 127) / 128);
+    p.sf_kc = (K + 127) / 128;
+    p.SA = static_cast<const uint8_t *>(SA);
+    p.SB = static_cast<const uint8_t *>(SB);
+    p.idesc = tpg::make_idesc_mxf8(tpg::mx::BM, static_cast<uint32_t>(tile_n), static_cast<uint32_t>(a_format),
+                                   static_cast<uint32_t>(b_format));
+    p.alpha = alpha;
+    p.beta = beta;
+    p.C = use_c ? C : nullptr;
+    p.ldc = ldc;
+    p.D = D;
+    p.ldd = ldd;
+    p.status = h->status;
+    p.timeout_ns = h->timeout_ns;
+    const tpg::MxLaunch l{static_cast<int>(p.sched.workers), tile_n, f32, stream, &tmA, &tmB, &tmC, &tmD, &p};
+    return tpg::mx_launch(l) == cudaSuccess ? TPGEMM_OK : TPGEMM_ERR_CUDA;
+}
+
+int gemm_mx_query_plan(tpgemm_handle *h, int64_t M, int64_t N, int64_t K, int *tile_m, int *tile_n,
+                       int64_t *num_tiles, int *grid, int *smem_bytes) {
+    if (!h || M < 0 || N < 0 || K < 0) return TPGEMM_ERR_INVALID_ARG;
+    if (M > kMaxDim || N > kMaxDim || K > kMaxDim) return TPGEMM_ERR_TOO_LARGE;
+    const int tn = mx_tile_n(N);
+    const int64_t mt = (M + tpg::mx::BM - 1) / tpg::mx::BM;
+    const int64_t nt = (N + tn - 1) / tn;
+    const tpg::Schedule s = tpg::make_schedule(mt, nt, kGroupM, h->num_sms, 1, 0.5);
+    if (tile_m) *tile_m = tpg::mx::BM;
+    if (tile_n) *tile_n = tn;
+    if (num_tiles) *num_tiles = mt * nt;
+    if (grid) *grid = static_cast<int>(s.workers);
+    if (smem_bytes) *smem_bytes = tpg::mx_smem_bytes(tn);
+    return TPGEMM_OK;
 }
 
 } // extern "C"

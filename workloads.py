@@ -132,3 +132,77 @@ def sample_rows(M: int, count: int, tile: int = 128, seed: int = 1234):
     g = torch.Generator().manual_seed(seed)
     extra = torch.randperm(M, generator=g)[: max(0, count - len(fixed))].tolist()
     return sorted(fixed | set(extra))[:count] if len(fixed | set(extra)) > count else sorted(fixed | set(extra))
+
+
+# ------------------------------------------------------------------ block-scaled (MXFP8) inputs
+#
+# The MXFP8 workloads of the block-scaled GEMM (scaled_mm): the shapes of the
+# QKV projection and of the decode projection above, plus a medium square one,
+# the shape classes whose MXFP8 results "TorchInductor ganha suporte a GEMMs de
+# alta performance com CuteDSL" reports. Elements are drawn as N(0,1) (A) and
+# N(0,1) (B), cast to E4M3 by PyTorch's round-to-nearest-even conversion
+# (clamped to the format's largest finite value first); the E8M0 block scales
+# are drawn uniformly from 2^-3..2^3 for A and 2^-10..2^-6 for B (weights near
+# N(0, 0.02)). The integer variant draws elements from {-4..4} and scales from
+# {2^-1, 2^0, 2^1}, so that every partial sum is exact in fp32.
+
+@dataclasses.dataclass(frozen=True)
+class MxConfig:
+    name: str
+    M: int
+    N: int
+    K: int
+    seed: int
+    description: str
+
+    @property
+    def flops(self) -> int:
+        return 2 * self.M * self.N * self.K
+
+
+MX_CONFIGS = {
+    "mx_qkv": MxConfig("mx_qkv", 8192, 6144, 4096, 12, "MXFP8 QKV projection 8192x6144x4096, E4M3, bf16 output"),
+    "mx_medium": MxConfig("mx_medium", 2048, 4096, 4096, 13, "MXFP8 medium GEMM 2048x4096x4096, E4M3, bf16 output"),
+    "mx_decode": MxConfig("mx_decode", 16, 28672, 4096, 14,
+                          "MXFP8 decode projection 16x28672x4096, E4M3, bf16 output"),
+}
+
+_FP8_DTYPES = {0: torch.float8_e4m3fn, 1: torch.float8_e5m2}
+_FP8_MAX = {0: 448.0, 1: 57344.0}
+
+
+def _fp8_codes(x: torch.Tensor, fmt: int) -> torch.Tensor:
+    x = x.clamp(-_FP8_MAX[fmt], _FP8_MAX[fmt])
+    return x.to(_FP8_DTYPES[fmt]).view(torch.uint8)
+
+
+def make_mx_inputs(M: int, N: int, K: int, seed: int, integer: bool = False, fmt_a: int = 0, fmt_b: int = 0,
+                   lda: int | None = None, ldb: int | None = None):
+    """Seeded MXFP8 inputs as uint8 CPU tensors: A [M, K] and Bt [N, K] element
+    codes (B transposed), SA [M, K/32] and SB [N, K/32] E8M0 scale codes, all
+    row-major; lda / ldb > K give padded rows whose padding holds 0xFF."""
+    if K % 32:
+        raise ValueError("K must be a multiple of 32")
+    gen = torch.Generator(device="cpu")
+    gen.manual_seed(seed)
+    if integer:
+        a = torch.randint(-4, 5, (M, K), generator=gen).to(torch.float32)
+        b = torch.randint(-4, 5, (N, K), generator=gen).to(torch.float32)
+        sa = torch.randint(126, 129, (M, K // 32), generator=gen).to(torch.uint8)
+        sb = torch.randint(126, 129, (N, K // 32), generator=gen).to(torch.uint8)
+    else:
+        a = torch.randn((M, K), generator=gen)
+        b = torch.randn((N, K), generator=gen)
+        sa = torch.randint(124, 131, (M, K // 32), generator=gen).to(torch.uint8)
+        sb = torch.randint(117, 122, (N, K // 32), generator=gen).to(torch.uint8)
+    A = _fp8_codes(a, fmt_a)
+    Bt = _fp8_codes(b, fmt_b)
+
+    def padded(x, ld):
+        if ld is None or ld == x.shape[1]:
+            return x
+        base = torch.full((x.shape[0], ld), 0xFF, dtype=torch.uint8)
+        base[:, :x.shape[1]] = x
+        return base[:, :x.shape[1]]
+
+    return padded(A, lda), sa, padded(Bt, ldb), sb
