@@ -56,6 +56,7 @@ def parse_args():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="budget of the oracle sample")
     ap.add_argument("--no-sustained", action="store_true", help="skip the repetitions and the sustained regions")
+    ap.add_argument("--only-mx", action="store_true", help="of the per_config rows, measure the MXFP8 ones only")
     return ap.parse_args()
 
 
@@ -273,6 +274,128 @@ class MultiWorkload:
         return tpd.gemm_run_grouped(h, self.group_rows, self.N, self.K, s["A"].data_ptr(), self.K, s["B"].data_ptr(),
                                     self.N, self.K * self.N, None, self.N, s["D"].data_ptr(), self.N, 1.0, 0.0, 0,
                                     stream)
+
+
+class MxWorkload:
+    """A block-scaled (MXFP8) workload through gemm_run_mx: E4M3 A and B's
+    transpose, E8M0 scales in the blocked layout, bf16 D, rotating device copies."""
+
+    def __init__(self, cfg, torch, l2_bytes):
+        from workloads import make_mx_inputs, mx_blocked_scales
+        self.cfg = cfg
+        A, SA, Bt, SB = make_mx_inputs(cfg.M, cfg.N, cfg.K, seed=cfg.seed)
+        self.host = (A, SA, Bt, SB)
+        sa = torch.from_numpy(mx_blocked_scales(SA.numpy()))
+        sb = torch.from_numpy(mx_blocked_scales(SB.numpy()))
+        per_set = A.numel() + Bt.numel() + sa.numel() + sb.numel() + cfg.M * cfg.N * 2
+        self.nsets = max(2, -(-3 * l2_bytes // per_set) + 1)
+        self.sets = [{"A": A.cuda(), "B": Bt.cuda(), "SA": sa.cuda(), "SB": sb.cuda(),
+                      "D": torch.empty((cfg.M, cfg.N), dtype=torch.bfloat16, device="cuda")}
+                     for _ in range(self.nsets)]
+        self.b_bytes = Bt.numel() + sb.numel()
+
+    def run(self, tpd, h, i, stream):
+        s = self.sets[i % self.nsets]
+        c = self.cfg
+        return tpd.gemm_run_mx(h, c.M, c.N, c.K, s["A"].data_ptr(), c.K, tpd.FP8_E4M3, s["SA"].data_ptr(),
+                               s["B"].data_ptr(), c.K, tpd.FP8_E4M3, s["SB"].data_ptr(), None, c.N,
+                               s["D"].data_ptr(), c.N, 1.0, 0.0, tpd.OUT_BF16, stream)
+
+
+class TorchScaledMM:
+    """The same MXFP8 workload through torch._scaled_mm (NVIDIA's library
+    kernel), on the same buffers: a comparison row, not this library's path."""
+
+    def __init__(self, wl, torch):
+        self.wl = wl
+        self.torch = torch
+
+    def run(self, tpd, h, i, stream):
+        torch = self.torch
+        s = self.wl.sets[i % self.wl.nsets]
+        a = s["A"].view(torch.float8_e4m3fn)
+        b = s["B"].view(torch.float8_e4m3fn).t()
+        torch._scaled_mm(a, b, s["SA"].view(torch.float8_e8m0fnu), s["SB"].view(torch.float8_e8m0fnu),
+                         out_dtype=torch.bfloat16, out=s["D"])
+        return 0
+
+
+def mx_entries(torch, tpd, h, l2, peaks, local, barrier, rank, world, args):
+    """The MXFP8 rows: TFLOP/s against the FP8 tensor peak (the measured bf16
+    peak times the nominal FP8 : bf16 ratio of 2) for the QKV and medium
+    shapes; bytes of B and its scales per second against the HBM copy peak for
+    the decode shape. Each with torch._scaled_mm on the same buffers when
+    this torch offers MXFP8 scaled_mm, and the MX oracle's CPU baseline."""
+    from workloads import MX_CONFIGS
+    out = {}
+    fp8_peak = 2.0 * peaks["bf16_tflops"]
+    for name in ["mx_qkv", "mx_medium", "mx_decode"]:
+        cfg = MX_CONFIGS[name]
+        wl = MxWorkload(cfg, torch, l2)
+        plan = tpd.gemm_mx_query_plan(h, cfg.M, cfg.N, cfg.K)
+        steps = 400 if name != "mx_qkv" else 200
+        span, eager = time_launches(torch, tpd, h, wl, steps, 10, barrier)
+        ms = span / steps
+        decode = name == "mx_decode"
+        if decode:
+            v, unit, peak, bound = wl.b_bytes / (ms * 1e-3) / 1e9, "GB/s", peaks["hbm_gbs"], "hbm"
+        else:
+            v, unit, peak, bound = cfg.flops / (ms * 1e-3) / 1e12, "TFLOP/s", fp8_peak, "tensor"
+        e = {"value": round(v, 2), "unit": unit, "ms_per_step": round(ms, 5), "eager_ms_per_step": round(eager / steps, 5),
+             "steps": steps, "tflops": round(cfg.flops / (ms * 1e-3) / 1e12, 2),
+             "roofline": {"bound": bound, "achieved": round(v, 2), "peak": peak, "unit": unit,
+                          "frac": round(v / peak, 4), "kernel": "tpg::mx::gemm_mx_kernel",
+                          "peak_source": "2 x MEASURED_PEAKS.json bf16 burst (nominal FP8 : bf16 = 2)" if not decode
+                          else "MEASURED_PEAKS.json hbm_gbs"},
+             "config": {"workload": f"{name}: {cfg.description}", "M": cfg.M, "N": cfg.N, "K": cfg.K,
+                        "l2": f"inputs larger than L2: {wl.nsets} rotating device copies"},
+             "plan": plan}
+        if not args.no_sustained:
+            work = wl.b_bytes if decode else cfg.flops
+            times = time_reps(torch, tpd, h, wl, REPS)
+            med, best = statistics.median(times), min(times)
+            sc = 1e9 if decode else 1e12
+            e["reps"] = {"count": REPS, "median_ms": round(med, 5), "best_ms": round(best, 5),
+                         "median": round(work / (med * 1e-3) / sc, 2), "best": round(work / (best * 1e-3) / sc, 2),
+                         "unit": unit}
+            if name == "mx_qkv":
+                sms, n, secs, clocks = time_sustained(torch, tpd, h, wl, ms, SUSTAINED_SECONDS, local)
+                sv = work / (sms * 1e-3) / sc
+                e["sustained"] = {"value": round(sv, 2), "unit": unit, "ms_per_launch": round(sms, 5), "launches": n,
+                                  "seconds": round(secs, 3), "clocks": clocks}
+        try:
+            tspan, _ = time_launches(torch, tpd, h, TorchScaledMM(wl, torch), min(steps, 100), 3, barrier)
+            tms = tspan / min(steps, 100)
+            e["torch_scaled_mm"] = {"ms_per_step": round(tms, 5), "ours_over_torch": round(tms / ms, 3)}
+        except Exception as exc:  # this torch may not offer MXFP8 scaled_mm
+            e["torch_scaled_mm"] = {"unavailable": f"{type(exc).__name__}: {str(exc).splitlines()[0][:160]}"}
+            torch.cuda.synchronize()
+        if rank == 0 and world == 1 and not args.no_cpu_baseline:
+            e["cpu_baseline"] = mx_cpu_baseline(cfg, wl.host, 3.0)
+        out[name] = e
+        del wl
+        torch.cuda.empty_cache()
+    return out
+
+
+def mx_cpu_baseline(cfg, host, budget_s):
+    """The MX oracle as it stands, on a bounded row sample of the same workload."""
+    import oracle
+    from workloads import sample_rows
+    A, SA, Bt, SB = host
+    threads = len(os.sched_getaffinity(0))
+    probe = sample_rows(cfg.M, max(1, min(cfg.M, threads)), seed=7)
+    t0 = time.perf_counter()
+    oracle.mx_gemm_rows(A, SA, Bt, SB, None, 1.0, 0.0, 0, rows=probe, nthreads=threads)
+    per_row = (time.perf_counter() - t0) / len(probe)
+    nrows = int(max(len(probe), min(cfg.M, budget_s / max(per_row, 1e-9))))
+    rows = sample_rows(cfg.M, nrows, seed=11)
+    t0 = time.perf_counter()
+    oracle.mx_gemm_rows(A, SA, Bt, SB, None, 1.0, 0.0, 0, rows=rows, nthreads=threads)
+    dt = time.perf_counter() - t0
+    return {"value": 2.0 * len(rows) * cfg.N * cfg.K / dt / 1e12, "unit": "TFLOP/s", "cores": threads,
+            "kind": "oracle", "sample": f"{len(rows)} of {cfg.M} rows of {cfg.name}, {dt:.1f} s, fp64 C MX oracle, "
+                                        f"{threads} threads"}
 
 
 class FusedWorkload(Workload):
@@ -715,7 +838,8 @@ def run_ours(args):
     per_config = {}
     launches = args.steps
     torch_rows = {}
-    if not args.no_extra:
+    bf16_extra = not args.no_extra and not args.only_mx
+    if bf16_extra:
         if cfg.name != "tiny":
             torch_rows[cfg.name] = torch_matmul_entry(torch, tpd, h, wl, min(args.steps, 400), avg_max, barrier)
         for name in ["qkv", "mlp_down", "decode", "square", "tiny"]:
@@ -753,7 +877,7 @@ def run_ours(args):
             del w2
             torch.cuda.empty_cache()
 
-    if not args.no_extra:
+    if bf16_extra:
         # fused epilogue (bias + sigmoid + aux multiply) on the QKV shape, against the
         # plain GEMM followed by the same element-wise work in torch
         c2 = CONFIGS["qkv"]
@@ -791,6 +915,10 @@ def run_ours(args):
             torch.cuda.empty_cache()
 
     if not args.no_extra:
+        per_config.update(mx_entries(torch, tpd, h, l2, peaks, local, barrier, rank, world, args))
+        launches += 200 + 400 + 400
+
+    if bf16_extra:
         per_config["tp_overlay_chunks"] = chunk_tradeoff(torch, tpd, h)
         per_config["torch_matmul"] = {
             "note": "torch.matmul / addmm (cuBLAS) on the same shapes and rotating buffers, timed the same way; "

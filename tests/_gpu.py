@@ -17,6 +17,7 @@ import torch
 
 import oracle
 import tile_partitioned_dense_gb300 as tpd
+from workloads import mx_blocked_scales as mx_blocked  # noqa: F401 (re-exported for the tests)
 
 BF16_NAN = 0x7FC0
 DEV = torch.device("cuda:0")
@@ -131,16 +132,3 @@ def assert_within_tolerance(got: np.ndarray, want: np.ndarray, out_dtype: torch.
         assert not bad.any(), (f"{what}: {int(bad.sum())} elements outside 2^-7|O| + 1e-5 max|O|; "
                                f"worst excess {float((err - bound).max()):.3e}")
 
-
-def mx_blocked(S: np.ndarray) -> np.ndarray:
-    """Scale codes [R, K/32] (row-major) rearranged into gemm_run_mx's blocked
-    layout: 512-byte chunks of 128 rows x 4 scale columns in (row block, column
-    block) order, the scale of row r, column c of a chunk at byte
-    (r % 32) * 16 + (r / 32) * 4 + c. Padding rows and columns hold 127 (a
-    scale of 1). A permutation of bytes, nothing else."""
-    S = np.asarray(S, dtype=np.uint8)
-    R, nb = S.shape
-    rbs, kc = -(-R // 128), -(-nb // 4)
-    P = np.full((rbs * 128, kc * 4), 127, dtype=np.uint8)
-    P[:R, :nb] = S
-    return np.ascontiguousarray(P.reshape(rbs, 4, 32, kc, 4).transpose(0, 3, 2, 1, 4).reshape(-1))

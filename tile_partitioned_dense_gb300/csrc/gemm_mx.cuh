@@ -20,12 +20,18 @@
 //               both K-major with 128-byte swizzle, plus the K block's scale
 //               chunks: 512 bytes for A's 128 rows and one or two for B's rows,
 //               copied as they are from the caller's blocked scale layout.
+//   warp 6      scale copier: once a stage has landed, one lane copies its
+//               scale chunks into the stage's TMEM scale columns (tcgen05.cp,
+//               32 lanes x 16 bytes, repeated in all four lane quarters) and
+//               commits them to the stage's scales-ready barrier. Keeping the
+//               copies off the MMA thread leaves that thread four MMAs, one
+//               wait and one commit per stage: the thread's instruction issue
+//               is what paces the tensor pipe on these tiles.
 //   warp 1      allocates TMEM (two fp32 accumulators of kBN columns and, per
-//               ring stage, 4 scale columns for A and 8 for B); one lane copies
-//               each stage's scale chunks into TMEM (tcgen05.cp, 32 lanes x 16
-//               bytes, repeated in all four lane quarters) and issues the four
-//               K = 32 MMAs of the stage, scale byte j of each TMEM cell going
-//               with MMA j; tcgen05.commit frees the stage.
+//               ring stage, 4 scale columns for A and 8 for B); one lane issues
+//               the four K = 32 MMAs of a stage once its scales are in TMEM,
+//               scale byte j of each TMEM cell going with MMA j;
+//               tcgen05.commit frees the stage.
 //   warps 2-5   epilogue, as in the bf16 kernel: TMEM -> registers -> alpha,
 //               beta*C -> one rounding -> swizzled staging -> TMA store.
 //
@@ -69,7 +75,7 @@ namespace mx {
 
 constexpr int BM = 128;
 constexpr int BK = 128; // K elements (bytes) per stage: four MMAs of K = 32, four scale columns
-constexpr int THREADS = 192;
+constexpr int THREADS = 224; // warps 0-5 as the bf16 kernel, warp 6 copies scales
 constexpr int EPI_THREADS = 128;
 constexpr uint32_t SF_CHUNK = 512;
 constexpr uint32_t EPI_BUF_BYTES = BM * 128;
@@ -88,8 +94,8 @@ struct Layout {
     static constexpr uint32_t OFF_SF = OFF_B + STAGES * B_BYTES;
     static constexpr uint32_t OFF_EPI = OFF_SF + STAGES * SF_BYTES;
     static constexpr uint32_t OFF_BAR = OFF_EPI + 2 * EPI_BUF_BYTES;
-    // full, empty, tfull, tempty, c, drain
-    static constexpr uint32_t NUM_BARS = 2 * STAGES + 2 + 2 + 2 + 1;
+    // full, empty, scales ready, tfull, tempty, c, drain, scale-copy drain
+    static constexpr uint32_t NUM_BARS = 3 * STAGES + 2 + 2 + 2 + 2;
     static constexpr uint32_t OFF_MISC = OFF_BAR + NUM_BARS * 8;
     static constexpr uint32_t SMEM_BYTES = OFF_MISC + 16 + 1024;
     static constexpr uint32_t SF_COL0 = 2 * kBN; // first TMEM column of the scale region
@@ -122,10 +128,12 @@ __global__ void __launch_bounds__(THREADS, 1)
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::OFF_BAR);
     uint64_t *full = bars;
     uint64_t *empty = bars + STAGES;
-    uint64_t *tfull = bars + 2 * STAGES;
+    uint64_t *sfready = bars + 2 * STAGES;
+    uint64_t *tfull = bars + 3 * STAGES;
     uint64_t *tempty = tfull + 2;
     uint64_t *cbar = tempty + 2;
     uint64_t *drain = cbar + 2;
+    uint64_t *sfdrain = drain + 1;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::OFF_MISC);
     volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(smem + L::OFF_MISC + 4);
 
@@ -138,6 +146,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
+            mbar_init(&sfready[s], 1);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&tfull[b], 1);
@@ -145,6 +154,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             mbar_init(&cbar[b], 1);
         }
         mbar_init(drain, 1);
+        mbar_init(sfdrain, 1);
         *abort_flag = 0u;
         fence_barrier_init();
     }
@@ -224,9 +234,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (lane == 0) {
             const uint64_t adesc0 = make_smem_desc_sw128(smem_addr(smem + L::OFF_A), 16, 1024);
             const uint64_t bdesc0 = make_smem_desc_sw128(smem_addr(smem + L::OFF_B), 16, 1024);
-            // a scale chunk: 32 rows of 16 bytes, groups of 8 rows 128 bytes apart
-            const uint64_t sdesc0 = make_smem_desc_plain(smem_addr(smem + L::OFF_SF), 512, 128);
-            const uint32_t full_a = smem_addr(full), empty_a = smem_addr(empty);
+            const uint32_t ready_a = smem_addr(sfready), empty_a = smem_addr(empty);
             uint32_t stage = 0, phase = 0;
             uint32_t acc = 0, acc_phase = 0;
             bool ok = true;
@@ -242,18 +250,15 @@ __global__ void __launch_bounds__(THREADS, 1)
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + acc * kBN;
                 for (int32_t kb = 0; kb < p.kb; ++kb) {
-                    if (!mbar_try_wait(full_a + stage * 8u, phase) &&
-                        !mbar_wait(&full[stage], phase, ctl, kStatusTimeoutMma)) {
+                    // the stage's operands have landed and its scales are in TMEM
+                    if (!mbar_try_wait(ready_a + stage * 8u, phase) &&
+                        !mbar_wait(&sfready[stage], phase, ctl, kStatusTimeoutMma)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
                     const uint32_t sfa_t = tmem_base + L::SF_COL0 + stage * SF_TMEM_STRIDE;
                     const uint32_t sfb_t = sfa_t + 4;
-                    const uint64_t sd = sdesc0 + stage * (L::SF_BYTES >> 4);
-                    tc_cp_32x128b_x4(sfa_t, sd);
-                    tc_cp_32x128b_x4(sfb_t, sd + (SF_CHUNK >> 4));
-                    if constexpr (kBN > 128) tc_cp_32x128b_x4(sfb_t + 4, sd + (2 * SF_CHUNK >> 4));
                     const uint64_t ad = adesc0 + stage * (L::A_BYTES >> 4);
                     const uint64_t bd = bdesc0 + stage * (L::B_BYTES >> 4);
 #pragma unroll
@@ -278,9 +283,49 @@ __global__ void __launch_bounds__(THREADS, 1)
                 }
             }
             if (!ok && any) {
-                // Wait for every MMA and copy issued so far before TMEM is freed.
+                // Wait for every MMA issued so far before TMEM is freed.
                 tc_commit(drain);
                 if (!mx_drain_wait(drain, 0, p.timeout_ns) && p.status) atomicOr(p.status, kStatusTimeoutDrain);
+            }
+        }
+        __syncwarp();
+    } else if (warp == 6) {
+        // ------------------------------------------------ scale copies into TMEM
+        if (lane == 0) {
+            // a scale chunk: 32 rows of 16 bytes, groups of 8 rows 128 bytes apart
+            const uint64_t sdesc0 = make_smem_desc_plain(smem_addr(smem + L::OFF_SF), 512, 128);
+            const uint32_t full_a = smem_addr(full);
+            uint32_t stage = 0, phase = 0;
+            bool ok = true;
+            bool any = false;
+            WorkItem w;
+            for (int64_t t = worker; ok && work_item(p.sched, t, kBN, w); t += workers) {
+                for (int32_t kb = 0; kb < p.kb; ++kb) {
+                    // Stage s was last read by MMAs that completed before the producer
+                    // could refill it, so its TMEM scale columns are free once it is full.
+                    if (!mbar_try_wait(full_a + stage * 8u, phase) &&
+                        !mbar_wait(&full[stage], phase, ctl, kStatusTimeoutMma)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t sfa_t = tmem_base + L::SF_COL0 + stage * SF_TMEM_STRIDE;
+                    const uint64_t sd = sdesc0 + stage * (L::SF_BYTES >> 4);
+                    tc_cp_32x128b_x4(sfa_t, sd);
+                    tc_cp_32x128b_x4(sfa_t + 4, sd + (SF_CHUNK >> 4));
+                    if constexpr (kBN > 128) tc_cp_32x128b_x4(sfa_t + 8, sd + (2 * SF_CHUNK >> 4));
+                    tc_commit(&sfready[stage]);
+                    any = true;
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            if (!ok && any) {
+                // Wait for every copy issued so far before TMEM is freed.
+                tc_commit(sfdrain);
+                if (!mx_drain_wait(sfdrain, 0, p.timeout_ns) && p.status) atomicOr(p.status, kStatusTimeoutDrain);
             }
         }
         __syncwarp();

@@ -206,3 +206,18 @@ def make_mx_inputs(M: int, N: int, K: int, seed: int, integer: bool = False, fmt
         return base[:, :x.shape[1]]
 
     return padded(A, lda), sa, padded(Bt, ldb), sb
+
+
+def mx_blocked_scales(S) -> "np.ndarray":
+    """Scale codes [R, K/32] (row-major) rearranged into the blocked layout
+    gemm_run_mx takes: 512-byte chunks of 128 rows x 4 scale columns in (row
+    block, column block) order, the scale of row r, column c of a chunk at
+    byte (r % 32) * 16 + (r / 32) * 4 + c. Padding rows and columns hold 127
+    (a scale of 1). A permutation of bytes, nothing else."""
+    import numpy as np
+    S = np.asarray(S, dtype=np.uint8)
+    R, nb = S.shape
+    rbs, kc = -(-R // 128), -(-nb // 4)
+    P = np.full((rbs * 128, kc * 4), 127, dtype=np.uint8)
+    P[:R, :nb] = S
+    return np.ascontiguousarray(P.reshape(rbs, 4, 32, kc, 4).transpose(0, 3, 2, 1, 4).reshape(-1))
