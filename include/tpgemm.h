@@ -457,8 +457,9 @@ enum tpgemm_fp8_format {
  * K == 0 gives D = beta*C. D may equal C (same stride); any other overlap of
  * D with A, B, SA, SB or C is TPGEMM_ERR_OVERLAP. Errors as gemm_run, plus
  * TPGEMM_ERR_INVALID_ARG for a bad format or K not a multiple of 32.
- * Allocates nothing and never synchronises. Runs a persistent 1-CTA kernel of
- * 128 x 192 tiles (128 x 128 when N <= 128).
+ * Allocates nothing and never synchronises. Runs a persistent kernel of
+ * 256 x 192 tiles on CTA pairs when M and N are both above 128, else of
+ * 128 x 192 tiles on single CTAs (128 x 128 when N <= 128).
  */
 int gemm_run_mx(tpgemm_handle *h, int64_t M, int64_t N, int64_t K, const void *A, int64_t lda, int a_format,
                 const void *SA, const void *B, int64_t ldb, int b_format, const void *SB, const void *C,
@@ -475,10 +476,10 @@ int gemm_mx_check_args(int64_t M, int64_t N, int64_t K, const void *A, int64_t l
                        const void *D, int64_t ldd, float beta, int out_dtype);
 
 /* What gemm_run_mx launches for this shape: tile rows and columns, tiles, grid
- * (CTAs, one per SM at most) and dynamic shared memory per CTA. Any output
- * pointer may be NULL. */
-int gemm_mx_query_plan(tpgemm_handle *h, int64_t M, int64_t N, int64_t K, int *tile_m, int *tile_n,
-                       int64_t *num_tiles, int *grid, int *smem_bytes);
+ * (CTAs, one per SM at most), cluster size (2 for CTA pairs) and dynamic
+ * shared memory per CTA. Any output pointer may be NULL. */
+int gemm_mx_query_plan(tpgemm_handle *h, int64_t M, int64_t N, int64_t K, int out_dtype, int *tile_m, int *tile_n,
+                       int64_t *num_tiles, int *grid, int *cluster, int *smem_bytes);
 
 /*
  * Allocation-free GEMM (no counterpart in the paper; it serves callers that

@@ -72,13 +72,15 @@ def _want(A, SA, Bt, SB, C, alpha, beta, out_dtype, fmt_a=0, fmt_b=0, rows=None)
     return D
 
 
-# (M, N, K, lda, ldb): one 128 x 192 tile and a second one starting 64 rows
-# into B's second scale chunk; ragged everything with K = 96 (a partial K
+# (M, N, K, lda, ldb): one 256 x 192 pair tile and a second one starting 64
+# rows into B's second scale chunk; ragged everything with K = 96 (a partial K
 # block and a partial scale chunk) and N = 200 (the last tile's second scale
-# chunk does not exist); 128-column tiles (N <= 128); several tiles in both
-# directions with many K blocks.
+# chunk does not exist), on pairs whose second CTA owns rows past M; 128-column
+# tiles on single CTAs (N <= 128); single CTAs with 192-wide tiles (M <= 128);
+# several pair tiles in both directions with many K blocks; a pair whose
+# second CTA has one row.
 SHAPES = [(256, 384, 256, None, None), (300, 200, 96, 112, 96), (200, 100, 320, 336, 352),
-          (640, 1000, 1024, None, 1040), (129, 577, 160, 176, 160)]
+          (128, 577, 160, 176, 160), (640, 1000, 1024, None, 1040), (129, 577, 160, 176, 160)]
 
 
 def _ids(s):
@@ -183,8 +185,11 @@ def test_mx_argument_errors(h):
 
 
 def test_mx_plan(h):
+    sms = tpd.gemm_num_sms(h)
     p = tpd.gemm_mx_query_plan(h, 8192, 6144, 4096)
-    assert p["tile_m"] == 128 and p["tile_n"] == 192 and p["num_tiles"] == 64 * 32
-    assert p["grid"] == tpd.gemm_num_sms(h)
+    assert p["tile_m"] == 256 and p["tile_n"] == 192 and p["num_tiles"] == 32 * 32 and p["cluster"] == 2
+    assert p["grid"] % 2 == 0 and sms - 8 <= p["grid"] <= sms
+    p = tpd.gemm_mx_query_plan(h, 16, 28672, 4096)  # 128 rows or fewer: single CTAs
+    assert p["tile_m"] == 128 and p["tile_n"] == 192 and p["cluster"] == 1 and p["num_tiles"] == 150
     p = tpd.gemm_mx_query_plan(h, 256, 128, 4096)
-    assert p["tile_n"] == 128 and p["num_tiles"] == 2 and p["grid"] == 2
+    assert p["tile_m"] == 128 and p["tile_n"] == 128 and p["num_tiles"] == 2 and p["grid"] == 2

@@ -100,7 +100,7 @@ def load_library() -> ctypes.CDLL:
             "gemm_mx_scale_bytes": (i64, [i64, i64]),
             "gemm_mx_check_args": (i32, [i64, i64, i64, vp, i64, i32, vp, vp, i64, i32, vp, vp, i64, vp, i64, f32,
                                          i32]),
-            "gemm_mx_query_plan": (i32, [vp, i64, i64, i64, pi32, pi32, pi64, pi32, pi32]),
+            "gemm_mx_query_plan": (i32, [vp, i64, i64, i64, i32, pi32, pi32, pi64, pi32, pi32, pi32]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -269,15 +269,16 @@ def gemm_mx_check_args(M, N, K, A, lda, a_format, SA, B, ldb, b_format, SB, C, l
                                              beta, out_dtype)
 
 
-def gemm_mx_query_plan(h, M, N, K) -> dict:
-    tm, tn, grid, smem = (ctypes.c_int() for _ in range(4))
+def gemm_mx_query_plan(h, M, N, K, out_dtype=OUT_BF16) -> dict:
+    tm, tn, grid, cl, smem = (ctypes.c_int() for _ in range(5))
     tiles = ctypes.c_int64()
-    st = load_library().gemm_mx_query_plan(h, M, N, K, ctypes.byref(tm), ctypes.byref(tn), ctypes.byref(tiles),
-                                           ctypes.byref(grid), ctypes.byref(smem))
+    st = load_library().gemm_mx_query_plan(h, M, N, K, out_dtype, ctypes.byref(tm), ctypes.byref(tn),
+                                           ctypes.byref(tiles), ctypes.byref(grid), ctypes.byref(cl),
+                                           ctypes.byref(smem))
     if st != OK:
         raise TpgemmError(st, "gemm_mx_query_plan")
     return {"tile_m": tm.value, "tile_n": tn.value, "num_tiles": tiles.value, "grid": grid.value,
-            "smem_bytes": smem.value}
+            "cluster": cl.value, "smem_bytes": smem.value}
 
 
 # ------------------------------------------------------------------ torch convenience

@@ -11,29 +11,38 @@
 // scale_vec::1X reads one scale byte per row (of A) and per column (of B) from
 // TMEM for each K = 32 instruction.
 //
-// One CTA per SM owns 128 x kBN output tiles (kBN = 128 or 192) of the same
-// grouped-raster persistent schedule as the bf16 kernel; each tile has one
-// owner ("cuTile Rust explained", "Ownership crosses the launch boundary").
+// Two modes of one kernel template, on the grouped-raster persistent schedule
+// of the bf16 kernel; each tile has one owner ("cuTile Rust explained",
+// "Ownership crosses the launch boundary"):
+//   kPair = false  one CTA per SM owns 128 x kBN tiles (kBN = 128 or 192).
+//   kPair = true   the two CTAs of a cluster pair own a 256 x 192 tile through
+//                  tcgen05.mma.cta_group::2 (M = 256) issued by the even CTA;
+//                  each CTA stages its own 128 rows of A and its own 96 rows of
+//                  B's transpose, so per SM a stage is 28 KB of operands
+//                  instead of 40 KB: six stages fit where four did, and each SM
+//                  reads 30% fewer operand bytes from L2 per MMA.
 // Roles, connected by mbarriers:
 //   warp 0      TMA producer: per 128-wide K block, one A box (128 rows x 128
-//               bytes) and one B box (kBN rows of B's transpose x 128 bytes),
-//               both K-major with 128-byte swizzle, plus the K block's scale
-//               chunks: 512 bytes for A's 128 rows and one or two for B's rows,
-//               copied as they are from the caller's blocked scale layout.
-//   warp 6      scale copier: once a stage has landed, one lane copies its
-//               scale chunks into the stage's TMEM scale columns (tcgen05.cp,
-//               32 lanes x 16 bytes, repeated in all four lane quarters) and
-//               commits them to the stage's scales-ready barrier. Keeping the
-//               copies off the MMA thread leaves that thread four MMAs, one
-//               wait and one commit per stage: the thread's instruction issue
-//               is what paces the tensor pipe on these tiles.
+//               bytes) and one B box (kBN / CTAs rows of B's transpose x 128
+//               bytes), both K-major with 128-byte swizzle, plus the K block's
+//               scale chunks: 512 bytes for the CTA's 128 rows of A and one or
+//               two for the tile's rows of B (all of them, in both CTAs of a
+//               pair), copied as they are from the caller's blocked layout.
+//   warp 6      scale copier (even CTA): once a stage has landed, one lane
+//               copies its scale chunks into the stage's TMEM scale columns
+//               (tcgen05.cp, 32 lanes x 16 bytes, repeated in all four lane
+//               quarters, into both CTAs' TMEM in pair mode) and commits them
+//               to the stage's scales-ready barrier. Keeping the copies off the
+//               MMA thread leaves that thread four MMAs, one wait and one
+//               commit per stage.
 //   warp 1      allocates TMEM (two fp32 accumulators of kBN columns and, per
-//               ring stage, 4 scale columns for A and 8 for B); one lane issues
-//               the four K = 32 MMAs of a stage once its scales are in TMEM,
-//               scale byte j of each TMEM cell going with MMA j;
-//               tcgen05.commit frees the stage.
+//               ring stage, 4 scale columns for A and 8 for B); one lane (of
+//               the even CTA) issues the four K = 32 MMAs of a stage once its
+//               scales are in TMEM, scale byte j of each TMEM cell going with
+//               MMA j; tcgen05.commit frees the stage (in both CTAs).
 //   warps 2-5   epilogue, as in the bf16 kernel: TMEM -> registers -> alpha,
-//               beta*C -> one rounding -> swizzled staging -> TMA store.
+//               beta*C -> one rounding -> swizzled staging -> TMA store, each
+//               CTA its own 128 rows.
 //
 // The scale layout, per operand of R rows and K/32 scale columns: chunks of 128
 // rows x 4 scale columns (512 bytes), chunk (row block rb, column block cb)
@@ -55,12 +64,10 @@ namespace tpg {
 struct MxParams {
     int32_t M, N, K;
     int32_t kb;       // K blocks of 128
-    Schedule sched;   // 128 x kBN tiles, no column pieces
+    Schedule sched;   // tiles of 128 (CTA pairs: 256) x kBN, no column pieces
     int32_t n_tma;    // columns [0, n_tma) of C and D go through the tensor maps (see TiledParams)
     int32_t sfb_rows; // row blocks of 128 in B's scales: chunks past the last are not loaded
-    int64_t sf_kc;    // scale chunks per row block: ceil(K / 128)
-    const uint8_t *SA;
-    const uint8_t *SB;
+    int32_t sf_kc;    // scale chunks per row block: ceil(K / 128)
     uint32_t idesc;   // instruction descriptor without the scale-factor IDs
     float alpha, beta;
     const void *C;
@@ -73,7 +80,7 @@ struct MxParams {
 
 namespace mx {
 
-constexpr int BM = 128;
+constexpr int BM = 128; // rows per CTA
 constexpr int BK = 128; // K elements (bytes) per stage: four MMAs of K = 32, four scale columns
 constexpr int THREADS = 224; // warps 0-5 as the bf16 kernel, warp 6 copies scales
 constexpr int EPI_THREADS = 128;
@@ -82,12 +89,15 @@ constexpr uint32_t EPI_BUF_BYTES = BM * 128;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t SF_TMEM_STRIDE = 16; // TMEM columns per stage: A at +0 (4), B at +4 (8)
 
-template <int kBN>
+template <int kBN, bool kPair>
 struct Layout {
     static_assert(kBN == 128 || kBN == 192, "tile width");
-    static constexpr int STAGES = kBN == 192 ? 4 : 5;
+    static_assert(!kPair || kBN == 192, "CTA pairs run 192-wide tiles");
+    static constexpr int CL = kPair ? 2 : 1;
+    static constexpr int STAGES = kPair ? 6 : (kBN == 192 ? 4 : 5);
     static constexpr uint32_t A_BYTES = BM * BK;
-    static constexpr uint32_t B_BYTES = kBN * BK;
+    static constexpr uint32_t B_ROWS = kBN / CL; // rows of B's transpose this CTA stages
+    static constexpr uint32_t B_BYTES = B_ROWS * BK;
     static constexpr uint32_t SF_BYTES = 2048; // A chunk at 0, B chunks at 512 and 1024
     static constexpr uint32_t OFF_A = 0;
     static constexpr uint32_t OFF_B = OFF_A + STAGES * A_BYTES;
@@ -113,13 +123,22 @@ __device__ __forceinline__ bool mx_drain_wait(uint64_t *bar, uint32_t parity, ui
     return false;
 }
 
-template <bool kOutF32, int kBN>
+// Busy-waits `ns` nanoseconds (abort path only).
+__device__ __forceinline__ void mx_settle(uint64_t ns) {
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t i = 0; i < (1u << 26) && globaltimer_ns() - t0 < ns; ++i) {
+    }
+}
+
+template <bool kOutF32, int kBN, bool kPair>
 __global__ void __launch_bounds__(THREADS, 1)
     gemm_mx_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmSB,
                    const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmD,
                    const MxParams p) {
-    using L = Layout<kBN>;
+    using L = Layout<kBN, kPair>;
     constexpr int STAGES = L::STAGES;
+    constexpr int CL = L::CL;
     constexpr int CHUNK = kOutF32 ? 32 : 64; // output columns per 128-byte staging row
 
     extern __shared__ uint8_t smem_raw[];
@@ -139,8 +158,9 @@ __global__ void __launch_bounds__(THREADS, 1)
 
     const uint32_t warp = threadIdx.x / 32;
     const uint32_t lane = threadIdx.x % 32;
-    const int64_t worker = blockIdx.x;
-    const int64_t workers = gridDim.x;
+    const uint32_t rank = kPair ? cluster_ctarank() : 0u; // 0 = the even CTA, which issues copies and MMAs
+    const int64_t worker = static_cast<int64_t>(blockIdx.x) / CL;
+    const int64_t workers = static_cast<int64_t>(gridDim.x) / CL;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
@@ -150,7 +170,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&tfull[b], 1);
-            mbar_init(&tempty[b], EPI_THREADS / 32);
+            // every epilogue warp of the worker hands the accumulator back
+            mbar_init(&tempty[b], CL * EPI_THREADS / 32);
             mbar_init(&cbar[b], 1);
         }
         mbar_init(drain, 1);
@@ -161,15 +182,25 @@ __global__ void __launch_bounds__(THREADS, 1)
     if (warp == 0 && lane == 0) {
         prefetch_tensormap(&tmA);
         prefetch_tensormap(&tmB);
+        prefetch_tensormap(&tmSA);
+        prefetch_tensormap(&tmSB);
         prefetch_tensormap(&tmD);
         if (p.beta != 0.0f) prefetch_tensormap(&tmC);
     }
     if (warp == 1) {
-        tmem_alloc(tmem_slot, TMEM_COLS);
-        tmem_relinquish();
+        if constexpr (kPair) {
+            tmem_alloc_pair(tmem_slot, TMEM_COLS);
+            tmem_relinquish_pair();
+        } else {
+            tmem_alloc(tmem_slot, TMEM_COLS);
+            tmem_relinquish();
+        }
     }
     tc_fence_before();
-    __syncthreads();
+    if constexpr (kPair)
+        cluster_sync(); // both CTAs' barriers initialised and TMEM allocated
+    else
+        __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
     grid_dependency_wait();
@@ -178,34 +209,49 @@ __global__ void __launch_bounds__(THREADS, 1)
     const WaitCtl ctl{abort_flag, p.status, p.timeout_ns};
 
     if (warp == 0) {
-        // ------------------------------------------------ TMA producer
+        // ------------------------------------------------ TMA producer (both CTAs)
         if (lane == 0) {
+            // In pair mode both CTAs' loads complete on the even CTA's barrier.
+            const uint32_t full0 = kPair ? map_to_rank(smem_addr(full), 0) : 0u;
             uint32_t stage = 0, phase = 0;
             int64_t issued = 0;
             bool ok = true;
             WorkItem w;
             for (int64_t t = worker; ok && work_item(p.sched, t, kBN, w); t += workers) {
-                const int32_t m0 = w.m * BM;
+                const int32_t arow = w.m * CL + static_cast<int32_t>(rank); // this CTA's 128-row block of A
+                const int32_t m0 = arow * BM;
+                const int32_t n0 = w.n + static_cast<int32_t>(rank * L::B_ROWS);
                 const int32_t rb = w.n / 128; // B's first scale row block
                 // a 192-wide tile may reach into the next row block of B's scales
                 const bool two = kBN + (w.n % 128) > 128 && rb + 1 < p.sfb_rows;
-                const uint8_t *sfa = p.SA + static_cast<int64_t>(w.m) * p.sf_kc * SF_CHUNK;
-                const uint8_t *sfb = p.SB + static_cast<int64_t>(rb) * p.sf_kc * SF_CHUNK;
-                const uint32_t tx = L::A_BYTES + L::B_BYTES + SF_CHUNK * (two ? 3u : 2u);
+                const uint32_t tx = CL * (L::A_BYTES + L::B_BYTES + SF_CHUNK * (two ? 3u : 2u));
+                const int32_t ca = static_cast<int32_t>(arow * p.sf_kc);
+                const int32_t cb = static_cast<int32_t>(rb * p.sf_kc);
                 for (int32_t kb = 0; kb < p.kb; ++kb) {
                     if (!mbar_wait(&empty[stage], phase ^ 1u, ctl, kStatusTimeoutProducer)) {
                         ok = false;
                         break;
                     }
+                    uint8_t *adst = smem + L::OFF_A + stage * L::A_BYTES;
+                    uint8_t *bdst = smem + L::OFF_B + stage * L::B_BYTES;
                     uint8_t *sf = smem + L::OFF_SF + stage * L::SF_BYTES;
-                    mbar_arrive_expect_tx(&full[stage], tx);
-                    tma_load_2d(&tmA, &full[stage], smem + L::OFF_A + stage * L::A_BYTES, kb * BK, m0);
-                    tma_load_2d(&tmB, &full[stage], smem + L::OFF_B + stage * L::B_BYTES, kb * BK, w.n);
-                    bulk_load_g2s(sf, sfa + static_cast<int64_t>(kb) * SF_CHUNK, SF_CHUNK, &full[stage]);
-                    bulk_load_g2s(sf + SF_CHUNK, sfb + static_cast<int64_t>(kb) * SF_CHUNK, SF_CHUNK, &full[stage]);
-                    if (two)
-                        bulk_load_g2s(sf + 2 * SF_CHUNK, sfb + (p.sf_kc + kb) * static_cast<int64_t>(SF_CHUNK), SF_CHUNK,
-                                      &full[stage]);
+                    if constexpr (kPair) {
+                        if (rank == 0) mbar_arrive_expect_tx(&full[stage], tx);
+                        const uint32_t fb = full0 + stage * 8u;
+                        tma_load_2d_pair(&tmA, fb, adst, kb * BK, m0);
+                        tma_load_2d_pair(&tmB, fb, bdst, kb * BK, n0);
+                        tma_load_2d_pair(&tmSA, fb, sf, 0, ca + kb);
+                        tma_load_2d_pair(&tmSB, fb, sf + SF_CHUNK, 0, cb + kb);
+                        if (two) tma_load_2d_pair(&tmSB, fb, sf + 2 * SF_CHUNK, 0, cb + static_cast<int32_t>(p.sf_kc) + kb);
+                    } else {
+                        mbar_arrive_expect_tx(&full[stage], tx);
+                        tma_load_2d(&tmA, &full[stage], adst, kb * BK, m0);
+                        tma_load_2d(&tmB, &full[stage], bdst, kb * BK, n0);
+                        tma_load_2d(&tmSA, &full[stage], sf, 0, ca + kb);
+                        tma_load_2d(&tmSB, &full[stage], sf + SF_CHUNK, 0, cb + kb);
+                        if (two)
+                            tma_load_2d(&tmSB, &full[stage], sf + 2 * SF_CHUNK, 0, cb + static_cast<int32_t>(p.sf_kc) + kb);
+                    }
                     ++issued;
                     if (++stage == STAGES) {
                         stage = 0;
@@ -214,24 +260,30 @@ __global__ void __launch_bounds__(THREADS, 1)
                 }
             }
             if (!ok) {
-                // Let the loads already issued land before the CTA exits.
-                const int64_t pending = issued < STAGES ? issued : STAGES;
-                uint32_t s = stage, ph = phase;
-                for (int64_t i = 0; i < pending; ++i) {
-                    if (s == 0) {
-                        s = STAGES - 1;
-                        ph ^= 1u;
-                    } else {
-                        --s;
+                if (!kPair || rank == 0) {
+                    // Let the loads already issued land before the CTA exits.
+                    const int64_t pending = issued < STAGES ? issued : STAGES;
+                    uint32_t s = stage, ph = phase;
+                    for (int64_t i = 0; i < pending; ++i) {
+                        if (s == 0) {
+                            s = STAGES - 1;
+                            ph ^= 1u;
+                        } else {
+                            --s;
+                        }
+                        if (!mx_drain_wait(&full[s], ph, p.timeout_ns) && p.status)
+                            atomicOr(p.status, kStatusTimeoutDrain);
                     }
-                    if (!mx_drain_wait(&full[s], ph, p.timeout_ns) && p.status) atomicOr(p.status, kStatusTimeoutDrain);
                 }
+                // The odd CTA's loads complete on the even CTA's barriers, which it
+                // cannot wait on: give them time to land.
+                if (kPair) mx_settle(200000);
             }
         }
         __syncwarp();
     } else if (warp == 1) {
-        // ------------------------------------------------ scale copies and MMA issue
-        if (lane == 0) {
+        // ------------------------------------------------ MMA issue (even CTA only in pair mode)
+        if (lane == 0 && rank == 0) {
             const uint64_t adesc0 = make_smem_desc_sw128(smem_addr(smem + L::OFF_A), 16, 1024);
             const uint64_t bdesc0 = make_smem_desc_sw128(smem_addr(smem + L::OFF_B), 16, 1024);
             const uint32_t ready_a = smem_addr(sfready), empty_a = smem_addr(empty);
@@ -258,25 +310,34 @@ __global__ void __launch_bounds__(THREADS, 1)
                     }
                     tc_fence_after();
                     const uint32_t sfa_t = tmem_base + L::SF_COL0 + stage * SF_TMEM_STRIDE;
-                    const uint32_t sfb_t = sfa_t + 4;
+                    const uint32_t sfb_t = sfa_t + 4 + sfb_skip;
                     const uint64_t ad = adesc0 + stage * (L::A_BYTES >> 4);
                     const uint64_t bd = bdesc0 + stage * (L::B_BYTES >> 4);
 #pragma unroll
                     for (int kk = 0; kk < BK / 32; ++kk) {
                         // K = 32 FP8 elements are 32 bytes: +2 in the descriptors' address field
                         const uint32_t accumulate = (kb != 0 || kk != 0) ? 1u : 0u;
-                        tc_mma_mxf8(d_tmem, ad + kk * 2, bd + kk * 2, p.idesc | idesc_mx_sf_ids(kk, kk), sfa_t,
-                                    sfb_t + sfb_skip, accumulate);
+                        const uint32_t idesc = p.idesc | idesc_mx_sf_ids(kk, kk);
+                        if constexpr (kPair)
+                            tc_mma_mxf8_pair(d_tmem, ad + kk * 2, bd + kk * 2, idesc, sfa_t, sfb_t, accumulate);
+                        else
+                            tc_mma_mxf8(d_tmem, ad + kk * 2, bd + kk * 2, idesc, sfa_t, sfb_t, accumulate);
                     }
                     any = true;
-                    tc_commit_addr(empty_a + stage * 8u);
+                    if constexpr (kPair)
+                        tc_commit_pair_mc_addr(empty_a + stage * 8u, 0x3);
+                    else
+                        tc_commit_addr(empty_a + stage * 8u);
                     if (++stage == STAGES) {
                         stage = 0;
                         phase ^= 1u;
                     }
                 }
                 if (!ok) break;
-                tc_commit(&tfull[acc]);
+                if constexpr (kPair)
+                    tc_commit_pair_mc(&tfull[acc], 0x3);
+                else
+                    tc_commit(&tfull[acc]);
                 if (++acc == 2) {
                     acc = 0;
                     acc_phase ^= 1u;
@@ -284,14 +345,17 @@ __global__ void __launch_bounds__(THREADS, 1)
             }
             if (!ok && any) {
                 // Wait for every MMA issued so far before TMEM is freed.
-                tc_commit(drain);
+                if constexpr (kPair)
+                    tc_commit_pair_mc(drain, 0x1);
+                else
+                    tc_commit(drain);
                 if (!mx_drain_wait(drain, 0, p.timeout_ns) && p.status) atomicOr(p.status, kStatusTimeoutDrain);
             }
         }
         __syncwarp();
     } else if (warp == 6) {
-        // ------------------------------------------------ scale copies into TMEM
-        if (lane == 0) {
+        // ------------------------------------------------ scale copies into TMEM (even CTA)
+        if (lane == 0 && rank == 0) {
             // a scale chunk: 32 rows of 16 bytes, groups of 8 rows 128 bytes apart
             const uint64_t sdesc0 = make_smem_desc_plain(smem_addr(smem + L::OFF_SF), 512, 128);
             const uint32_t full_a = smem_addr(full);
@@ -311,10 +375,17 @@ __global__ void __launch_bounds__(THREADS, 1)
                     tc_fence_after();
                     const uint32_t sfa_t = tmem_base + L::SF_COL0 + stage * SF_TMEM_STRIDE;
                     const uint64_t sd = sdesc0 + stage * (L::SF_BYTES >> 4);
-                    tc_cp_32x128b_x4(sfa_t, sd);
-                    tc_cp_32x128b_x4(sfa_t + 4, sd + (SF_CHUNK >> 4));
-                    if constexpr (kBN > 128) tc_cp_32x128b_x4(sfa_t + 8, sd + (2 * SF_CHUNK >> 4));
-                    tc_commit(&sfready[stage]);
+                    if constexpr (kPair) {
+                        tc_cp_32x128b_x4_pair(sfa_t, sd);
+                        tc_cp_32x128b_x4_pair(sfa_t + 4, sd + (SF_CHUNK >> 4));
+                        tc_cp_32x128b_x4_pair(sfa_t + 8, sd + (2 * SF_CHUNK >> 4));
+                        tc_commit_pair_mc(&sfready[stage], 0x1);
+                    } else {
+                        tc_cp_32x128b_x4(sfa_t, sd);
+                        tc_cp_32x128b_x4(sfa_t + 4, sd + (SF_CHUNK >> 4));
+                        if constexpr (kBN > 128) tc_cp_32x128b_x4(sfa_t + 8, sd + (2 * SF_CHUNK >> 4));
+                        tc_commit(&sfready[stage]);
+                    }
                     any = true;
                     if (++stage == STAGES) {
                         stage = 0;
@@ -324,17 +395,21 @@ __global__ void __launch_bounds__(THREADS, 1)
             }
             if (!ok && any) {
                 // Wait for every copy issued so far before TMEM is freed.
-                tc_commit(sfdrain);
+                if constexpr (kPair)
+                    tc_commit_pair_mc(sfdrain, 0x1);
+                else
+                    tc_commit(sfdrain);
                 if (!mx_drain_wait(sfdrain, 0, p.timeout_ns) && p.status) atomicOr(p.status, kStatusTimeoutDrain);
             }
         }
         __syncwarp();
     } else {
-        // ------------------------------------------------ epilogue (warps 2..5)
+        // ------------------------------------------------ epilogue (warps 2..5, both CTAs)
         const uint32_t q = warp & 3u;        // TMEM lane quarter this warp may read
-        const uint32_t row = q * 32u + lane; // row of the tile held by this thread
+        const uint32_t row = q * 32u + lane; // row of the CTA's 128 rows held by this thread
         const bool leader = threadIdx.x == 64;
         const bool has_beta = p.beta != 0.0f;
+        const uint32_t tempty0 = kPair ? map_to_rank(smem_addr(tempty), 0) : 0u;
         uint8_t *epi = smem + L::OFF_EPI;
         uint32_t acc = 0, acc_phase = 0;
         uint32_t slot = 0;
@@ -342,9 +417,9 @@ __global__ void __launch_bounds__(THREADS, 1)
         bool ok = true;
         WorkItem w;
         for (int64_t t = worker; ok && work_item(p.sched, t, kBN, w); t += workers) {
-            const int32_t m0 = w.m * BM;
+            const int32_t m0 = (w.m * CL + static_cast<int32_t>(rank)) * BM;
             int32_t rows_valid = p.M - m0;
-            rows_valid = rows_valid > BM ? BM : rows_valid;
+            rows_valid = rows_valid < 0 ? 0 : (rows_valid > BM ? BM : rows_valid);
             int nchunks = (p.N - w.n + CHUNK - 1) / CHUNK;
             if (nchunks > kBN / CHUNK) nchunks = kBN / CHUNK;
             const bool got = mbar_wait(&tfull[acc], acc_phase, ctl, kStatusTimeoutEpilogue);
@@ -357,8 +432,14 @@ __global__ void __launch_bounds__(THREADS, 1)
             auto release = [&]() {
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&tempty[acc_now]);
+                if (lane == 0) {
+                    if constexpr (kPair)
+                        mbar_arrive_cluster(tempty0 + acc_now * 8u);
+                    else
+                        mbar_arrive(&tempty[acc_now]);
+                }
             };
+            if (nchunks == 0) release();
             for (int c = 0; c < nchunks; ++c) {
                 uint8_t *buf = epi + slot * EPI_BUF_BYTES;
                 const int32_t cb = w.n + c * CHUNK;
@@ -464,7 +545,6 @@ __global__ void __launch_bounds__(THREADS, 1)
                 slot ^= 1u;
             }
             if (!ok) break;
-            if (nchunks == 0) release();
             if (++acc == 2) {
                 acc = 0;
                 acc_phase ^= 1u;
@@ -474,10 +554,16 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
 
     tc_fence_before();
-    __syncthreads();
+    if constexpr (kPair)
+        cluster_sync(); // the peer may still arrive on this CTA's barriers until here
+    else
+        __syncthreads();
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc(tmem_base, TMEM_COLS);
+        if constexpr (kPair)
+            tmem_dealloc_pair(tmem_base, TMEM_COLS);
+        else
+            tmem_dealloc(tmem_base, TMEM_COLS);
     }
 }
 

@@ -76,18 +76,21 @@ struct StreamLaunch {
 };
 
 struct MxLaunch {
-    int grid;
+    int grid;   // CTAs (twice the pairs in pair mode)
     int tile_n; // 128 or 192
+    bool pair;  // 256 x 192 tiles on CTA pairs
     bool f32;
     cudaStream_t stream;
-    const CUtensorMap *a, *b, *c, *d;
+    const CUtensorMap *a, *b, *sa, *sb, *c, *d;
     const MxParams *p;
 };
 
 // mx_inst.cu: the block-scaled (MX) kernel
 cudaError_t mx_launch(const MxLaunch &l);
 bool mx_set_limits();
-int mx_smem_bytes(int tile_n);
+int mx_smem_bytes(int tile_n, bool pair);
+// co-resident CTA pairs of the MX kernel's pair mode, or -1
+int mx_pair_clusters(bool f32, int num_sms);
 
 // tiled_inst.cu, one definition per mode E (compiled with -DTPG_EPI=E).
 cudaError_t tiled_launch_e0(const TiledLaunch &l);

@@ -601,6 +601,25 @@ __device__ __forceinline__ void tc_mma_mxf8(uint32_t d_tmem, uint64_t a_desc, ui
         : "memory");
 }
 
+// CTA-pair forms, issued by one thread of the even CTA. The copy takes the
+// same shared-memory offset in both CTAs of the pair and writes each CTA's
+// chunk into that CTA's TMEM; the MMA computes the pair's 256-row tile, each
+// CTA's 128 rows with the A scales in its own TMEM and the B scales of all N
+// columns, which each CTA therefore holds in full.
+__device__ __forceinline__ void tc_cp_32x128b_x4_pair(uint32_t taddr, uint64_t sdesc) {
+    asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+__device__ __forceinline__ void tc_mma_mxf8_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                                 uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}\n" ::"r"(
+            d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+        : "memory");
+}
+
 // Instruction descriptor of a block-scaled MMA, kind::mxf8f6f4, both operands
 // K-major, E8M0 scales:
 //   bits 4-5 B scale-factor ID, bits 7-9 A format and 10-12 B format (0 E4M3,

@@ -88,6 +88,8 @@ struct tpgemm_handle {
     // co-resident clusters of 2 and 4 CTAs of the tiled kernel in 1-CTA mode (K
     // split), per [out f32][0: two, 1: four]
     std::atomic<int> ks_clusters[2][2] = {};
+    // co-resident CTA pairs of the MX kernel's pair mode, per [out f32]
+    std::atomic<int> mx_pairs[2] = {};
     // Caller-owned workspace (gemm_set_workspace), or null, and the tag of the
     // latest call that may use it.
     void *ws = nullptr;
@@ -1013,6 +1015,54 @@ int64_t mx_scale_bytes(int64_t rows, int64_t K) {
 // enough to hide its issue cost) unless the output is at most 128 wide.
 int mx_tile_n(int64_t N) { return N > 128 ? 192 : 128; }
 
+// CTA pairs (256 x 192 tiles) when there are more than 128 rows and columns:
+// per SM they stage and read 28 KB of operands per K block instead of 40 KB.
+bool mx_pair(int64_t M, int64_t N) { return M > 128 && N > 128; }
+
+int mx_pairs_for(tpgemm_handle *h, bool f32) {
+    std::atomic<int> &slot = h->mx_pairs[f32 ? 1 : 0];
+    const int cached = slot.load(std::memory_order_relaxed);
+    if (cached > 0) return cached;
+    const int n = tpg::mx_pair_clusters(f32, h->num_sms);
+    const int v = n > 0 ? n : h->num_sms / 2;
+    slot.store(v, std::memory_order_relaxed);
+    return v;
+}
+
+struct MxPlan {
+    int tile_m, tile_n;
+    bool pair;
+    int64_t mt, nt;
+    tpg::Schedule sched;
+    int grid;
+};
+
+MxPlan mx_plan(tpgemm_handle *h, int64_t M, int64_t N, bool f32) {
+    MxPlan pl;
+    pl.pair = mx_pair(M, N);
+    pl.tile_n = mx_tile_n(N);
+    pl.tile_m = tpg::mx::BM * (pl.pair ? 2 : 1);
+    pl.mt = (M + pl.tile_m - 1) / pl.tile_m;
+    pl.nt = (N + pl.tile_n - 1) / pl.tile_n;
+    const int64_t cap = pl.pair ? mx_pairs_for(h, f32) : h->num_sms;
+    pl.sched = tpg::make_schedule(pl.mt, pl.nt, pl.pair ? kGroupMPair : kGroupM, cap, 1, 0.5);
+    pl.grid = static_cast<int>(pl.sched.workers * (pl.pair ? 2 : 1));
+    return pl;
+}
+
+// The scales of one operand as a tensor of 512-byte chunks (128 x 32-bit
+// words each), one chunk per box.
+int encode_chunks(tpgemm_handle *h, CUtensorMap *map, const void *ptr, int64_t chunks) {
+    cuuint64_t dims[2] = {128, static_cast<cuuint64_t>(chunks)};
+    cuuint64_t strides[1] = {512};
+    cuuint32_t box[2] = {128, 1};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = h->encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<void *>(ptr), dims, strides, box, estr,
+                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? TPGEMM_OK : TPGEMM_ERR_CUDA;
+}
+
 } // namespace
 
 extern "C" {
@@ -1032,6 +1082,8 @@ int gemm_mx_check_args(int64_t M, int64_t N, int64_t K, const void *A, int64_t l
     if (M < 0 || N < 0 || K < 0 || K % kMxBlock != 0) return TPGEMM_ERR_INVALID_ARG;
     if (M > kMaxDim || N > kMaxDim || K > kMaxDim) return TPGEMM_ERR_TOO_LARGE;
     if (M == 0 || N == 0) return TPGEMM_OK;
+    // the kernel addresses scale chunks with 32-bit indices
+    if (mx_scale_bytes(M, K) / 512 > kMaxDim || mx_scale_bytes(N, K) / 512 > kMaxDim) return TPGEMM_ERR_TOO_LARGE;
     const int64_t elt = out_dtype == TPGEMM_OUT_F32 ? 4 : 2;
     const bool use_c = beta != 0.0f;
     if (!D || ldd < N) return TPGEMM_ERR_INVALID_ARG;
@@ -1082,16 +1134,19 @@ int gemm_run_mx(tpgemm_handle *h, int64_t M, int64_t N, int64_t K, const void *A
                    : launch(tpg::epilogue_only_kernel<false, false>, static_cast<int>(blocks), 256, 0, 1, stream, m,
                             n, beta, c, ldc, D, ldd, none);
     }
-    const int tile_n = mx_tile_n(N);
+    const MxPlan pl = mx_plan(h, M, N, f32);
+    const int tile_n = pl.tile_n;
     const uint32_t chunk = f32 ? 32u : 64u;
     const int64_t cell = 16 / elt;
     const int64_t n_tma = N / cell * cell;
     const uint64_t map_n = static_cast<uint64_t>(n_tma > 0 ? n_tma : N);
     const CUtensorMapDataType out_dt = f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-    CUtensorMap tmA, tmB, tmC, tmD;
+    CUtensorMap tmA, tmB, tmSA, tmSB, tmC, tmD;
     if (encode_2d(h, &tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, A, K, M, tma_stride(M, K, lda, 1), 128, 128) ||
         encode_2d(h, &tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, B, K, N, tma_stride(N, K, ldb, 1), 128,
-                  static_cast<uint32_t>(tile_n)) ||
+                  static_cast<uint32_t>(pl.pair ? tile_n / 2 : tile_n)) ||
+        encode_chunks(h, &tmSA, SA, mx_scale_bytes(M, K) / 512) ||
+        encode_chunks(h, &tmSB, SB, mx_scale_bytes(N, K) / 512) ||
         encode_2d(h, &tmD, out_dt, D, map_n, M, tma_stride(M, N, ldd, elt), chunk, 128) ||
         encode_2d(h, &tmC, out_dt, use_c ? C : D, map_n, M,
                   use_c ? tma_stride(M, N, ldc, elt) : tma_stride(M, N, ldd, elt), chunk, 128))
@@ -1101,16 +1156,12 @@ int gemm_run_mx(tpgemm_handle *h, int64_t M, int64_t N, int64_t K, const void *A
     p.N = static_cast<int32_t>(N);
     p.K = static_cast<int32_t>(K);
     p.kb = static_cast<int32_t>((K + tpg::mx::BK - 1) / tpg::mx::BK);
-    const int64_t mt = (M + tpg::mx::BM - 1) / tpg::mx::BM;
-    const int64_t nt = (N + tile_n - 1) / tile_n;
-    p.sched = tpg::make_schedule(mt, nt, kGroupM, h->num_sms, 1, 0.5);
+    p.sched = pl.sched;
     p.n_tma = static_cast<int32_t>(n_tma);
     p.sfb_rows = static_cast<int32_t>((N + 127) / 128);
-    p.sf_kc = (K + 127) / 128;
-    p.SA = static_cast<const uint8_t *>(SA);
-    p.SB = static_cast<const uint8_t *>(SB);
-    p.idesc = tpg::make_idesc_mxf8(tpg::mx::BM, static_cast<uint32_t>(tile_n), static_cast<uint32_t>(a_format),
-                                   static_cast<uint32_t>(b_format));
+    p.sf_kc = static_cast<int32_t>((K + 127) / 128);
+    p.idesc = tpg::make_idesc_mxf8(static_cast<uint32_t>(pl.tile_m), static_cast<uint32_t>(tile_n),
+                                   static_cast<uint32_t>(a_format), static_cast<uint32_t>(b_format));
     p.alpha = alpha;
     p.beta = beta;
     p.C = use_c ? C : nullptr;
@@ -1119,23 +1170,23 @@ int gemm_run_mx(tpgemm_handle *h, int64_t M, int64_t N, int64_t K, const void *A
     p.ldd = ldd;
     p.status = h->status;
     p.timeout_ns = h->timeout_ns;
-    const tpg::MxLaunch l{static_cast<int>(p.sched.workers), tile_n, f32, stream, &tmA, &tmB, &tmC, &tmD, &p};
+    const tpg::MxLaunch l{pl.grid, tile_n, pl.pair, f32, stream, &tmA, &tmB, &tmSA, &tmSB, &tmC, &tmD, &p};
     return tpg::mx_launch(l) == cudaSuccess ? TPGEMM_OK : TPGEMM_ERR_CUDA;
 }
 
-int gemm_mx_query_plan(tpgemm_handle *h, int64_t M, int64_t N, int64_t K, int *tile_m, int *tile_n,
-                       int64_t *num_tiles, int *grid, int *smem_bytes) {
+int gemm_mx_query_plan(tpgemm_handle *h, int64_t M, int64_t N, int64_t K, int out_dtype, int *tile_m, int *tile_n,
+                       int64_t *num_tiles, int *grid, int *cluster, int *smem_bytes) {
     if (!h || M < 0 || N < 0 || K < 0) return TPGEMM_ERR_INVALID_ARG;
+    if (out_dtype != TPGEMM_OUT_BF16 && out_dtype != TPGEMM_OUT_F32) return TPGEMM_ERR_INVALID_ARG;
     if (M > kMaxDim || N > kMaxDim || K > kMaxDim) return TPGEMM_ERR_TOO_LARGE;
-    const int tn = mx_tile_n(N);
-    const int64_t mt = (M + tpg::mx::BM - 1) / tpg::mx::BM;
-    const int64_t nt = (N + tn - 1) / tn;
-    const tpg::Schedule s = tpg::make_schedule(mt, nt, kGroupM, h->num_sms, 1, 0.5);
-    if (tile_m) *tile_m = tpg::mx::BM;
-    if (tile_n) *tile_n = tn;
-    if (num_tiles) *num_tiles = mt * nt;
-    if (grid) *grid = static_cast<int>(s.workers);
-    if (smem_bytes) *smem_bytes = tpg::mx_smem_bytes(tn);
+    DeviceGuard guard(h->device);
+    const MxPlan pl = mx_plan(h, M, N, out_dtype == TPGEMM_OUT_F32);
+    if (tile_m) *tile_m = pl.tile_m;
+    if (tile_n) *tile_n = pl.tile_n;
+    if (num_tiles) *num_tiles = pl.mt * pl.nt;
+    if (grid) *grid = pl.grid;
+    if (cluster) *cluster = pl.pair ? 2 : 1;
+    if (smem_bytes) *smem_bytes = tpg::mx_smem_bytes(pl.tile_n, pl.pair);
     return TPGEMM_OK;
 }
 
