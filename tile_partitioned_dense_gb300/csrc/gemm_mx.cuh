@@ -301,14 +301,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                 }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + acc * kBN;
-                for (int32_t kb = 0; kb < p.kb; ++kb) {
-                    // the stage's operands have landed and its scales are in TMEM
-                    if (!mbar_try_wait(ready_a + stage * 8u, phase) &&
-                        !mbar_wait(&sfready[stage], phase, ctl, kStatusTimeoutMma)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
+                // Issues the four MMAs of K block kb from the current stage and frees the stage.
+                auto issue = [&](int32_t kb) {
                     const uint32_t sfa_t = tmem_base + L::SF_COL0 + stage * SF_TMEM_STRIDE;
                     const uint32_t sfb_t = sfa_t + 4 + sfb_skip;
                     const uint64_t ad = adesc0 + stage * (L::A_BYTES >> 4);
@@ -332,6 +326,21 @@ __global__ void __launch_bounds__(THREADS, 1)
                         stage = 0;
                         phase ^= 1u;
                     }
+                };
+                for (int32_t kb = 0; kb < p.kb;) {
+                    // Wait until the stage's operands have landed and its scales are in
+                    // TMEM, and test the next stage in the same breath: when both are
+                    // ready, one wait serves two K blocks.
+                    const uint32_t nstage = stage + 1 == STAGES ? 0u : stage + 1;
+                    const uint32_t nphase = stage + 1 == STAGES ? phase ^ 1u : phase;
+                    const uint32_t st2 = mbar_try_wait_and_test(ready_a + stage * 8u, phase, ready_a + nstage * 8u, nphase);
+                    if (!(st2 & 1u) && !mbar_wait(&sfready[stage], phase, ctl, kStatusTimeoutMma)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    issue(kb++);
+                    if ((st2 & 2u) && kb < p.kb) issue(kb++);
                 }
                 if (!ok) break;
                 if constexpr (kPair)

@@ -426,13 +426,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                 }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + acc * BN;
-                for (int32_t kb = kr.lo; kb < kr.hi; ++kb) {
-                    if (!mbar_try_wait(full_a + stage * 8u, phase) &&
-                        !mbar_wait(&full[stage], phase, ctl, kStatusTimeoutMma)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
+                // Issues the MMAs of K block kb from the current stage and frees the stage.
+                auto issue = [&](int32_t kb) {
                     // The stage's descriptors: stage 0's plus the stage's byte offset >> 4
                     // in the start-address field.
                     const uint64_t ad = adesc0 + stage * (A_STAGE_BYTES >> 4);
@@ -456,6 +451,21 @@ __global__ void __launch_bounds__(THREADS, 1)
                         stage = 0;
                         phase ^= 1u;
                     }
+                };
+                for (int32_t kb = kr.lo; kb < kr.hi;) {
+                    // Wait for this stage and, in the same breath, test the next one: when
+                    // both have landed, one wait serves two K blocks (the issuing thread's
+                    // instructions per K block are what pace the tensor pipe).
+                    const uint32_t nstage = stage + 1 == STAGES ? 0u : stage + 1;
+                    const uint32_t nphase = stage + 1 == STAGES ? phase ^ 1u : phase;
+                    const uint32_t st2 = mbar_try_wait_and_test(full_a + stage * 8u, phase, full_a + nstage * 8u, nphase);
+                    if (!(st2 & 1u) && !mbar_wait(&full[stage], phase, ctl, kStatusTimeoutMma)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    issue(kb++);
+                    if ((st2 & 2u) && kb < kr.hi) issue(kb++);
                 }
                 if (!ok) break;
                 if constexpr (kPair)

@@ -89,6 +89,23 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t addr, uint32_t parity) {
     return ok != 0;
 }
 
+// Two ring stages at once: a (possibly blocking) wait on the first barrier and
+// a non-blocking test of the second, issued together so that their latencies
+// overlap. Bit 0 of the result: the first phase is complete; bit 1: the second.
+__device__ __forceinline__ uint32_t mbar_try_wait_and_test(uint32_t a1, uint32_t p1, uint32_t a2, uint32_t p2) {
+    uint32_t r1, r2;
+    asm volatile(
+        "{\n\t.reg .pred q1, q2;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 q1, [%2], %3;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 q2, [%4], %5;\n\t"
+        "selp.u32 %0, 1, 0, q1;\n\t"
+        "selp.u32 %1, 2, 0, q2;\n\t}\n"
+        : "=r"(r1), "=r"(r2)
+        : "r"(a1), "r"(p1), "r"(a2), "r"(p2)
+        : "memory");
+    return r1 | r2;
+}
+
 // Cluster-scope acquire form, for barriers that peers arrive on remotely.
 __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t addr, uint32_t parity) {
     uint32_t ok;
