@@ -453,19 +453,25 @@ __global__ void __launch_bounds__(THREADS, 1)
                     }
                 };
                 for (int32_t kb = kr.lo; kb < kr.hi;) {
-                    // Wait for this stage and, in the same breath, test the next one: when
-                    // both have landed, one wait serves two K blocks (the issuing thread's
-                    // instructions per K block are what pace the tensor pipe).
-                    const uint32_t nstage = stage + 1 == STAGES ? 0u : stage + 1;
-                    const uint32_t nphase = stage + 1 == STAGES ? phase ^ 1u : phase;
-                    const uint32_t st2 = mbar_try_wait_and_test(full_a + stage * 8u, phase, full_a + nstage * 8u, nphase);
-                    if (!(st2 & 1u) && !mbar_wait(&full[stage], phase, ctl, kStatusTimeoutMma)) {
+                    // Wait for this stage and, in the same breath, test the next two: when
+                    // they have landed, one wait serves up to three K blocks (the issuing
+                    // thread's instructions per K block are what pace the tensor pipe).
+                    const uint32_t s1 = stage + 1 == STAGES ? 0u : stage + 1;
+                    const uint32_t p1 = stage + 1 == STAGES ? phase ^ 1u : phase;
+                    const uint32_t s2 = s1 + 1 == STAGES ? 0u : s1 + 1;
+                    const uint32_t p2 = s1 + 1 == STAGES ? p1 ^ 1u : p1;
+                    const uint32_t st = mbar_try_wait_and_test2(full_a + stage * 8u, phase, full_a + s1 * 8u, p1,
+                                                                full_a + s2 * 8u, p2);
+                    if (!(st & 1u) && !mbar_wait(&full[stage], phase, ctl, kStatusTimeoutMma)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
                     issue(kb++);
-                    if ((st2 & 2u) && kb < kr.hi) issue(kb++);
+                    if ((st & 2u) && kb < kr.hi) {
+                        issue(kb++);
+                        if ((st & 4u) && kb < kr.hi) issue(kb++);
+                    }
                 }
                 if (!ok) break;
                 if constexpr (kPair)

@@ -106,6 +106,25 @@ __device__ __forceinline__ uint32_t mbar_try_wait_and_test(uint32_t a1, uint32_t
     return r1 | r2;
 }
 
+// The same over three stages: bit 0 the first (waited on), bits 1 and 2 the
+// next two (tested).
+__device__ __forceinline__ uint32_t mbar_try_wait_and_test2(uint32_t a1, uint32_t p1, uint32_t a2, uint32_t p2,
+                                                            uint32_t a3, uint32_t p3) {
+    uint32_t r1, r2, r3;
+    asm volatile(
+        "{\n\t.reg .pred q1, q2, q3;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 q1, [%3], %4;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 q2, [%5], %6;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 q3, [%7], %8;\n\t"
+        "selp.u32 %0, 1, 0, q1;\n\t"
+        "selp.u32 %1, 2, 0, q2;\n\t"
+        "selp.u32 %2, 4, 0, q3;\n\t}\n"
+        : "=r"(r1), "=r"(r2), "=r"(r3)
+        : "r"(a1), "r"(p1), "r"(a2), "r"(p2), "r"(a3), "r"(p3)
+        : "memory");
+    return r1 | r2 | r3;
+}
+
 // Cluster-scope acquire form, for barriers that peers arrive on remotely.
 __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t addr, uint32_t parity) {
     uint32_t ok;
