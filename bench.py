@@ -361,8 +361,10 @@ def mx_entries(torch, tpd, h, l2, peaks, local, barrier, rank, world, args):
             if name == "mx_qkv":
                 sms, n, secs, clocks = time_sustained(torch, tpd, h, wl, ms, SUSTAINED_SECONDS, local)
                 sv = work / (sms * 1e-3) / sc
+                speak = 2.0 * peaks["bf16_tflops_sustained"]
                 e["sustained"] = {"value": round(sv, 2), "unit": unit, "ms_per_launch": round(sms, 5), "launches": n,
-                                  "seconds": round(secs, 3), "clocks": clocks}
+                                  "seconds": round(secs, 3), "peak": speak, "frac": round(sv / speak, 4),
+                                  "peak_key": "2 x bf16_tflops_sustained", "clocks": clocks}
         try:
             tspan, _ = time_launches(torch, tpd, h, TorchScaledMM(wl, torch), min(steps, 100), 3, barrier)
             tms = tspan / min(steps, 100)
