@@ -78,9 +78,12 @@ def _want(A, SA, Bt, SB, C, alpha, beta, out_dtype, fmt_a=0, fmt_b=0, rows=None)
 # chunk does not exist), on pairs whose second CTA owns rows past M; 128-column
 # tiles on single CTAs (N <= 128); single CTAs with 192-wide tiles (M <= 128);
 # several pair tiles in both directions with many K blocks; a pair whose
-# second CTA has one row.
+# second CTA has one row; M <= 32 on 32-row A boxes, M <= 64 on 64-row ones, and
+# M <= 64 with N <= 128 on the 128-wide tiles that keep 128-row boxes.
 SHAPES = [(256, 384, 256, None, None), (300, 200, 96, 112, 96), (200, 100, 320, 336, 352),
-          (128, 577, 160, 176, 160), (640, 1000, 1024, None, 1040), (129, 577, 160, 176, 160)]
+          (128, 577, 160, 176, 160), (640, 1000, 1024, None, 1040), (129, 577, 160, 176, 160),
+          (16, 1000, 512, None, None), (33, 600, 192, None, None), (64, 577, 160, 176, 160),
+          (40, 100, 256, None, None)]
 
 
 def _ids(s):
@@ -191,5 +194,10 @@ def test_mx_plan(h):
     assert p["grid"] % 2 == 0 and sms - 8 <= p["grid"] <= sms
     p = tpd.gemm_mx_query_plan(h, 16, 28672, 4096)  # 128 rows or fewer: single CTAs
     assert p["tile_m"] == 128 and p["tile_n"] == 192 and p["cluster"] == 1 and p["num_tiles"] == 150
+    sizes = {p["smem_bytes"]}
+    for m in (64, 100):  # 64-row A boxes, then 128-row ones: each its own ring
+        p = tpd.gemm_mx_query_plan(h, m, 28672, 4096)
+        assert p["tile_m"] == 128 and p["cluster"] == 1 and p["smem_bytes"] not in sizes
+        sizes.add(p["smem_bytes"])
     p = tpd.gemm_mx_query_plan(h, 256, 128, 4096)
     assert p["tile_m"] == 128 and p["tile_n"] == 128 and p["num_tiles"] == 2 and p["grid"] == 2

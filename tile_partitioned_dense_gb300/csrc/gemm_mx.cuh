@@ -89,18 +89,27 @@ constexpr uint32_t EPI_BUF_BYTES = BM * 128;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t SF_TMEM_STRIDE = 16; // TMEM columns per stage: A at +0 (4), B at +4 (8)
 
-template <int kBN, bool kPair>
+// kARows < 128 (1-CTA, M <= kARows): A's TMA box is kARows rows (64 or 32),
+// so a stage holds 8 or 4 KB of A instead of 16 and the ring one or two
+// stages more; the MMA still reads 128 rows, and the rows past the box (the
+// next stages' bytes) only reach accumulator rows that are never stored.
+template <int kBN, bool kPair, int kARows = 128>
 struct Layout {
     static_assert(kBN == 128 || kBN == 192, "tile width");
     static_assert(!kPair || kBN == 192, "CTA pairs run 192-wide tiles");
+    static_assert(kARows == 128 || (!kPair && kBN == 192 && (kARows == 64 || kARows == 32)),
+                  "the small-M rings are 1-CTA, 192 wide");
     static constexpr int CL = kPair ? 2 : 1;
-    static constexpr int STAGES = kPair ? 6 : (kBN == 192 ? 4 : 5);
-    static constexpr uint32_t A_BYTES = BM * BK;
+    static constexpr int STAGES = kPair ? 6 : (kARows == 32 ? 6 : (kARows == 64 ? 5 : (kBN == 192 ? 4 : 5)));
+    static constexpr uint32_t A_ROWS = kARows; // rows of A's box
+    static constexpr uint32_t A_BYTES = A_ROWS * BK;
     static constexpr uint32_t B_ROWS = kBN / CL; // rows of B's transpose this CTA stages
     static constexpr uint32_t B_BYTES = B_ROWS * BK;
     static constexpr uint32_t SF_BYTES = 2048; // A chunk at 0, B chunks at 512 and 1024
     static constexpr uint32_t OFF_A = 0;
     static constexpr uint32_t OFF_B = OFF_A + STAGES * A_BYTES;
+    static_assert(OFF_A + (STAGES - 1) * A_BYTES + BM * BK <= OFF_B + STAGES * (kBN / CL) * BK,
+                  "the MMA's 128-row reads of A stay inside the operand ring");
     static constexpr uint32_t OFF_SF = OFF_B + STAGES * B_BYTES;
     static constexpr uint32_t OFF_EPI = OFF_SF + STAGES * SF_BYTES;
     static constexpr uint32_t OFF_BAR = OFF_EPI + 2 * EPI_BUF_BYTES;
@@ -130,13 +139,13 @@ __device__ __forceinline__ void mx_settle(uint64_t ns) {
     }
 }
 
-template <bool kOutF32, int kBN, bool kPair>
+template <bool kOutF32, int kBN, bool kPair, int kARows = 128>
 __global__ void __launch_bounds__(THREADS, 1)
     gemm_mx_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmSB,
                    const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmD,
                    const MxParams p) {
-    using L = Layout<kBN, kPair>;
+    using L = Layout<kBN, kPair, kARows>;
     constexpr int STAGES = L::STAGES;
     constexpr int CL = L::CL;
     constexpr int CHUNK = kOutF32 ? 32 : 64; // output columns per 128-byte staging row

@@ -78,7 +78,8 @@ struct StreamLaunch {
 struct MxLaunch {
     int grid;   // CTAs (twice the pairs in pair mode)
     int tile_n; // 128 or 192
-    bool pair;  // 256 x 192 tiles on CTA pairs
+    bool pair;    // 256 x 192 tiles on CTA pairs
+    int a_rows;   // rows of A's box: 128, or 64 / 32 for M <= 64 / 32 on 1-CTA 192-wide tiles
     bool f32;
     cudaStream_t stream;
     const CUtensorMap *a, *b, *sa, *sb, *c, *d;
@@ -88,7 +89,7 @@ struct MxLaunch {
 // mx_inst.cu: the block-scaled (MX) kernel
 cudaError_t mx_launch(const MxLaunch &l);
 bool mx_set_limits();
-int mx_smem_bytes(int tile_n, bool pair);
+int mx_smem_bytes(int tile_n, bool pair, int a_rows);
 // co-resident CTA pairs of the MX kernel's pair mode, or -1
 int mx_pair_clusters(bool f32, int num_sms);
 

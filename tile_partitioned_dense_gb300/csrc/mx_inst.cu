@@ -6,16 +6,17 @@
 namespace tpg {
 
 namespace {
-template <bool kOutF32, int kBN, bool kPair>
+template <bool kOutF32, int kBN, bool kPair, int kARows = 128>
 bool set_limit() {
-    return cudaFuncSetAttribute(mx::gemm_mx_kernel<kOutF32, kBN, kPair>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                static_cast<int>(mx::Layout<kBN, kPair>::SMEM_BYTES)) == cudaSuccess;
+    return cudaFuncSetAttribute(mx::gemm_mx_kernel<kOutF32, kBN, kPair, kARows>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                static_cast<int>(mx::Layout<kBN, kPair, kARows>::SMEM_BYTES)) == cudaSuccess;
 }
-template <bool kOutF32, int kBN, bool kPair>
+template <bool kOutF32, int kBN, bool kPair, int kARows = 128>
 cudaError_t launch_one(const MxLaunch &l) {
-    return launch_ex(mx::gemm_mx_kernel<kOutF32, kBN, kPair>, l.grid, mx::THREADS,
-                     static_cast<int>(mx::Layout<kBN, kPair>::SMEM_BYTES), kPair ? 2 : 1, true, l.stream, *l.a, *l.b,
-                     *l.sa, *l.sb, *l.c, *l.d, *l.p);
+    return launch_ex(mx::gemm_mx_kernel<kOutF32, kBN, kPair, kARows>, l.grid, mx::THREADS,
+                     static_cast<int>(mx::Layout<kBN, kPair, kARows>::SMEM_BYTES), kPair ? 2 : 1, true, l.stream,
+                     *l.a, *l.b, *l.sa, *l.sb, *l.c, *l.d, *l.p);
 }
 } // namespace
 
@@ -24,6 +25,10 @@ cudaError_t mx_launch(const MxLaunch &l) {
         if (l.tile_n != 192 || l.grid % 2 != 0) return cudaErrorInvalidValue;
         return l.f32 ? launch_one<true, 192, true>(l) : launch_one<false, 192, true>(l);
     }
+    if (l.tile_n == 192 && l.a_rows == 32)
+        return l.f32 ? launch_one<true, 192, false, 32>(l) : launch_one<false, 192, false, 32>(l);
+    if (l.tile_n == 192 && l.a_rows == 64)
+        return l.f32 ? launch_one<true, 192, false, 64>(l) : launch_one<false, 192, false, 64>(l);
     if (l.tile_n == 192) return l.f32 ? launch_one<true, 192, false>(l) : launch_one<false, 192, false>(l);
     if (l.tile_n == 128) return l.f32 ? launch_one<true, 128, false>(l) : launch_one<false, 128, false>(l);
     return cudaErrorInvalidValue;
@@ -34,13 +39,19 @@ bool mx_set_limits() {
     ok = set_limit<true, 128, false>() && ok;
     ok = set_limit<false, 192, false>() && ok;
     ok = set_limit<true, 192, false>() && ok;
+    ok = set_limit<false, 192, false, 64>() && ok;
+    ok = set_limit<true, 192, false, 64>() && ok;
+    ok = set_limit<false, 192, false, 32>() && ok;
+    ok = set_limit<true, 192, false, 32>() && ok;
     ok = set_limit<false, 192, true>() && ok;
     ok = set_limit<true, 192, true>() && ok;
     return ok;
 }
 
-int mx_smem_bytes(int tile_n, bool pair) {
+int mx_smem_bytes(int tile_n, bool pair, int a_rows) {
     if (pair) return static_cast<int>(mx::Layout<192, true>::SMEM_BYTES);
+    if (a_rows == 32 && tile_n == 192) return static_cast<int>(mx::Layout<192, false, 32>::SMEM_BYTES);
+    if (a_rows == 64 && tile_n == 192) return static_cast<int>(mx::Layout<192, false, 64>::SMEM_BYTES);
     return tile_n == 192 ? static_cast<int>(mx::Layout<192, false>::SMEM_BYTES)
                          : static_cast<int>(mx::Layout<128, false>::SMEM_BYTES);
 }

@@ -1032,6 +1032,7 @@ int mx_pairs_for(tpgemm_handle *h, bool f32) {
 struct MxPlan {
     int tile_m, tile_n;
     bool pair;
+    int a_rows; // rows of A's box: 128, or 64 / 32 on 1-CTA 192-wide tiles for M <= 64 / 32 (deeper rings)
     int64_t mt, nt;
     tpg::Schedule sched;
     int grid;
@@ -1041,6 +1042,7 @@ MxPlan mx_plan(tpgemm_handle *h, int64_t M, int64_t N, bool f32) {
     MxPlan pl;
     pl.pair = mx_pair(M, N);
     pl.tile_n = mx_tile_n(N);
+    pl.a_rows = (!pl.pair && pl.tile_n == 192 && M <= 32) ? 32 : (!pl.pair && pl.tile_n == 192 && M <= 64) ? 64 : 128;
     pl.tile_m = tpg::mx::BM * (pl.pair ? 2 : 1);
     pl.mt = (M + pl.tile_m - 1) / pl.tile_m;
     pl.nt = (N + pl.tile_n - 1) / pl.tile_n;
@@ -1142,7 +1144,8 @@ int gemm_run_mx(tpgemm_handle *h, int64_t M, int64_t N, int64_t K, const void *A
     const uint64_t map_n = static_cast<uint64_t>(n_tma > 0 ? n_tma : N);
     const CUtensorMapDataType out_dt = f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
     CUtensorMap tmA, tmB, tmSA, tmSB, tmC, tmD;
-    if (encode_2d(h, &tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, A, K, M, tma_stride(M, K, lda, 1), 128, 128) ||
+    if (encode_2d(h, &tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, A, K, M, tma_stride(M, K, lda, 1), 128,
+                  static_cast<uint32_t>(pl.a_rows)) ||
         encode_2d(h, &tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, B, K, N, tma_stride(N, K, ldb, 1), 128,
                   static_cast<uint32_t>(pl.pair ? tile_n / 2 : tile_n)) ||
         encode_chunks(h, &tmSA, SA, mx_scale_bytes(M, K) / 512) ||
@@ -1170,7 +1173,7 @@ int gemm_run_mx(tpgemm_handle *h, int64_t M, int64_t N, int64_t K, const void *A
     p.ldd = ldd;
     p.status = h->status;
     p.timeout_ns = h->timeout_ns;
-    const tpg::MxLaunch l{pl.grid, tile_n, pl.pair, f32, stream, &tmA, &tmB, &tmSA, &tmSB, &tmC, &tmD, &p};
+    const tpg::MxLaunch l{pl.grid, tile_n, pl.pair, pl.a_rows, f32, stream, &tmA, &tmB, &tmSA, &tmSB, &tmC, &tmD, &p};
     return tpg::mx_launch(l) == cudaSuccess ? TPGEMM_OK : TPGEMM_ERR_CUDA;
 }
 
@@ -1186,7 +1189,7 @@ int gemm_mx_query_plan(tpgemm_handle *h, int64_t M, int64_t N, int64_t K, int ou
     if (num_tiles) *num_tiles = pl.mt * pl.nt;
     if (grid) *grid = pl.grid;
     if (cluster) *cluster = pl.pair ? 2 : 1;
-    if (smem_bytes) *smem_bytes = tpg::mx_smem_bytes(pl.tile_n, pl.pair);
+    if (smem_bytes) *smem_bytes = tpg::mx_smem_bytes(pl.tile_n, pl.pair, pl.a_rows);
     return TPGEMM_OK;
 }
 
