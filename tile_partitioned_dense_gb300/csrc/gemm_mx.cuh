@@ -100,19 +100,25 @@ struct Layout {
     static_assert(kARows == 128 || (!kPair && kBN == 192 && (kARows == 64 || kARows == 32)),
                   "the small-M rings are 1-CTA, 192 wide");
     static constexpr int CL = kPair ? 2 : 1;
-    static constexpr int STAGES = kPair ? 6 : (kARows == 32 ? 6 : (kARows == 64 ? 5 : (kBN == 192 ? 4 : 5)));
+    // Pair mode keeps one epilogue staging buffer and 1.5 KB scale slots, which
+    // makes room for a seventh stage: its MMAs use a stage up in 384 cycles,
+    // against 512 for the bf16 kernel's, so it needs the deeper ring more.
+    static constexpr int STAGES = kPair ? 7 : (kARows == 32 ? 6 : (kARows == 64 ? 5 : (kBN == 192 ? 4 : 5)));
+    static constexpr int EPI_BUFS = kPair ? 1 : 2;
     static constexpr uint32_t A_ROWS = kARows; // rows of A's box
     static constexpr uint32_t A_BYTES = A_ROWS * BK;
     static constexpr uint32_t B_ROWS = kBN / CL; // rows of B's transpose this CTA stages
     static constexpr uint32_t B_BYTES = B_ROWS * BK;
-    static constexpr uint32_t SF_BYTES = 2048; // A chunk at 0, B chunks at 512 and 1024
+    static constexpr uint32_t SF_BYTES = kPair ? 1536 : 2048; // A chunk at 0, B chunks at 512 and 1024
     static constexpr uint32_t OFF_A = 0;
     static constexpr uint32_t OFF_B = OFF_A + STAGES * A_BYTES;
     static_assert(OFF_A + (STAGES - 1) * A_BYTES + BM * BK <= OFF_B + STAGES * (kBN / CL) * BK,
                   "the MMA's 128-row reads of A stay inside the operand ring");
     static constexpr uint32_t OFF_SF = OFF_B + STAGES * B_BYTES;
-    static constexpr uint32_t OFF_EPI = OFF_SF + STAGES * SF_BYTES;
-    static constexpr uint32_t OFF_BAR = OFF_EPI + 2 * EPI_BUF_BYTES;
+    // the staging buffers are 128-byte swizzled, a pattern taken from address
+    // bits 7-9: they start on a 1024-byte boundary
+    static constexpr uint32_t OFF_EPI = (OFF_SF + STAGES * SF_BYTES + 1023) / 1024 * 1024;
+    static constexpr uint32_t OFF_BAR = OFF_EPI + EPI_BUFS * EPI_BUF_BYTES;
     // full, empty, scales ready, tfull, tempty, c, drain, scale-copy drain
     static constexpr uint32_t NUM_BARS = 3 * STAGES + 2 + 2 + 2 + 2;
     static constexpr uint32_t OFF_MISC = OFF_BAR + NUM_BARS * 8;
@@ -120,6 +126,8 @@ struct Layout {
     static constexpr uint32_t SF_COL0 = 2 * kBN; // first TMEM column of the scale region
     static_assert(SF_COL0 + STAGES * SF_TMEM_STRIDE <= TMEM_COLS, "TMEM overflow");
     static_assert(SMEM_BYTES <= 232448, "exceeds the 227 KB shared-memory limit per CTA");
+    static_assert(OFF_A % 1024 == 0 && OFF_B % 1024 == 0 && A_BYTES % 1024 == 0 && B_BYTES % 1024 == 0,
+                  "128-byte swizzled operand stages start on 1024-byte boundaries");
 };
 
 __device__ __forceinline__ bool mx_drain_wait(uint64_t *bar, uint32_t parity, uint64_t limit_ns) {
@@ -469,7 +477,13 @@ __global__ void __launch_bounds__(THREADS, 1)
                 const bool row_ok = static_cast<int32_t>(row) < rows_valid;
                 const int64_t crow = static_cast<int64_t>(grow) * p.ldc;
                 const int64_t drow = static_cast<int64_t>(grow) * p.ldd;
-                if (leader) bulk_wait_group_read<1>();
+                // The store that last used this buffer must have finished reading it.
+                if (leader) {
+                    if constexpr (L::EPI_BUFS == 2)
+                        bulk_wait_group_read<1>();
+                    else
+                        bulk_wait_group_read<0>();
+                }
                 named_barrier_sync(1, EPI_THREADS);
                 if (has_beta && chunk_tma) {
                     if (leader) {
@@ -560,7 +574,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                     tma_store_2d(&tmD, buf, cb, m0);
                     bulk_commit_group();
                 }
-                slot ^= 1u;
+                if constexpr (L::EPI_BUFS == 2) slot ^= 1u;
             }
             if (!ok) break;
             if (++acc == 2) {
