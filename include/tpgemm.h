@@ -458,7 +458,7 @@ enum tpgemm_fp8_format {
  * D with A, B, SA, SB or C is TPGEMM_ERR_OVERLAP. Errors as gemm_run, plus
  * TPGEMM_ERR_INVALID_ARG for a bad format or K not a multiple of 32.
  * Allocates nothing and never synchronises. Runs a persistent kernel of
- * 256 x 192 tiles on CTA pairs when M and N are both above 128, else of
+ * 256 x 256 tiles on CTA pairs when M and N are both above 128, else of
  * 128 x 192 tiles on single CTAs (128 x 128 when N <= 128).
  */
 int gemm_run_mx(tpgemm_handle *h, int64_t M, int64_t N, int64_t K, const void *A, int64_t lda, int a_format,

@@ -72,10 +72,10 @@ def _want(A, SA, Bt, SB, C, alpha, beta, out_dtype, fmt_a=0, fmt_b=0, rows=None)
     return D
 
 
-# (M, N, K, lda, ldb): one 256 x 192 pair tile and a second one starting 64
-# rows into B's second scale chunk; ragged everything with K = 96 (a partial K
-# block and a partial scale chunk) and N = 200 (the last tile's second scale
-# chunk does not exist), on pairs whose second CTA owns rows past M; 128-column
+# (M, N, K, lda, ldb): one 256 x 256 pair tile and a second one whose second
+# scale chunk does not exist (N = 384); ragged everything with K = 96 (a
+# partial K block and a partial scale chunk) and N = 200, on pairs whose second
+# CTA owns rows past M; 128-column
 # tiles on single CTAs (N <= 128); single CTAs with 192-wide tiles (M <= 128);
 # several pair tiles in both directions with many K blocks; a pair whose
 # second CTA has one row; M <= 32 on 32-row A boxes, M <= 64 on 64-row ones, and
@@ -190,7 +190,7 @@ def test_mx_argument_errors(h):
 def test_mx_plan(h):
     sms = tpd.gemm_num_sms(h)
     p = tpd.gemm_mx_query_plan(h, 8192, 6144, 4096)
-    assert p["tile_m"] == 256 and p["tile_n"] == 192 and p["num_tiles"] == 32 * 32 and p["cluster"] == 2
+    assert p["tile_m"] == 256 and p["tile_n"] == 256 and p["num_tiles"] == 32 * 24 and p["cluster"] == 2
     assert p["grid"] % 2 == 0 and sms - 8 <= p["grid"] <= sms
     p = tpd.gemm_mx_query_plan(h, 16, 28672, 4096)  # 128 rows or fewer: single CTAs
     assert p["tile_m"] == 128 and p["tile_n"] == 192 and p["cluster"] == 1 and p["num_tiles"] == 150
@@ -201,3 +201,55 @@ def test_mx_plan(h):
         sizes.add(p["smem_bytes"])
     p = tpd.gemm_mx_query_plan(h, 256, 128, 4096)
     assert p["tile_m"] == 128 and p["tile_n"] == 128 and p["num_tiles"] == 2 and p["grid"] == 2
+
+
+def test_mx_graph_replay_and_two_streams(h):
+    """gemm_run_mx allocates nothing and keeps no per-call state in the
+    handle: a captured call replays with new inputs, and calls on two streams
+    may run at the same time."""
+    M, N, K = 384, 640, 512
+    Ad = torch.empty((M, K), dtype=torch.uint8, device=DEV)
+    Bd = torch.empty((N, K), dtype=torch.uint8, device=DEV)
+    SAd = torch.empty(tpd.gemm_mx_scale_bytes(M, K), dtype=torch.uint8, device=DEV)
+    SBd = torch.empty(tpd.gemm_mx_scale_bytes(N, K), dtype=torch.uint8, device=DEV)
+    D = torch.empty((M, N), dtype=torch.float32, device=DEV)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(graph, stream=side):
+            st = tpd.gemm_run_mx(h, M, N, K, Ad.data_ptr(), K, 0, SAd.data_ptr(), Bd.data_ptr(), K, 0, SBd.data_ptr(),
+                                 None, N, D.data_ptr(), N, 1.0, 0.0, tpd.OUT_F32,
+                                 torch.cuda.current_stream().cuda_stream)
+            assert st == tpd.OK
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    for rep in range(3):
+        A, SA, Bt, SB = make_mx_inputs(M, N, K, seed=300 + rep, integer=True)
+        Ad.copy_(A)
+        Bd.copy_(Bt)
+        SAd.copy_(torch.from_numpy(mx_blocked(SA.numpy())))
+        SBd.copy_(torch.from_numpy(mx_blocked(SB.numpy())))
+        graph.replay()
+        torch.cuda.synchronize()
+        assert tpd.gemm_sync_status(h, None) == tpd.OK
+        assert_bit_exact(bits(D), _want(A, SA, Bt, SB, None, 1.0, 0.0, torch.float32), f"replay {rep}")
+    del graph
+    # two streams at once, each with its own inputs and output
+    jobs = []
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    for i, s in enumerate(streams):
+        A, SA, Bt, SB = make_mx_inputs(M, N, K, seed=400 + i, integer=True)
+        ins = [A.to(DEV), Bt.to(DEV), torch.from_numpy(mx_blocked(SA.numpy())).to(DEV),
+               torch.from_numpy(mx_blocked(SB.numpy())).to(DEV)]
+        out = torch.empty((M, N), dtype=torch.float32, device=DEV)
+        jobs.append((A, SA, Bt, SB, ins, out, s))
+    torch.cuda.synchronize()
+    for A, SA, Bt, SB, ins, out, s in jobs:
+        st = tpd.gemm_run_mx(h, M, N, K, ins[0].data_ptr(), K, 0, ins[2].data_ptr(), ins[1].data_ptr(), K, 0,
+                             ins[3].data_ptr(), None, N, out.data_ptr(), N, 1.0, 0.0, tpd.OUT_F32, s.cuda_stream)
+        assert st == tpd.OK
+    torch.cuda.synchronize()
+    for A, SA, Bt, SB, ins, out, s in jobs:
+        assert_bit_exact(bits(out), _want(A, SA, Bt, SB, None, 1.0, 0.0, torch.float32), "two streams")

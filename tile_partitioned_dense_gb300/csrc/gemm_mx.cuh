@@ -15,12 +15,17 @@
 // of the bf16 kernel; each tile has one owner ("cuTile Rust explained",
 // "Ownership crosses the launch boundary"):
 //   kPair = false  one CTA per SM owns 128 x kBN tiles (kBN = 128 or 192).
-//   kPair = true   the two CTAs of a cluster pair own a 256 x 192 tile through
-//                  tcgen05.mma.cta_group::2 (M = 256) issued by the even CTA;
-//                  each CTA stages its own 128 rows of A and its own 96 rows of
-//                  B's transpose, so per SM a stage is 28 KB of operands
-//                  instead of 40 KB: six stages fit where four did, and each SM
-//                  reads 30% fewer operand bytes from L2 per MMA.
+//   kPair = true   the two CTAs of a cluster pair own a 256 x 256 tile through
+//                  tcgen05.mma.cta_group::2 (M = 256, N = 256) issued by the
+//                  even CTA; each CTA stages its own 128 rows of A and of B's
+//                  transpose. A 256-wide block-scaled MMA gives the tensor pipe
+//                  128 cycles of work per SM, more than issuing it costs the
+//                  issuing thread (192-wide ones, 96 cycles, capped the kernel
+//                  near 80% of the FP8 rate). Two 256-column accumulators would
+//                  fill TMEM and leave no room for the scales, so a pair has one;
+//                  the epilogue reads it whole into registers (packed bf16)
+//                  before it stages anything, so the next tile's MMAs wait only
+//                  for that read.
 // Roles, connected by mbarriers:
 //   warp 0      TMA producer: per 128-wide K block, one A box (128 rows x 128
 //               bytes) and one B box (kBN / CTAs rows of B's transpose x 128
@@ -35,8 +40,9 @@
 //               to the stage's scales-ready barrier. Keeping the copies off the
 //               MMA thread leaves that thread four MMAs, one wait and one
 //               commit per stage.
-//   warp 1      allocates TMEM (two fp32 accumulators of kBN columns and, per
-//               ring stage, 4 scale columns for A and 8 for B); one lane (of
+//   warp 1      allocates TMEM (fp32 accumulators of kBN columns, two or, for
+//               pairs, one, and per ring stage 4 scale columns for A and 8 for
+//               B); one lane (of
 //               the even CTA) issues the four K = 32 MMAs of a stage once its
 //               scales are in TMEM, scale byte j of each TMEM cell going with
 //               MMA j; tcgen05.commit frees the stage (in both CTAs).
@@ -95,15 +101,15 @@ constexpr uint32_t SF_TMEM_STRIDE = 16; // TMEM columns per stage: A at +0 (4), 
 // next stages' bytes) only reach accumulator rows that are never stored.
 template <int kBN, bool kPair, int kARows = 128>
 struct Layout {
-    static_assert(kBN == 128 || kBN == 192, "tile width");
-    static_assert(!kPair || kBN == 192, "CTA pairs run 192-wide tiles");
+    static_assert(kPair ? kBN == 256 : (kBN == 128 || kBN == 192), "tile width");
     static_assert(kARows == 128 || (!kPair && kBN == 192 && (kARows == 64 || kARows == 32)),
                   "the small-M rings are 1-CTA, 192 wide");
     static constexpr int CL = kPair ? 2 : 1;
-    // Pair mode keeps one epilogue staging buffer and 1.5 KB scale slots, which
-    // makes room for a seventh stage: its MMAs use a stage up in 384 cycles,
-    // against 512 for the bf16 kernel's, so it needs the deeper ring more.
-    static constexpr int STAGES = kPair ? 7 : (kARows == 32 ? 6 : (kARows == 64 ? 5 : (kBN == 192 ? 4 : 5)));
+    // Pair mode: one accumulator of 256 columns (two would fill TMEM and leave
+    // no room for the scales), one epilogue staging buffer and 1.5 KB scale
+    // slots; six stages fit.
+    static constexpr int ACCS = kPair ? 1 : 2;
+    static constexpr int STAGES = kPair ? 6 : (kARows == 32 ? 6 : (kARows == 64 ? 5 : (kBN == 192 ? 4 : 5)));
     static constexpr int EPI_BUFS = kPair ? 1 : 2;
     static constexpr uint32_t A_ROWS = kARows; // rows of A's box
     static constexpr uint32_t A_BYTES = A_ROWS * BK;
@@ -123,7 +129,7 @@ struct Layout {
     static constexpr uint32_t NUM_BARS = 3 * STAGES + 2 + 2 + 2 + 2;
     static constexpr uint32_t OFF_MISC = OFF_BAR + NUM_BARS * 8;
     static constexpr uint32_t SMEM_BYTES = OFF_MISC + 16 + 1024;
-    static constexpr uint32_t SF_COL0 = 2 * kBN; // first TMEM column of the scale region
+    static constexpr uint32_t SF_COL0 = ACCS * kBN; // first TMEM column of the scale region
     static_assert(SF_COL0 + STAGES * SF_TMEM_STRIDE <= TMEM_COLS, "TMEM overflow");
     static_assert(SMEM_BYTES <= 232448, "exceeds the 227 KB shared-memory limit per CTA");
     static_assert(OFF_A % 1024 == 0 && OFF_B % 1024 == 0 && A_BYTES % 1024 == 0 && B_BYTES % 1024 == 0,
@@ -364,7 +370,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                     tc_commit_pair_mc(&tfull[acc], 0x3);
                 else
                     tc_commit(&tfull[acc]);
-                if (++acc == 2) {
+                if (++acc == static_cast<uint32_t>(L::ACCS)) {
                     acc = 0;
                     acc_phase ^= 1u;
                 }
@@ -466,6 +472,52 @@ __global__ void __launch_bounds__(THREADS, 1)
                 }
             };
             if (nchunks == 0) release();
+            if constexpr (kPair && !kOutF32) {
+                if (!has_beta && p.n_tma == p.N) {
+                    // One accumulator per pair: the next tile's MMAs wait until this
+                    // one is read. So read all 256 columns first, packed to bf16 in
+                    // registers (alpha applied, one rounding), hand the accumulator
+                    // back, and only then stage and store the chunks.
+                    uint32_t packed[kBN / 2];
+#pragma unroll
+                    for (int g = 0; g < kBN / 32; ++g) {
+                        uint32_t ra[32];
+                        tmem_ld32(tmem_base + acc * kBN + static_cast<uint32_t>(g * 32) + ((q * 32u) << 16), ra);
+                        tc_wait_ld();
+#pragma unroll
+                        for (int e = 0; e < 16; ++e)
+                            packed[g * 16 + e] = pack_bf16x2(p.alpha * __uint_as_float(ra[2 * e]),
+                                                             p.alpha * __uint_as_float(ra[2 * e + 1]));
+                    }
+                    release();
+                    // N is a whole number of 16-byte cells here, so every chunk goes
+                    // through the tensor map; rows past M are clipped by the store.
+                    uint8_t *rowp = epi + row * 128u;
+#pragma unroll
+                    for (int c = 0; c < kBN / CHUNK; ++c) {
+                        if (c >= nchunks) break;
+                        if (leader) bulk_wait_group_read<0>(); // the last store has read the buffer
+                        named_barrier_sync(1, EPI_THREADS);
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) {
+                            const int base = c * 32 + j * 4; // packed[base .. base+3]: this cell's 8 columns
+                            *reinterpret_cast<uint4 *>(rowp + ((j ^ (row & 7u)) << 4)) =
+                                make_uint4(packed[base], packed[base + 1], packed[base + 2], packed[base + 3]);
+                        }
+                        fence_proxy_async_smem();
+                        named_barrier_sync(1, EPI_THREADS);
+                        if (leader) {
+                            tma_store_2d(&tmD, epi, w.n + c * CHUNK, m0);
+                            bulk_commit_group();
+                        }
+                    }
+                    if (++acc == static_cast<uint32_t>(L::ACCS)) {
+                        acc = 0;
+                        acc_phase ^= 1u;
+                    }
+                    continue;
+                }
+            }
             for (int c = 0; c < nchunks; ++c) {
                 uint8_t *buf = epi + slot * EPI_BUF_BYTES;
                 const int32_t cb = w.n + c * CHUNK;
@@ -577,7 +629,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 if constexpr (L::EPI_BUFS == 2) slot ^= 1u;
             }
             if (!ok) break;
-            if (++acc == 2) {
+            if (++acc == static_cast<uint32_t>(L::ACCS)) {
                 acc = 0;
                 acc_phase ^= 1u;
             }

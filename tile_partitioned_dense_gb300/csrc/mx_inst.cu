@@ -1,5 +1,5 @@
 // Instantiations of the block-scaled (MX) GEMM kernel: 1-CTA tiles 128 or 192
-// columns wide and CTA-pair tiles of 256 x 192, bf16 or fp32 output. The host
+// columns wide and CTA-pair tiles of 256 x 256, bf16 or fp32 output. The host
 // library reaches them through the functions below (launch.cuh).
 #include "launch.cuh"
 
@@ -22,8 +22,8 @@ cudaError_t launch_one(const MxLaunch &l) {
 
 cudaError_t mx_launch(const MxLaunch &l) {
     if (l.pair) {
-        if (l.tile_n != 192 || l.grid % 2 != 0) return cudaErrorInvalidValue;
-        return l.f32 ? launch_one<true, 192, true>(l) : launch_one<false, 192, true>(l);
+        if (l.tile_n != 256 || l.grid % 2 != 0) return cudaErrorInvalidValue;
+        return l.f32 ? launch_one<true, 256, true>(l) : launch_one<false, 256, true>(l);
     }
     if (l.tile_n == 192 && l.a_rows == 32)
         return l.f32 ? launch_one<true, 192, false, 32>(l) : launch_one<false, 192, false, 32>(l);
@@ -43,13 +43,13 @@ bool mx_set_limits() {
     ok = set_limit<true, 192, false, 64>() && ok;
     ok = set_limit<false, 192, false, 32>() && ok;
     ok = set_limit<true, 192, false, 32>() && ok;
-    ok = set_limit<false, 192, true>() && ok;
-    ok = set_limit<true, 192, true>() && ok;
+    ok = set_limit<false, 256, true>() && ok;
+    ok = set_limit<true, 256, true>() && ok;
     return ok;
 }
 
 int mx_smem_bytes(int tile_n, bool pair, int a_rows) {
-    if (pair) return static_cast<int>(mx::Layout<192, true>::SMEM_BYTES);
+    if (pair) return static_cast<int>(mx::Layout<256, true>::SMEM_BYTES);
     if (a_rows == 32 && tile_n == 192) return static_cast<int>(mx::Layout<192, false, 32>::SMEM_BYTES);
     if (a_rows == 64 && tile_n == 192) return static_cast<int>(mx::Layout<192, false, 64>::SMEM_BYTES);
     return tile_n == 192 ? static_cast<int>(mx::Layout<192, false>::SMEM_BYTES)
@@ -60,7 +60,7 @@ int mx_pair_clusters(bool f32, int num_sms) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(2 * (num_sms / 2)), 1, 1);
     cfg.blockDim = dim3(mx::THREADS, 1, 1);
-    cfg.dynamicSmemBytes = mx::Layout<192, true>::SMEM_BYTES;
+    cfg.dynamicSmemBytes = mx::Layout<256, true>::SMEM_BYTES;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 2;
@@ -69,8 +69,8 @@ int mx_pair_clusters(bool f32, int num_sms) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int n = 0;
-    const cudaError_t e = f32 ? cudaOccupancyMaxActiveClusters(&n, mx::gemm_mx_kernel<true, 192, true>, &cfg)
-                              : cudaOccupancyMaxActiveClusters(&n, mx::gemm_mx_kernel<false, 192, true>, &cfg);
+    const cudaError_t e = f32 ? cudaOccupancyMaxActiveClusters(&n, mx::gemm_mx_kernel<true, 256, true>, &cfg)
+                              : cudaOccupancyMaxActiveClusters(&n, mx::gemm_mx_kernel<false, 256, true>, &cfg);
     if (e != cudaSuccess) {
         (void)cudaGetLastError();
         return -1;

@@ -1015,9 +1015,12 @@ int64_t mx_scale_bytes(int64_t rows, int64_t K) {
 // enough to hide its issue cost) unless the output is at most 128 wide.
 int mx_tile_n(int64_t N) { return N > 128 ? 192 : 128; }
 
-// CTA pairs (256 x 192 tiles) when there are more than 128 rows and columns:
-// per SM they stage and read 28 KB of operands per K block instead of 40 KB.
+// CTA pairs (256 x 256 tiles) when there are more than 128 rows and columns:
+// per SM they stage and read 32 KB of operands per K block for twice the
+// work of a 1-CTA 128 x 192 tile's 40 KB, with MMAs wide enough to hide their
+// issue cost.
 bool mx_pair(int64_t M, int64_t N) { return M > 128 && N > 128; }
+constexpr int kMxPairTileN = 256;
 
 int mx_pairs_for(tpgemm_handle *h, bool f32) {
     std::atomic<int> &slot = h->mx_pairs[f32 ? 1 : 0];
@@ -1041,7 +1044,7 @@ struct MxPlan {
 MxPlan mx_plan(tpgemm_handle *h, int64_t M, int64_t N, bool f32) {
     MxPlan pl;
     pl.pair = mx_pair(M, N);
-    pl.tile_n = mx_tile_n(N);
+    pl.tile_n = pl.pair ? kMxPairTileN : mx_tile_n(N);
     pl.a_rows = (!pl.pair && pl.tile_n == 192 && M <= 32) ? 32 : (!pl.pair && pl.tile_n == 192 && M <= 64) ? 64 : 128;
     pl.tile_m = tpg::mx::BM * (pl.pair ? 2 : 1);
     pl.mt = (M + pl.tile_m - 1) / pl.tile_m;
