@@ -29,6 +29,8 @@ ACT_TANH = 3
 FP8_E4M3 = 0
 FP8_E5M2 = 1
 SCALE_E8M0 = 2
+FP4_E2M1 = 3
+SCALE_E4M3 = 0
 MX_BLOCK = 32
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -79,6 +81,10 @@ def _load():
         lib.oracle_mx_gemm_rows.argtypes = [i64, i64, i64, vp, i64, ctypes.c_int, vp, i64, vp, i64, ctypes.c_int,
                                             vp, i64, vp, i64, dbl, dbl, ctypes.c_int, vp, i64, vp, i64, vp, i64,
                                             ctypes.c_int]
+        lib.oracle_bs_gemm_rows.restype = ctypes.c_int
+        lib.oracle_bs_gemm_rows.argtypes = [i64, i64, i64, vp, i64, ctypes.c_int, vp, i64, vp, i64, ctypes.c_int,
+                                            vp, i64, ctypes.c_int, ctypes.c_int, vp, i64, dbl, dbl, ctypes.c_int, vp,
+                                            i64, vp, i64, vp, i64, ctypes.c_int]
         lib.oracle_decode_mx_array.restype = None
         lib.oracle_decode_mx_array.argtypes = [ctypes.c_int, vp, vp, i64]
         _lib = lib
@@ -272,4 +278,48 @@ def mx_gemm_rows(A, SA, Bt, SB, C, alpha: float, beta: float, out_dtype: int, fm
                                  max(N, 1), int(nthreads))
     if rc != 0:
         raise RuntimeError("oracle_mx_gemm_rows rejected its arguments")
+    return D, pre
+
+
+def bs_gemm_rows(A, SA, Bt, SB, C, alpha: float, beta: float, out_dtype: int, fmt_a: int, fmt_b: int,
+                 scale_fmt: int, block: int, rows=None, want_pre: bool = False, nthreads: int | None = None):
+    """The block-scaled GEMM in general form (see oracle_mx.c): element formats
+    FP8_E4M3, FP8_E5M2 or FP4_E2M1 (two per byte, the even element in the low
+    four bits, so a row of K elements is K/2 bytes), scale format SCALE_E8M0 or
+    SCALE_E4M3, `block` (16 or 32) elements per scale. A [M, K or K/2] and Bt
+    [N, K or K/2] are uint8 codes, SA [M, K/block] and SB [N, K/block] scale
+    codes. Returns (D, pre) like gemm_rows."""
+    lib = _load()
+    A, a_ptr, lda = _u8_view(A, "A")
+    SA, sa_ptr, ldsa = _u8_view(SA, "SA")
+    Bt, b_ptr, ldb = _u8_view(Bt, "Bt")
+    SB, sb_ptr, ldsb = _u8_view(SB, "SB")
+    M = A.shape[0]
+    N = Bt.shape[0]
+    K = A.shape[1] * (2 if fmt_a == FP4_E2M1 else 1)
+    kb_ = Bt.shape[1] * (2 if fmt_b == FP4_E2M1 else 1)
+    if kb_ != K or K % block or SA.shape != (M, K // block) or SB.shape != (N, K // block):
+        raise ValueError("shapes of A, SA, Bt, SB do not agree")
+    alpha = float(np.float32(alpha))
+    beta = float(np.float32(beta))
+    if rows is None:
+        rows = np.arange(M, dtype=np.int64)
+    rows = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+    c_ptr, ldc = 0, max(N, 1)
+    if beta != 0.0:
+        want = torch.bfloat16 if out_dtype == OUT_BF16 else torch.float32
+        if C is None or C.dtype != want or tuple(C.shape) != (M, N):
+            raise ValueError("C must be [M,N] of the output dtype when beta != 0")
+        c_ptr, ldc = _bits_view(C, "C")
+    out_np = np.uint16 if out_dtype == OUT_BF16 else np.float32
+    D = np.zeros((len(rows), N), dtype=out_np)
+    pre = np.zeros((len(rows), N), dtype=np.float64) if want_pre else None
+    if nthreads is None:
+        nthreads = len(os.sched_getaffinity(0))
+    rc = lib.oracle_bs_gemm_rows(M, N, K, a_ptr, lda, int(fmt_a), sa_ptr, ldsa, b_ptr, ldb, int(fmt_b), sb_ptr,
+                                 ldsb, int(scale_fmt), int(block), c_ptr, ldc, alpha, beta, out_dtype,
+                                 rows.ctypes.data, len(rows), D.ctypes.data, max(N, 1),
+                                 pre.ctypes.data if pre is not None else None, max(N, 1), int(nthreads))
+    if rc != 0:
+        raise RuntimeError("oracle_bs_gemm_rows rejected its arguments")
     return D, pre

@@ -29,11 +29,27 @@
  * In fp64 every element product is exact (FP8 significands have at most 4
  * bits), and so is every scale product (a power of two between 2^-254 and
  * 2^254); the only roundings are those of the fp64 sums and the final one.
+ * (With NVFP4's E4M3 scales, below, a scale product has at most 8 significant
+ * bits and an element product at most 4: still exact.)
  *
  * Layouts (the oracle's own, plain ones): A is [M, K] bytes, row-major with
  * row stride lda; B is given transposed, Bt = [N, K] bytes, row-major with
  * row stride ldb (B[k,n] = Bt[n,k]); SA is [M, K/32] and SB is [N, K/32] scale
  * bytes, row-major with row strides ldsa and ldsb. K must be a multiple of 32.
+ *
+ * FP4. The same page names FP4 GEMMs, NVFP4 and MXF4, and reports NVFP4
+ * results on decode shapes. Read here as:
+ *  - an FP4 element is E2M1 (OCP MX specification): sign, two exponent bits
+ *    with bias 1, one mantissa bit, a subnormal 0.5 at exponent field 0, no
+ *    infinities or NaNs; the values are 0, 0.5, 1, 1.5, 2, 3, 4 and 6 and
+ *    their negatives;
+ *  - two elements share a byte, the even-numbered one (along K) in the low
+ *    four bits, so a row of K elements is K/2 bytes;
+ *  - MXFP4 (OCP MX): blocks of 32 elements, E8M0 scales, as above;
+ *  - NVFP4 (NVIDIA's FP4 format): blocks of 16 elements, each with an E4M3
+ *    scale, decoded as E4M3 above; the format's per-tensor scale is a plain
+ *    multiplier of the product and is the caller's alpha here.
+ * The block dot product and the GEMM are as above, over K/16 or K/32 blocks.
  */
 #include <math.h>
 #include <pthread.h>
@@ -43,6 +59,8 @@
 
 #define ORACLE_FP8_E4M3 0
 #define ORACLE_FP8_E5M2 1
+#define ORACLE_SCALE_E8M0 2
+#define ORACLE_FP4_E2M1 3
 #define ORACLE_MX_BLOCK 32
 
 /* Defined in oracle.c. */
@@ -72,21 +90,45 @@ double oracle_decode_e5m2(uint8_t x) {
 /* E8M0: 2^(e - 127), e = 255 is NaN. */
 double oracle_decode_e8m0(uint8_t x) { return x == 255 ? NAN : ldexp(1.0, (int)x - 127); }
 
+/* E2M1: s ee m (low four bits of x); exponent field 0 holds the subnormal m/2. */
+double oracle_decode_e2m1(uint8_t x) {
+    const int s = (x >> 3) & 1;
+    const int e = (x >> 1) & 0x3;
+    const int m = x & 0x1;
+    const double v = e == 0 ? 0.5 * m : ldexp((double)(2 + m), e - 2);
+    return s ? -v : v;
+}
+
 static double oracle_decode_fp8(int fmt, uint8_t x) {
     return fmt == ORACLE_FP8_E5M2 ? oracle_decode_e5m2(x) : oracle_decode_e4m3(x);
 }
 
-/* Batch decoders, for the pins. fmt: 0 E4M3, 1 E5M2, 2 E8M0. */
+/* Element k of a row of codes in format fmt (FP4 packs two per byte, element
+ * 2i in the low four bits of byte i). */
+static double oracle_element(int fmt, const uint8_t *row, int64_t k) {
+    if (fmt == ORACLE_FP4_E2M1) return oracle_decode_e2m1((uint8_t)((row[k / 2] >> (4 * (k % 2))) & 0xF));
+    return oracle_decode_fp8(fmt, row[k]);
+}
+
+static double oracle_scale(int sfmt, uint8_t x) {
+    return sfmt == ORACLE_SCALE_E8M0 ? oracle_decode_e8m0(x) : oracle_decode_e4m3(x);
+}
+
+/* Batch decoders, for the pins. fmt: 0 E4M3, 1 E5M2, 2 E8M0, 3 E2M1 (the low
+ * four bits of each byte). */
 void oracle_decode_mx_array(int fmt, const uint8_t *in, double *out, int64_t n) {
     for (int64_t i = 0; i < n; ++i)
-        out[i] = fmt == 2 ? oracle_decode_e8m0(in[i]) : oracle_decode_fp8(fmt, in[i]);
+        out[i] = fmt == ORACLE_SCALE_E8M0 ? oracle_decode_e8m0(in[i])
+                 : fmt == ORACLE_FP4_E2M1 ? oracle_decode_e2m1((uint8_t)(in[i] & 0xF))
+                                           : oracle_decode_fp8(fmt, in[i]);
 }
 
 typedef struct {
-    int64_t N, K, nb;
+    int64_t N, K, nb, block;
     const uint8_t *A;
     int64_t lda;
     int fmt_a;
+    int sfmt;
     const uint8_t *SA;
     int64_t ldsa;
     const double *Bd;  /* decoded B, [K, N] */
@@ -119,15 +161,15 @@ static void *oracle_mx_worker(void *arg) {
         const int64_t i = j->rows[r];
         for (int64_t n = 0; n < j->N; ++n) acc[n] = 0.0;
         for (int64_t b = 0; b < j->nb; ++b) {
-            /* part[n] = sum over the block's 32 k, ascending, of A[i,k] * B[k,n] */
+            /* part[n] = sum over the block's k, ascending, of A[i,k] * B[k,n] */
             for (int64_t n = 0; n < j->N; ++n) part[n] = 0.0;
-            for (int64_t k = b * ORACLE_MX_BLOCK; k < (b + 1) * ORACLE_MX_BLOCK; ++k) {
-                const double a = oracle_decode_fp8(j->fmt_a, j->A[i * j->lda + k]);
+            for (int64_t k = b * j->block; k < (b + 1) * j->block; ++k) {
+                const double a = oracle_element(j->fmt_a, j->A + i * j->lda, k);
                 const double *brow = j->Bd + k * j->N;
                 for (int64_t n = 0; n < j->N; ++n) part[n] += a * brow[n];
             }
             /* acc[n] += (SA[i,b] * SB[n,b]) * part[n] */
-            const double sa = oracle_decode_e8m0(j->SA[i * j->ldsa + b]);
+            const double sa = oracle_scale(j->sfmt, j->SA[i * j->ldsa + b]);
             const double *sb = j->SBd + b * j->N;
             for (int64_t n = 0; n < j->N; ++n) acc[n] += (sa * sb[n]) * part[n];
         }
@@ -159,26 +201,32 @@ static void *oracle_mx_worker(void *arg) {
 }
 
 /*
- * Output rows rows[0..nrows) of the MX GEMM described at the top of this file.
- * C is of the output dtype (0 bf16, 1 fp32), [M, N] with row stride ldc, not
- * read when beta == 0. D is packed [nrows, ldd]; pre (optional) [nrows, ldpre]
- * receives the fp64 value before rounding. fmt_a, fmt_b: 0 E4M3, 1 E5M2.
- * Returns 0, or -1 on a bad argument or an allocation failure.
+ * Output rows rows[0..nrows) of the block-scaled GEMM described at the top of
+ * this file. fmt_a, fmt_b: 0 E4M3, 1 E5M2, 3 E2M1 (FP4, two per byte); sfmt:
+ * 2 E8M0 or 0 E4M3; block: 32 or 16 elements per scale. Row strides are in
+ * bytes; a row of K FP4 elements is K/2 bytes. C is of the output dtype (0
+ * bf16, 1 fp32), [M, N] with row stride ldc, not read when beta == 0. D is
+ * packed [nrows, ldd]; pre (optional) [nrows, ldpre] receives the fp64 value
+ * before rounding. Returns 0, or -1 on a bad argument or an allocation failure.
  */
-int oracle_mx_gemm_rows(int64_t M, int64_t N, int64_t K, const uint8_t *A, int64_t lda, int fmt_a,
+int oracle_bs_gemm_rows(int64_t M, int64_t N, int64_t K, const uint8_t *A, int64_t lda, int fmt_a,
                         const uint8_t *SA, int64_t ldsa, const uint8_t *Bt, int64_t ldb, int fmt_b,
-                        const uint8_t *SB, int64_t ldsb, const void *C, int64_t ldc, double alpha,
-                        double beta, int out_dtype, const int64_t *rows, int64_t nrows, void *D,
+                        const uint8_t *SB, int64_t ldsb, int sfmt, int block, const void *C, int64_t ldc,
+                        double alpha, double beta, int out_dtype, const int64_t *rows, int64_t nrows, void *D,
                         int64_t ldd, double *pre, int64_t ldpre, int nthreads) {
-    if (M < 0 || N < 0 || K < 0 || nrows < 0 || K % ORACLE_MX_BLOCK != 0) return -1;
+    if (block != 16 && block != 32) return -1;
+    if (M < 0 || N < 0 || K < 0 || nrows < 0 || K % block != 0) return -1;
     if (out_dtype != 0 && out_dtype != 1) return -1;
-    if ((fmt_a != ORACLE_FP8_E4M3 && fmt_a != ORACLE_FP8_E5M2) ||
-        (fmt_b != ORACLE_FP8_E4M3 && fmt_b != ORACLE_FP8_E5M2))
+    if (sfmt != ORACLE_SCALE_E8M0 && sfmt != ORACLE_FP8_E4M3) return -1;
+    if ((fmt_a != ORACLE_FP8_E4M3 && fmt_a != ORACLE_FP8_E5M2 && fmt_a != ORACLE_FP4_E2M1) ||
+        (fmt_b != ORACLE_FP8_E4M3 && fmt_b != ORACLE_FP8_E5M2 && fmt_b != ORACLE_FP4_E2M1))
         return -1;
     if (nrows == 0 || N == 0) return 0;
-    const int64_t nb = K / ORACLE_MX_BLOCK;
+    const int64_t nb = K / block;
+    const int64_t row_a = fmt_a == ORACLE_FP4_E2M1 ? K / 2 : K;
+    const int64_t row_b = fmt_b == ORACLE_FP4_E2M1 ? K / 2 : K;
     if (!rows || !D || ldd < N) return -1;
-    if (K > 0 && (!A || !Bt || !SA || !SB || lda < K || ldb < K || ldsa < nb || ldsb < nb)) return -1;
+    if (K > 0 && (!A || !Bt || !SA || !SB || lda < row_a || ldb < row_b || ldsa < nb || ldsb < nb)) return -1;
     if (beta != 0.0 && (!C || ldc < N)) return -1;
     if (pre && ldpre < N) return -1;
     for (int64_t r = 0; r < nrows; ++r)
@@ -194,8 +242,8 @@ int oracle_mx_gemm_rows(int64_t M, int64_t N, int64_t K, const uint8_t *A, int64
         return -1;
     }
     for (int64_t n = 0; n < N; ++n) {
-        for (int64_t k = 0; k < K; ++k) Bd[k * N + n] = oracle_decode_fp8(fmt_b, Bt[n * ldb + k]);
-        for (int64_t b = 0; b < nb; ++b) SBd[b * N + n] = oracle_decode_e8m0(SB[n * ldsb + b]);
+        for (int64_t k = 0; k < K; ++k) Bd[k * N + n] = oracle_element(fmt_b, Bt + n * ldb, k);
+        for (int64_t b = 0; b < nb; ++b) SBd[b * N + n] = oracle_scale(sfmt, SB[n * ldsb + b]);
     }
 
     if (nthreads < 1) nthreads = 1;
@@ -213,8 +261,8 @@ int oracle_mx_gemm_rows(int64_t M, int64_t N, int64_t K, const uint8_t *A, int64
     }
     for (int t = 0; t < nthreads; ++t) {
         oracle_mx_job *j = &jobs[t];
-        j->N = N; j->K = K; j->nb = nb;
-        j->A = A; j->lda = lda; j->fmt_a = fmt_a; j->SA = SA; j->ldsa = ldsa;
+        j->N = N; j->K = K; j->nb = nb; j->block = block;
+        j->A = A; j->lda = lda; j->fmt_a = fmt_a; j->sfmt = sfmt; j->SA = SA; j->ldsa = ldsa;
         j->Bd = Bd; j->SBd = SBd;
         j->C = C; j->ldc = ldc; j->alpha = alpha; j->beta = beta; j->out_dtype = out_dtype;
         j->rows = rows; j->D = D; j->ldd = ldd; j->pre = pre; j->ldpre = ldpre;
@@ -239,4 +287,18 @@ int oracle_mx_gemm_rows(int64_t M, int64_t N, int64_t K, const uint8_t *A, int64
     free(Bd);
     free(SBd);
     return rc;
+}
+
+/* The MX (FP8 elements, E8M0 scales, blocks of 32) form of oracle_bs_gemm_rows. */
+int oracle_mx_gemm_rows(int64_t M, int64_t N, int64_t K, const uint8_t *A, int64_t lda, int fmt_a,
+                        const uint8_t *SA, int64_t ldsa, const uint8_t *Bt, int64_t ldb, int fmt_b,
+                        const uint8_t *SB, int64_t ldsb, const void *C, int64_t ldc, double alpha,
+                        double beta, int out_dtype, const int64_t *rows, int64_t nrows, void *D,
+                        int64_t ldd, double *pre, int64_t ldpre, int nthreads) {
+    if ((fmt_a != ORACLE_FP8_E4M3 && fmt_a != ORACLE_FP8_E5M2) ||
+        (fmt_b != ORACLE_FP8_E4M3 && fmt_b != ORACLE_FP8_E5M2))
+        return -1;
+    return oracle_bs_gemm_rows(M, N, K, A, lda, fmt_a, SA, ldsa, Bt, ldb, fmt_b, SB, ldsb, ORACLE_SCALE_E8M0,
+                               ORACLE_MX_BLOCK, C, ldc, alpha, beta, out_dtype, rows, nrows, D, ldd, pre, ldpre,
+                               nthreads);
 }
