@@ -56,7 +56,7 @@ def parse_args():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="budget of the oracle sample")
     ap.add_argument("--no-sustained", action="store_true", help="skip the repetitions and the sustained regions")
-    ap.add_argument("--only-mx", action="store_true", help="of the per_config rows, measure the MXFP8 ones only")
+    ap.add_argument("--only-mx", action="store_true", help="of the per_config rows, measure the block-scaled (MXFP8, FP4) ones only")
     return ap.parse_args()
 
 
@@ -320,64 +320,159 @@ class TorchScaledMM:
         return 0
 
 
-def mx_entries(torch, tpd, h, l2, peaks, local, barrier, rank, world, args):
-    """The MXFP8 rows: TFLOP/s against the FP8 tensor peak (the measured bf16
-    peak times the nominal FP8 : bf16 ratio of 2) for the QKV and medium
-    shapes; bytes of B and its scales per second against the HBM copy peak for
-    the decode shape. Each with torch._scaled_mm on the same buffers when
-    this torch offers MXFP8 scaled_mm, and the MX oracle's CPU baseline."""
-    from workloads import MX_CONFIGS
+class Fp4Workload:
+    """A block-scaled FP4 workload through gemm_run_fp4: packed E2M1 A and B's
+    transpose (N(0,1) data quantised per block), scales in the blocked layout,
+    bf16 D, rotating device copies."""
+
+    def __init__(self, cfg, torch, l2_bytes):
+        from workloads import E4M3_ONE, FP4_NV, make_fp4_inputs, mx_blocked_scales
+        self.cfg = cfg
+        A, SA, Bt, SB = make_fp4_inputs(cfg.M, cfg.N, cfg.K, seed=cfg.seed, fmt=cfg.fmt)
+        self.host = (A, SA, Bt, SB)
+        pad = E4M3_ONE if cfg.fmt == FP4_NV else 127
+        sa = torch.from_numpy(mx_blocked_scales(SA.numpy(), pad=pad))
+        sb = torch.from_numpy(mx_blocked_scales(SB.numpy(), pad=pad))
+        per_set = A.numel() + Bt.numel() + sa.numel() + sb.numel() + cfg.M * cfg.N * 2
+        self.nsets = max(2, -(-3 * l2_bytes // per_set) + 1)
+        self.sets = [{"A": A.cuda(), "B": Bt.cuda(), "SA": sa.cuda(), "SB": sb.cuda(),
+                      "D": torch.empty((cfg.M, cfg.N), dtype=torch.bfloat16, device="cuda")}
+                     for _ in range(self.nsets)]
+        self.b_bytes = Bt.numel() + sb.numel()
+
+    def run(self, tpd, h, i, stream):
+        s = self.sets[i % self.nsets]
+        c = self.cfg
+        return tpd.gemm_run_fp4(h, c.M, c.N, c.K, c.fmt, s["A"].data_ptr(), c.K // 2, s["SA"].data_ptr(),
+                                s["B"].data_ptr(), c.K // 2, s["SB"].data_ptr(), None, c.N, s["D"].data_ptr(), c.N,
+                                1.0, 0.0, tpd.OUT_BF16, stream)
+
+
+class TorchScaledMMFp4:
+    """The same NVFP4 workload through torch._scaled_mm (NVIDIA's library
+    kernel), on the same buffers: a comparison row, not this library's path."""
+
+    def __init__(self, wl, torch):
+        self.wl = wl
+        self.torch = torch
+
+    def run(self, tpd, h, i, stream):
+        torch = self.torch
+        s = self.wl.sets[i % self.wl.nsets]
+        a = s["A"].view(torch.float4_e2m1fn_x2)
+        b = s["B"].view(torch.float4_e2m1fn_x2).t()
+        torch._scaled_mm(a, b, s["SA"].view(torch.float8_e4m3fn), s["SB"].view(torch.float8_e4m3fn),
+                         out_dtype=torch.bfloat16, out=s["D"])
+        return 0
+
+
+def block_scaled_rows(torch, tpd, h, l2, peaks, local, barrier, args, rows):
+    """Bench rows of the block-scaled GEMMs. Each row: TFLOP/s against the
+    format's tensor peak (the measured bf16 peak times the nominal ratio:
+    FP8 2, FP4 6) or, for the HBM-bound shapes, bytes of B and its scales per
+    second against the HBM copy peak; with torch._scaled_mm on the same
+    buffers when this torch offers it, and the oracle's CPU baseline."""
     out = {}
-    fp8_peak = 2.0 * peaks["bf16_tflops"]
-    for name in ["mx_qkv", "mx_medium", "mx_decode"]:
-        cfg = MX_CONFIGS[name]
-        wl = MxWorkload(cfg, torch, l2)
-        plan = tpd.gemm_mx_query_plan(h, cfg.M, cfg.N, cfg.K)
-        steps = 400 if name != "mx_qkv" else 200
+    for r in rows:
+        name, cfg, wl = r["name"], r["cfg"], r["make"](r["cfg"], torch, l2)
+        plan = r["plan"](cfg)
+        steps = r["steps"]
         span, eager = time_launches(torch, tpd, h, wl, steps, 10, barrier)
         ms = span / steps
-        decode = name == "mx_decode"
-        if decode:
+        hbm = r["hbm"]
+        tpeak = r["ratio"] * peaks["bf16_tflops"]
+        if hbm:
             v, unit, peak, bound = wl.b_bytes / (ms * 1e-3) / 1e9, "GB/s", peaks["hbm_gbs"], "hbm"
         else:
-            v, unit, peak, bound = cfg.flops / (ms * 1e-3) / 1e12, "TFLOP/s", fp8_peak, "tensor"
+            v, unit, peak, bound = cfg.flops / (ms * 1e-3) / 1e12, "TFLOP/s", tpeak, "tensor"
         e = {"value": round(v, 2), "unit": unit, "ms_per_step": round(ms, 5), "eager_ms_per_step": round(eager / steps, 5),
              "steps": steps, "tflops": round(cfg.flops / (ms * 1e-3) / 1e12, 2),
              "roofline": {"bound": bound, "achieved": round(v, 2), "peak": peak, "unit": unit,
                           "frac": round(v / peak, 4), "kernel": "tpg::mx::gemm_mx_kernel",
-                          "peak_source": "2 x MEASURED_PEAKS.json bf16 burst (nominal FP8 : bf16 = 2)" if not decode
+                          "peak_source": f"{r['ratio']:g} x MEASURED_PEAKS.json bf16 burst (nominal ratio)" if not hbm
                           else "MEASURED_PEAKS.json hbm_gbs"},
              "config": {"workload": f"{name}: {cfg.description}", "M": cfg.M, "N": cfg.N, "K": cfg.K,
                         "l2": f"inputs larger than L2: {wl.nsets} rotating device copies"},
              "plan": plan}
         if not args.no_sustained:
-            work = wl.b_bytes if decode else cfg.flops
+            work = wl.b_bytes if hbm else cfg.flops
             times = time_reps(torch, tpd, h, wl, REPS)
             med, best = statistics.median(times), min(times)
-            sc = 1e9 if decode else 1e12
+            sc = 1e9 if hbm else 1e12
             e["reps"] = {"count": REPS, "median_ms": round(med, 5), "best_ms": round(best, 5),
                          "median": round(work / (med * 1e-3) / sc, 2), "best": round(work / (best * 1e-3) / sc, 2),
                          "unit": unit}
-            if name == "mx_qkv":
+            if r.get("sustained"):
                 sms, n, secs, clocks = time_sustained(torch, tpd, h, wl, ms, SUSTAINED_SECONDS, local)
                 sv = work / (sms * 1e-3) / sc
-                speak = 2.0 * peaks["bf16_tflops_sustained"]
+                speak = r["ratio"] * peaks["bf16_tflops_sustained"]
                 e["sustained"] = {"value": round(sv, 2), "unit": unit, "ms_per_launch": round(sms, 5), "launches": n,
                                   "seconds": round(secs, 3), "peak": speak, "frac": round(sv / speak, 4),
-                                  "peak_key": "2 x bf16_tflops_sustained", "clocks": clocks}
-        try:
-            tspan, _ = time_launches(torch, tpd, h, TorchScaledMM(wl, torch), min(steps, 100), 3, barrier)
-            tms = tspan / min(steps, 100)
-            e["torch_scaled_mm"] = {"ms_per_step": round(tms, 5), "ours_over_torch": round(tms / ms, 3)}
-        except Exception as exc:  # this torch may not offer MXFP8 scaled_mm
-            e["torch_scaled_mm"] = {"unavailable": f"{type(exc).__name__}: {str(exc).splitlines()[0][:160]}"}
-            torch.cuda.synchronize()
-        if rank == 0 and world == 1 and not args.no_cpu_baseline:
-            e["cpu_baseline"] = mx_cpu_baseline(cfg, wl.host, 3.0)
+                                  "peak_key": f"{r['ratio']:g} x bf16_tflops_sustained", "clocks": clocks}
+        if r.get("torch") is not None:
+            try:
+                tspan, _ = time_launches(torch, tpd, h, r["torch"](wl, torch), min(steps, 100), 3, barrier)
+                tms = tspan / min(steps, 100)
+                e["torch_scaled_mm"] = {"ms_per_step": round(tms, 5), "ours_over_torch": round(tms / ms, 3)}
+            except Exception as exc:  # this torch may not offer the format in scaled_mm
+                e["torch_scaled_mm"] = {"unavailable": f"{type(exc).__name__}: {str(exc).splitlines()[0][:160]}"}
+                torch.cuda.synchronize()
+        if r.get("cpu"):
+            e["cpu_baseline"] = r["cpu"](cfg, wl.host, 3.0)
         out[name] = e
         del wl
         torch.cuda.empty_cache()
     return out
+
+
+def mx_entries(torch, tpd, h, l2, peaks, local, barrier, rank, world, args):
+    """The MXFP8 rows (QKV and medium shapes tensor-bound, decode HBM-bound)."""
+    from workloads import MX_CONFIGS
+    cpu = mx_cpu_baseline if rank == 0 and world == 1 and not args.no_cpu_baseline else None
+    plan = lambda c: tpd.gemm_mx_query_plan(h, c.M, c.N, c.K)  # noqa: E731
+    rows = [{"name": n, "cfg": MX_CONFIGS[n], "make": MxWorkload, "torch": TorchScaledMM, "plan": plan,
+             "ratio": 2.0, "hbm": n == "mx_decode", "steps": 200 if n == "mx_qkv" else 400,
+             "sustained": n == "mx_qkv", "cpu": cpu} for n in ["mx_qkv", "mx_medium", "mx_decode"]]
+    return block_scaled_rows(torch, tpd, h, l2, peaks, local, barrier, args, rows)
+
+
+def fp4_entries(torch, tpd, h, l2, peaks, local, barrier, rank, world, args):
+    """The NVFP4 rows: the decode shape and a 256-row one HBM-bound (bytes of
+    B and its scales per second), the QKV shape against the FP4 tensor peak
+    (the measured bf16 peak times the nominal FP4 : bf16 ratio of 6)."""
+    from workloads import FP4_CONFIGS
+    cpu = fp4_cpu_baseline if rank == 0 and world == 1 and not args.no_cpu_baseline else None
+    plan = lambda c: tpd.gemm_fp4_query_plan(h, c.fmt, c.M, c.N, c.K)  # noqa: E731
+    rows = [{"name": n, "cfg": FP4_CONFIGS[n], "make": Fp4Workload, "torch": TorchScaledMMFp4, "plan": plan,
+             "ratio": 6.0, "hbm": n != "nvfp4_qkv", "steps": 200 if n == "nvfp4_qkv" else 400,
+             "sustained": n == "nvfp4_qkv", "cpu": cpu} for n in FP4_CONFIGS]
+    return block_scaled_rows(torch, tpd, h, l2, peaks, local, barrier, args, rows)
+
+
+def fp4_cpu_baseline(cfg, host, budget_s):
+    """The block-scaled oracle as it stands, on a bounded row sample of the FP4 workload."""
+    import oracle
+    from workloads import FP4_BLOCK, FP4_NV, sample_rows
+    A, SA, Bt, SB = host
+    sf = oracle.SCALE_E4M3 if cfg.fmt == FP4_NV else oracle.SCALE_E8M0
+    threads = len(os.sched_getaffinity(0))
+
+    def run(rows):
+        oracle.bs_gemm_rows(A, SA, Bt, SB, None, 1.0, 0.0, 0, oracle.FP4_E2M1, oracle.FP4_E2M1, sf,
+                            FP4_BLOCK[cfg.fmt], rows=rows, nthreads=threads)
+
+    probe = sample_rows(cfg.M, max(1, min(cfg.M, threads)), seed=7)
+    t0 = time.perf_counter()
+    run(probe)
+    per_row = (time.perf_counter() - t0) / len(probe)
+    nrows = int(max(len(probe), min(cfg.M, budget_s / max(per_row, 1e-9))))
+    rows = sample_rows(cfg.M, nrows, seed=11)
+    t0 = time.perf_counter()
+    run(rows)
+    dt = time.perf_counter() - t0
+    return {"value": 2.0 * len(rows) * cfg.N * cfg.K / dt / 1e12, "unit": "TFLOP/s", "cores": threads,
+            "kind": "oracle", "sample": f"{len(rows)} of {cfg.M} rows of {cfg.name}, {dt:.1f} s, fp64 C block-scaled "
+                                        f"oracle, {threads} threads"}
 
 
 def mx_cpu_baseline(cfg, host, budget_s):
@@ -919,6 +1014,8 @@ def run_ours(args):
     if not args.no_extra:
         per_config.update(mx_entries(torch, tpd, h, l2, peaks, local, barrier, rank, world, args))
         launches += 200 + 400 + 400
+        per_config.update(fp4_entries(torch, tpd, h, l2, peaks, local, barrier, rank, world, args))
+        launches += 400 + 400 + 200
 
     if bf16_extra:
         per_config["tp_overlay_chunks"] = chunk_tradeoff(torch, tpd, h)

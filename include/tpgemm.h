@@ -481,6 +481,72 @@ int gemm_mx_check_args(int64_t M, int64_t N, int64_t K, const void *A, int64_t l
 int gemm_mx_query_plan(tpgemm_handle *h, int64_t M, int64_t N, int64_t K, int out_dtype, int *tile_m, int *tile_n,
                        int64_t *num_tiles, int *grid, int *cluster, int *smem_bytes);
 
+/* FP4 formats of the block-scaled GEMM (gemm_run_fp4). */
+enum tpgemm_fp4_format {
+    TPGEMM_NVFP4 = 0, /* E2M1 elements, one E4M3 scale per 16 elements along K */
+    TPGEMM_MXFP4 = 1  /* E2M1 elements, one E8M0 scale per 32 elements along K (OCP MX) */
+};
+
+/*
+ * Block-scaled GEMM, FP4 (scaled_mm): "TorchInductor ganha suporte a GEMMs de
+ * alta performance com CuteDSL" names NVFP4 and MXF4 GEMMs among those its
+ * backend covers (the enablement paragraph) and reports NVFP4 results on
+ * decode shapes (the results paragraph). The page defines no format; read as:
+ * an element is E2M1 (OCP MX v1.0: sign, two exponent bits with bias 1, one
+ * mantissa bit; the values 0, 0.5, 1, 1.5, 2, 3, 4, 6 and their negatives),
+ * two to a byte with the even-numbered element (along K) in the low four
+ * bits. NVFP4 gives every 16 consecutive elements along K one E4M3 scale
+ * (unsigned: the sign bit must be clear); its per-tensor fp32 scale is the
+ * caller's alpha. MXFP4 gives every 32 one E8M0 scale (2^(e - 127)). With
+ * A_b, B_b the b-th block of K:
+ *     D = alpha * sum_b (SA[:, b] SB[:, b]^T) .* (A_b * B_b) + beta * C
+ * accumulated in fp32 on the tensor cores (tcgen05.mma kind::mxf4nvf4 applies
+ * the scales), then alpha, beta*C and one rounding as in gemm_run.
+ *   M, N, K     >= 0, each <= 2^31 - 1; K a multiple of 16 (NVFP4) or 32
+ *               (MXFP4).
+ *   format      TPGEMM_NVFP4 or TPGEMM_MXFP4.
+ *   A, lda      packed E2M1 codes, row-major [M, K/2] bytes; lda is the row
+ *               stride in BYTES, >= K/2, a multiple of 16 (not checked for
+ *               M == 1).
+ *   B, ldb      packed E2M1 codes of B TRANSPOSED: row-major [N, K/2] bytes,
+ *               ldb >= K/2 bytes, a multiple of 16 (not checked for N == 1).
+ *   SA, SB      scale codes of A's M rows and B's N columns (E4M3 for NVFP4,
+ *               E8M0 for MXFP4) in the blocked layout of gemm_run_mx: 512-byte
+ *               chunks of 128 rows x 4 scale columns, chunk (row block rb,
+ *               column block cb) at byte (rb * ceil(K/(4*block)) + cb) * 512
+ *               (block = 16 or 32), inside it the scale of row r, scale column
+ *               c at byte (r % 32) * 16 + (r / 32) * 4 + c;
+ *               gemm_fp4_scale_bytes(format, M, K) and (format, N, K) bytes,
+ *               16-byte aligned. Bytes of rows past M (N) or of scale columns
+ *               past K/block are read and must hold finite scales (not 0x7F
+ *               or 0xFF for E4M3, not 255 for E8M0; zero is fine).
+ *   C, ldc, D, ldd, alpha, beta, out_dtype   as gemm_run.
+ * K == 0 gives D = beta*C. D may equal C (same stride); any other overlap of
+ * D with A, B, SA, SB or C is TPGEMM_ERR_OVERLAP. Errors as gemm_run, plus
+ * TPGEMM_ERR_INVALID_ARG for a bad format or K not a multiple of the block.
+ * Allocates nothing and never synchronises. Runs a persistent kernel of
+ * 256 x 256 tiles on CTA pairs when M and N are both above 128, else of
+ * 128 x 128 tiles on single CTAs.
+ */
+int gemm_run_fp4(tpgemm_handle *h, int64_t M, int64_t N, int64_t K, int format, const void *A, int64_t lda,
+                 const void *SA, const void *B, int64_t ldb, const void *SB, const void *C, int64_t ldc, void *D,
+                 int64_t ldd, float alpha, float beta, int out_dtype, void *stream);
+
+/* Bytes of one operand's scales in gemm_run_fp4's blocked layout:
+ * ceil(rows / 128) * ceil(K / (4 * block)) * 512, block = 16 (NVFP4) or 32
+ * (MXFP4); TPGEMM_ERR_INVALID_ARG for a bad format or negative sizes. */
+int64_t gemm_fp4_scale_bytes(int format, int64_t rows, int64_t K);
+
+/* The argument checks of gemm_run_fp4 alone (no handle, no GPU; pointers are
+ * only compared and tested for alignment). */
+int gemm_fp4_check_args(int64_t M, int64_t N, int64_t K, int format, const void *A, int64_t lda, const void *SA,
+                        const void *B, int64_t ldb, const void *SB, const void *C, int64_t ldc, const void *D,
+                        int64_t ldd, float beta, int out_dtype);
+
+/* What gemm_run_fp4 launches for this shape, as gemm_mx_query_plan. */
+int gemm_fp4_query_plan(tpgemm_handle *h, int format, int64_t M, int64_t N, int64_t K, int out_dtype, int *tile_m,
+                        int *tile_n, int64_t *num_tiles, int *grid, int *cluster, int *smem_bytes);
+
 /*
  * Allocation-free GEMM (no counterpart in the paper; it serves callers that
  * cannot allocate device memory). Some callers cannot call cudaMalloc: code

@@ -363,3 +363,58 @@ def test_mx_check_args():
 def test_mx_null_handle():
     assert tpd.gemm_run_mx(None, 8, 8, 32, A0, 32, 0, 0x50000000, B0, 32, 0, 0x60000000, None, 8, D0, 8, 1.0, 0.0,
                            tpd.OUT_F32, None) == tpd.ERR_INVALID_ARG
+
+
+# ---------------------------------------------------------------- block-scaled FP4 argument checks
+
+def fp4_chk(M=128, N=128, K=256, fmt=tpd.NVFP4, A=A0, lda=None, SA=0x50000000, B=B0, ldb=None, SB=0x60000000,
+            C=None, ldc=None, D=D0, ldd=None, beta=0.0, out=tpd.OUT_BF16):
+    lda = K // 2 if lda is None else lda
+    ldb = K // 2 if ldb is None else ldb
+    ldc = N if ldc is None else ldc
+    ldd = N if ldd is None else ldd
+    return tpd.gemm_fp4_check_args(M, N, K, fmt, A, lda, SA, B, ldb, SB, C, ldc, D, ldd, beta, out)
+
+
+def test_fp4_scale_bytes():
+    nv, mx = tpd.NVFP4, tpd.MXFP4
+    # NVFP4: a chunk per 128 rows and 64 elements of K; MXFP4: per 128 elements
+    assert tpd.gemm_fp4_scale_bytes(nv, 128, 64) == 512
+    assert tpd.gemm_fp4_scale_bytes(nv, 128, 80) == 1024
+    assert tpd.gemm_fp4_scale_bytes(nv, 129, 64) == 1024
+    assert tpd.gemm_fp4_scale_bytes(nv, 8192, 4096) == 64 * 64 * 512
+    assert tpd.gemm_fp4_scale_bytes(mx, 8192, 4096) == tpd.gemm_mx_scale_bytes(8192, 4096)
+    assert tpd.gemm_fp4_scale_bytes(mx, 128, 160) == 1024
+    assert tpd.gemm_fp4_scale_bytes(nv, 0, 4096) == 0
+    assert tpd.gemm_fp4_scale_bytes(nv, -1, 16) == tpd.ERR_INVALID_ARG
+    assert tpd.gemm_fp4_scale_bytes(2, 128, 64) == tpd.ERR_INVALID_ARG
+
+
+def test_fp4_check_args():
+    assert fp4_chk() == tpd.OK and fp4_chk(fmt=tpd.MXFP4) == tpd.OK
+    assert fp4_chk(K=96) == tpd.OK and fp4_chk(K=96, fmt=tpd.MXFP4) == tpd.OK
+    assert fp4_chk(K=80, lda=48, ldb=48) == tpd.OK                            # 16-element blocks
+    assert fp4_chk(K=80, lda=48, ldb=48, fmt=tpd.MXFP4) == tpd.ERR_INVALID_ARG  # not whole 32-element blocks
+    assert fp4_chk(K=100) == tpd.ERR_INVALID_ARG
+    assert fp4_chk(fmt=2) == tpd.ERR_INVALID_ARG and fp4_chk(fmt=-1) == tpd.ERR_INVALID_ARG
+    assert fp4_chk(out=5) == tpd.ERR_INVALID_ARG
+    assert fp4_chk(lda=64) == tpd.ERR_INVALID_ARG and fp4_chk(ldb=127) == tpd.ERR_INVALID_ARG  # < K/2 bytes
+    assert fp4_chk(lda=136) == tpd.ERR_ALIGNMENT and fp4_chk(ldb=136) == tpd.ERR_ALIGNMENT
+    assert fp4_chk(M=1, lda=136) == tpd.OK  # one row: its stride is not used
+    assert fp4_chk(SA=0x50000008) == tpd.ERR_ALIGNMENT and fp4_chk(SB=0x60000004) == tpd.ERR_ALIGNMENT
+    assert fp4_chk(SA=None) == tpd.ERR_INVALID_ARG
+    assert fp4_chk(M=2 ** 31) == tpd.ERR_TOO_LARGE
+    assert fp4_chk(M=0) == tpd.OK and fp4_chk(N=0, D=None) == tpd.OK
+    assert fp4_chk(K=0, A=None, B=None, SA=None, SB=None) == tpd.OK
+    assert fp4_chk(beta=1.0) == tpd.ERR_INVALID_ARG  # C missing
+    assert fp4_chk(beta=1.0, C=D0) == tpd.OK          # in place
+    assert fp4_chk(beta=1.0, C=D0 + 16) == tpd.ERR_OVERLAP
+    assert fp4_chk(D=0x50000000 + 1024) == tpd.ERR_OVERLAP  # D inside A's scales (2 KB for NVFP4 here)
+    assert fp4_chk(D=0x50000000 + 1024, fmt=tpd.MXFP4) == tpd.OK  # past MXFP4's 1 KB
+    assert fp4_chk(D=A0 + 64) == tpd.ERR_OVERLAP
+    assert fp4_chk(D=B0) == tpd.ERR_OVERLAP
+
+
+def test_fp4_null_handle():
+    assert tpd.gemm_run_fp4(None, 8, 8, 64, tpd.NVFP4, A0, 32, 0x50000000, B0, 32, 0x60000000, None, 8, D0, 8, 1.0,
+                            0.0, tpd.OUT_F32, None) == tpd.ERR_INVALID_ARG

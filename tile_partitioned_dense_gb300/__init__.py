@@ -31,6 +31,9 @@ ACT_TANH = 3
 FP8_E4M3 = 0
 FP8_E5M2 = 1
 
+NVFP4 = 0
+MXFP4 = 1
+
 OK = 0
 ERR_INVALID_ARG = -1
 ERR_ALIGNMENT = -2
@@ -101,6 +104,12 @@ def load_library() -> ctypes.CDLL:
             "gemm_mx_check_args": (i32, [i64, i64, i64, vp, i64, i32, vp, vp, i64, i32, vp, vp, i64, vp, i64, f32,
                                          i32]),
             "gemm_mx_query_plan": (i32, [vp, i64, i64, i64, i32, pi32, pi32, pi64, pi32, pi32, pi32]),
+            "gemm_run_fp4": (i32, [vp, i64, i64, i64, i32, vp, i64, vp, vp, i64, vp, vp, i64, vp, i64, f32, f32,
+                                   i32, vp]),
+            "gemm_fp4_scale_bytes": (i64, [i32, i64, i64]),
+            "gemm_fp4_check_args": (i32, [i64, i64, i64, i32, vp, i64, vp, vp, i64, vp, vp, i64, vp, i64, f32,
+                                          i32]),
+            "gemm_fp4_query_plan": (i32, [vp, i32, i64, i64, i64, i32, pi32, pi32, pi64, pi32, pi32, pi32]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -277,6 +286,35 @@ def gemm_mx_query_plan(h, M, N, K, out_dtype=OUT_BF16) -> dict:
                                            ctypes.byref(smem))
     if st != OK:
         raise TpgemmError(st, "gemm_mx_query_plan")
+    return {"tile_m": tm.value, "tile_n": tn.value, "num_tiles": tiles.value, "grid": grid.value,
+            "cluster": cl.value, "smem_bytes": smem.value}
+
+
+def gemm_run_fp4(h, M, N, K, fmt, A, lda, SA, B, ldb, SB, C, ldc, D, ldd, alpha, beta, out_dtype, stream) -> int:
+    """Block-scaled FP4 GEMM (fmt NVFP4 or MXFP4): A [M, K/2] and B transposed
+    [N, K/2] packed E2M1 bytes (lda, ldb in bytes), scales in the blocked
+    layout (see include/tpgemm.h)."""
+    return load_library().gemm_run_fp4(h, M, N, K, fmt, A, lda, SA, B, ldb, SB, C, ldc, D, ldd, alpha, beta,
+                                       out_dtype, stream)
+
+
+def gemm_fp4_scale_bytes(fmt: int, rows: int, K: int) -> int:
+    return load_library().gemm_fp4_scale_bytes(fmt, rows, K)
+
+
+def gemm_fp4_check_args(M, N, K, fmt, A, lda, SA, B, ldb, SB, C, ldc, D, ldd, beta, out_dtype) -> int:
+    return load_library().gemm_fp4_check_args(M, N, K, fmt, A, lda, SA, B, ldb, SB, C, ldc, D, ldd, beta,
+                                              out_dtype)
+
+
+def gemm_fp4_query_plan(h, fmt, M, N, K, out_dtype=OUT_BF16) -> dict:
+    tm, tn, grid, cl, smem = (ctypes.c_int() for _ in range(5))
+    tiles = ctypes.c_int64()
+    st = load_library().gemm_fp4_query_plan(h, fmt, M, N, K, out_dtype, ctypes.byref(tm), ctypes.byref(tn),
+                                            ctypes.byref(tiles), ctypes.byref(grid), ctypes.byref(cl),
+                                            ctypes.byref(smem))
+    if st != OK:
+        raise TpgemmError(st, "gemm_fp4_query_plan")
     return {"tile_m": tm.value, "tile_n": tn.value, "num_tiles": tiles.value, "grid": grid.value,
             "cluster": cl.value, "smem_bytes": smem.value}
 

@@ -23,7 +23,8 @@ INCLUDE = os.path.join(ROOT, "include")
 FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC",
          f"-I{INCLUDE}", f"-I{CSRC}"]
 
-UNITS = [("tpgemm.o", "tpgemm.cu", []), ("stream_inst.o", "stream_inst.cu", []), ("mx_inst.o", "mx_inst.cu", [])] + [
+UNITS = [("tpgemm.o", "tpgemm.cu", []), ("stream_inst.o", "stream_inst.cu", []), ("mx_inst.o", "mx_inst.cu", []),
+         ("fp4_nv.o", "fp4_inst.cu", ["-DTPG_FP4=1"]), ("fp4_mx.o", "fp4_inst.cu", ["-DTPG_FP4=2"])] + [
     (f"tiled_e{e}.o", "tiled_inst.cu", [f"-DTPG_EPI={e}"]) for e in range(6)] + [
     ("tiled_g0.o", "tiled_inst.cu", ["-DTPG_EPI=0", "-DTPG_GROUPED=1"])]
 

@@ -58,6 +58,20 @@
 // r / 32, byte c holds scale (r, c): row r's scale for MMA c of the K block.
 // For B tiles of 192 columns a tile may start 64 rows into a chunk; its scale
 // columns then start two TMEM columns into the copied pair of chunks.
+//
+// FP4 (kFmt = kFmtNvf4 or kFmtMxf4), the same page's NVFP4 and MXF4 GEMMs:
+// A and B hold E2M1 elements two to a byte (the even element in the low four
+// bits), so a 128-byte stage row is 256 elements and each of a stage's four
+// MMAs (kind::mxf4nvf4, K = 64) takes 32 bytes, the same descriptor steps as
+// FP8. NVFP4 scales every 16 elements with an E4M3 byte (scale_vec::4X: the
+// four bytes of a TMEM cell are the four scales of one MMA, one 512-byte chunk
+// per MMA and 128 rows); MXFP4 every 32 with an E8M0 byte (scale_vec::2X: one
+// chunk serves two MMAs, which take bytes 0-1 and 2-3 of each cell). Tiles are
+// 256 x 256 on CTA pairs or 128 x 128 on one CTA, so a tile's B scales are
+// whole row blocks, and the scale maps are rank 3 ([row block][chunk][128
+// words]): a stage's chunks arrive in one box per operand, and chunks past the
+// end of a row block (K not a multiple of the stage's 256 elements) or past the
+// last row block read as zero scales rather than the next row block's.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -86,6 +100,11 @@ struct MxParams {
 
 namespace mx {
 
+// Element and scale formats (the kernel's kFmt template argument).
+constexpr int kFmtMxf8 = 0; // FP8 elements, one E8M0 scale per 32 (kind::mxf8f6f4, scale_vec::1X)
+constexpr int kFmtNvf4 = 1; // packed E2M1, one E4M3 scale per 16 (kind::mxf4nvf4, scale_vec::4X)
+constexpr int kFmtMxf4 = 2; // packed E2M1, one E8M0 scale per 32 (kind::mxf4nvf4, scale_vec::2X)
+
 constexpr int BM = 128; // rows per CTA
 constexpr int BK = 128; // K elements (bytes) per stage: four MMAs of K = 32, four scale columns
 constexpr int THREADS = 224; // warps 0-5 as the bf16 kernel, warp 6 copies scales
@@ -99,23 +118,37 @@ constexpr uint32_t SF_TMEM_STRIDE = 16; // TMEM columns per stage: A at +0 (4), 
 // so a stage holds 8 or 4 KB of A instead of 16 and the ring one or two
 // stages more; the MMA still reads 128 rows, and the rows past the box (the
 // next stages' bytes) only reach accumulator rows that are never stored.
-template <int kBN, bool kPair, int kARows = 128>
+template <int kBN, bool kPair, int kARows = 128, int kFmt = kFmtMxf8>
 struct Layout {
-    static_assert(kPair ? kBN == 256 : (kBN == 128 || kBN == 192), "tile width");
-    static_assert(kARows == 128 || (!kPair && kBN == 192 && (kARows == 64 || kARows == 32)),
-                  "the small-M rings are 1-CTA, 192 wide");
+    static constexpr bool FP4 = kFmt != kFmtMxf8;
+    static_assert(kFmt == kFmtMxf8 || kFmt == kFmtNvf4 || kFmt == kFmtMxf4, "format");
+    static_assert(kPair ? kBN == 256 : (FP4 ? kBN == 128 : (kBN == 128 || kBN == 192)), "tile width");
+    static_assert(kARows == 128 || (!kPair && kBN == (FP4 ? 128 : 192) && (kARows == 64 || kARows == 32)),
+                  "the small-M rings are 1-CTA");
     static constexpr int CL = kPair ? 2 : 1;
+    // FP4: scale chunks per stage and row block (a stage is 256 elements of K:
+    // four NVFP4 chunks of 64, two MXFP4 chunks of 128), and row blocks of B's
+    // scales per tile.
+    static constexpr int CPS = kFmt == kFmtNvf4 ? 4 : 2;
+    static constexpr int NRB = kBN / 128;
     // Pair mode: one accumulator of 256 columns (two would fill TMEM and leave
     // no room for the scales), one epilogue staging buffer and 1.5 KB scale
-    // slots; six stages fit.
+    // slots; six stages fit (five with FP4's larger scale slots).
     static constexpr int ACCS = kPair ? 1 : 2;
-    static constexpr int STAGES = kPair ? 6 : (kARows == 32 ? 6 : (kARows == 64 ? 5 : (kBN == 192 ? 4 : 5)));
+    static constexpr int STAGES = FP4 ? (kPair ? 5 : (kARows == 32 ? 7 : (kARows == 64 ? 6 : 5)))
+                                      : (kPair ? 6 : (kARows == 32 ? 6 : (kARows == 64 ? 5 : (kBN == 192 ? 4 : 5))));
     static constexpr int EPI_BUFS = kPair ? 1 : 2;
     static constexpr uint32_t A_ROWS = kARows; // rows of A's box
     static constexpr uint32_t A_BYTES = A_ROWS * BK;
     static constexpr uint32_t B_ROWS = kBN / CL; // rows of B's transpose this CTA stages
     static constexpr uint32_t B_BYTES = B_ROWS * BK;
-    static constexpr uint32_t SF_BYTES = kPair ? 1536 : 2048; // A chunk at 0, B chunks at 512 and 1024
+    // FP8: A chunk at 0, B chunks at 512 and 1024 (and 1536 for 192-wide tiles
+    // that straddle two row blocks). FP4: A's chunks, then B's, row block by
+    // row block.
+    static constexpr uint32_t SF_BYTES = FP4 ? CPS * SF_CHUNK * (1 + NRB) : (kPair ? 1536 : 2048);
+    // TMEM columns per stage: FP8 A at +0 (4), B at +4 (8); FP4 four per chunk,
+    // A's CPS chunks first, then B's, the NRB row blocks of one chunk together.
+    static constexpr uint32_t SF_TSTRIDE = FP4 ? 4 * CPS * (1 + NRB) : SF_TMEM_STRIDE;
     static constexpr uint32_t OFF_A = 0;
     static constexpr uint32_t OFF_B = OFF_A + STAGES * A_BYTES;
     static_assert(OFF_A + (STAGES - 1) * A_BYTES + BM * BK <= OFF_B + STAGES * (kBN / CL) * BK,
@@ -130,10 +163,11 @@ struct Layout {
     static constexpr uint32_t OFF_MISC = OFF_BAR + NUM_BARS * 8;
     static constexpr uint32_t SMEM_BYTES = OFF_MISC + 16 + 1024;
     static constexpr uint32_t SF_COL0 = ACCS * kBN; // first TMEM column of the scale region
-    static_assert(SF_COL0 + STAGES * SF_TMEM_STRIDE <= TMEM_COLS, "TMEM overflow");
+    static_assert(SF_COL0 + STAGES * SF_TSTRIDE <= TMEM_COLS, "TMEM overflow");
     static_assert(SMEM_BYTES <= 232448, "exceeds the 227 KB shared-memory limit per CTA");
     static_assert(OFF_A % 1024 == 0 && OFF_B % 1024 == 0 && A_BYTES % 1024 == 0 && B_BYTES % 1024 == 0,
                   "128-byte swizzled operand stages start on 1024-byte boundaries");
+    static_assert(OFF_SF % 128 == 0 && SF_BYTES % 128 == 0, "scale boxes land on 128-byte boundaries");
 };
 
 __device__ __forceinline__ bool mx_drain_wait(uint64_t *bar, uint32_t parity, uint64_t limit_ns) {
@@ -153,13 +187,13 @@ __device__ __forceinline__ void mx_settle(uint64_t ns) {
     }
 }
 
-template <bool kOutF32, int kBN, bool kPair, int kARows = 128>
+template <bool kOutF32, int kBN, bool kPair, int kARows = 128, int kFmt = kFmtMxf8>
 __global__ void __launch_bounds__(THREADS, 1)
     gemm_mx_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmSB,
                    const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmD,
                    const MxParams p) {
-    using L = Layout<kBN, kPair, kARows>;
+    using L = Layout<kBN, kPair, kARows, kFmt>;
     constexpr int STAGES = L::STAGES;
     constexpr int CL = L::CL;
     constexpr int CHUNK = kOutF32 ? 32 : 64; // output columns per 128-byte staging row
@@ -245,9 +279,11 @@ __global__ void __launch_bounds__(THREADS, 1)
                 const int32_t m0 = arow * BM;
                 const int32_t n0 = w.n + static_cast<int32_t>(rank * L::B_ROWS);
                 const int32_t rb = w.n / 128; // B's first scale row block
-                // a 192-wide tile may reach into the next row block of B's scales
-                const bool two = kBN + (w.n % 128) > 128 && rb + 1 < p.sfb_rows;
-                const uint32_t tx = CL * (L::A_BYTES + L::B_BYTES + SF_CHUNK * (two ? 3u : 2u));
+                // a 192-wide FP8 tile may reach into the next row block of B's scales
+                const bool two = !L::FP4 && kBN + (w.n % 128) > 128 && rb + 1 < p.sfb_rows;
+                // FP4 scale boxes are whole (zero-filled past the ends), so always complete
+                const uint32_t tx = CL * (L::A_BYTES + L::B_BYTES +
+                                          (L::FP4 ? L::SF_BYTES : SF_CHUNK * (two ? 3u : 2u)));
                 const int32_t ca = static_cast<int32_t>(arow * p.sf_kc);
                 const int32_t cb = static_cast<int32_t>(rb * p.sf_kc);
                 for (int32_t kb = 0; kb < p.kb; ++kb) {
@@ -258,7 +294,24 @@ __global__ void __launch_bounds__(THREADS, 1)
                     uint8_t *adst = smem + L::OFF_A + stage * L::A_BYTES;
                     uint8_t *bdst = smem + L::OFF_B + stage * L::B_BYTES;
                     uint8_t *sf = smem + L::OFF_SF + stage * L::SF_BYTES;
-                    if constexpr (kPair) {
+                    if constexpr (L::FP4) {
+                        // this CTA's row block of A's scales; all of the tile's row blocks of B's
+                        const int32_t sc = kb * L::CPS;
+                        if constexpr (kPair) {
+                            if (rank == 0) mbar_arrive_expect_tx(&full[stage], tx);
+                            const uint32_t fb = full0 + stage * 8u;
+                            tma_load_2d_pair(&tmA, fb, adst, kb * BK, m0);
+                            tma_load_2d_pair(&tmB, fb, bdst, kb * BK, n0);
+                            tma_load_3d_pair(&tmSA, fb, sf, 0, sc, arow);
+                            tma_load_3d_pair(&tmSB, fb, sf + L::CPS * SF_CHUNK, 0, sc, rb);
+                        } else {
+                            mbar_arrive_expect_tx(&full[stage], tx);
+                            tma_load_2d(&tmA, &full[stage], adst, kb * BK, m0);
+                            tma_load_2d(&tmB, &full[stage], bdst, kb * BK, n0);
+                            tma_load_3d(&tmSA, &full[stage], sf, 0, sc, arow);
+                            tma_load_3d(&tmSB, &full[stage], sf + L::CPS * SF_CHUNK, 0, sc, rb);
+                        }
+                    } else if constexpr (kPair) {
                         if (rank == 0) mbar_arrive_expect_tx(&full[stage], tx);
                         const uint32_t fb = full0 + stage * 8u;
                         tma_load_2d_pair(&tmA, fb, adst, kb * BK, m0);
@@ -326,19 +379,35 @@ __global__ void __launch_bounds__(THREADS, 1)
                 const uint32_t d_tmem = tmem_base + acc * kBN;
                 // Issues the four MMAs of K block kb from the current stage and frees the stage.
                 auto issue = [&](int32_t kb) {
-                    const uint32_t sfa_t = tmem_base + L::SF_COL0 + stage * SF_TMEM_STRIDE;
-                    const uint32_t sfb_t = sfa_t + 4 + sfb_skip;
+                    const uint32_t sfa_t = tmem_base + L::SF_COL0 + stage * L::SF_TSTRIDE;
                     const uint64_t ad = adesc0 + stage * (L::A_BYTES >> 4);
                     const uint64_t bd = bdesc0 + stage * (L::B_BYTES >> 4);
+                    if constexpr (L::FP4) {
+                        const uint32_t sfb_t = sfa_t + 4 * L::CPS;
 #pragma unroll
-                    for (int kk = 0; kk < BK / 32; ++kk) {
-                        // K = 32 FP8 elements are 32 bytes: +2 in the descriptors' address field
-                        const uint32_t accumulate = (kb != 0 || kk != 0) ? 1u : 0u;
-                        const uint32_t idesc = p.idesc | idesc_mx_sf_ids(kk, kk);
-                        if constexpr (kPair)
-                            tc_mma_mxf8_pair(d_tmem, ad + kk * 2, bd + kk * 2, idesc, sfa_t, sfb_t, accumulate);
-                        else
-                            tc_mma_mxf8(d_tmem, ad + kk * 2, bd + kk * 2, idesc, sfa_t, sfb_t, accumulate);
+                        for (int kk = 0; kk < 4; ++kk) {
+                            // K = 64 FP4 elements are 32 bytes: +2 in the descriptors' address field.
+                            // NVFP4: chunk kk, all four bytes; MXFP4: chunk kk / 2, bytes 2 (kk % 2) and up.
+                            const uint32_t accumulate = (kb != 0 || kk != 0) ? 1u : 0u;
+                            const uint32_t g = kFmt == kFmtNvf4 ? kk : kk / 2;
+                            const uint32_t id = kFmt == kFmtNvf4 ? 0u : 2u * (kk % 2);
+                            const uint32_t idesc = p.idesc | idesc_mx_sf_ids(id, id);
+                            const uint32_t sfa = sfa_t + 4 * g, sfb = sfb_t + 4 * L::NRB * g;
+                            tc_mma_fp4<kPair, kFmt == kFmtNvf4>(d_tmem, ad + kk * 2, bd + kk * 2, idesc, sfa, sfb,
+                                                              accumulate);
+                        }
+                    } else {
+                        const uint32_t sfb_t = sfa_t + 4 + sfb_skip;
+#pragma unroll
+                        for (int kk = 0; kk < BK / 32; ++kk) {
+                            // K = 32 FP8 elements are 32 bytes: +2 in the descriptors' address field
+                            const uint32_t accumulate = (kb != 0 || kk != 0) ? 1u : 0u;
+                            const uint32_t idesc = p.idesc | idesc_mx_sf_ids(kk, kk);
+                            if constexpr (kPair)
+                                tc_mma_mxf8_pair(d_tmem, ad + kk * 2, bd + kk * 2, idesc, sfa_t, sfb_t, accumulate);
+                            else
+                                tc_mma_mxf8(d_tmem, ad + kk * 2, bd + kk * 2, idesc, sfa_t, sfb_t, accumulate);
+                        }
                     }
                     any = true;
                     if constexpr (kPair)
@@ -405,9 +474,37 @@ __global__ void __launch_bounds__(THREADS, 1)
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t sfa_t = tmem_base + L::SF_COL0 + stage * SF_TMEM_STRIDE;
+                    const uint32_t sfa_t = tmem_base + L::SF_COL0 + stage * L::SF_TSTRIDE;
                     const uint64_t sd = sdesc0 + stage * (L::SF_BYTES >> 4);
-                    if constexpr (kPair) {
+                    if constexpr (L::FP4) {
+                        // A's chunk j to column 4j; B's chunk j of row block r to
+                        // 4 CPS + 4 (NRB j + r), so that one MMA's B scales are NRB * 4
+                        // consecutive columns, row r of the tile in column r / 32.
+#pragma unroll
+                        for (int j = 0; j < L::CPS; ++j) {
+                            const uint64_t src = sd + ((j * SF_CHUNK) >> 4);
+                            if constexpr (kPair)
+                                tc_cp_32x128b_x4_pair(sfa_t + 4 * j, src);
+                            else
+                                tc_cp_32x128b_x4(sfa_t + 4 * j, src);
+                        }
+#pragma unroll
+                        for (int r = 0; r < L::NRB; ++r) {
+#pragma unroll
+                            for (int j = 0; j < L::CPS; ++j) {
+                                const uint64_t src = sd + ((((1 + r) * L::CPS + j) * SF_CHUNK) >> 4);
+                                const uint32_t dst = sfa_t + 4 * L::CPS + 4 * (L::NRB * j + r);
+                                if constexpr (kPair)
+                                    tc_cp_32x128b_x4_pair(dst, src);
+                                else
+                                    tc_cp_32x128b_x4(dst, src);
+                            }
+                        }
+                        if constexpr (kPair)
+                            tc_commit_pair_mc(&sfready[stage], 0x1);
+                        else
+                            tc_commit(&sfready[stage]);
+                    } else if constexpr (kPair) {
                         tc_cp_32x128b_x4_pair(sfa_t, sd);
                         tc_cp_32x128b_x4_pair(sfa_t + 4, sd + (SF_CHUNK >> 4));
                         tc_cp_32x128b_x4_pair(sfa_t + 8, sd + (2 * SF_CHUNK >> 4));

@@ -1,6 +1,7 @@
 // Kernel launch helpers and the interface between the host library
 // (tpgemm.cu) and the translation units that instantiate the GEMM kernels
-// (tiled_inst.cu, once per fused-epilogue mode, and stream_inst.cu). Only
+// (tiled_inst.cu, once per fused-epilogue mode, stream_inst.cu, mx_inst.cu and
+// fp4_inst.cu, once per FP4 format). Only
 // those units name kernel instantiations, so each instantiation is compiled
 // once, and the units build in parallel.
 #pragma once
@@ -77,9 +78,9 @@ struct StreamLaunch {
 
 struct MxLaunch {
     int grid;   // CTAs (twice the pairs in pair mode)
-    int tile_n; // 128 or 192
-    bool pair;    // 256 x 192 tiles on CTA pairs
-    int a_rows;   // rows of A's box: 128, or 64 / 32 for M <= 64 / 32 on 1-CTA 192-wide tiles
+    int tile_n; // 1-CTA tiles: 128 or 192 (FP8), 128 (FP4); 256 on pairs
+    bool pair;    // 256 x 256 tiles on CTA pairs
+    int a_rows;   // rows of A's box: 128, or 64 / 32 for M <= 64 / 32 on 1-CTA tiles (192-wide FP8, FP4)
     bool f32;
     cudaStream_t stream;
     const CUtensorMap *a, *b, *sa, *sb, *c, *d;
@@ -92,6 +93,16 @@ bool mx_set_limits();
 int mx_smem_bytes(int tile_n, bool pair, int a_rows);
 // co-resident CTA pairs of the MX kernel's pair mode, or -1
 int mx_pair_clusters(bool f32, int num_sms);
+
+// fp4_inst.cu, one set per FP4 format: _nv (NVFP4) and _mx (MXFP4)
+cudaError_t fp4_launch_nv(const MxLaunch &l);
+cudaError_t fp4_launch_mx(const MxLaunch &l);
+bool fp4_set_limits_nv();
+bool fp4_set_limits_mx();
+int fp4_smem_bytes_nv(bool pair, int a_rows);
+int fp4_smem_bytes_mx(bool pair, int a_rows);
+int fp4_pair_clusters_nv(bool f32, int num_sms);
+int fp4_pair_clusters_mx(bool f32, int num_sms);
 
 // tiled_inst.cu, one definition per mode E (compiled with -DTPG_EPI=E).
 cudaError_t tiled_launch_e0(const TiledLaunch &l);

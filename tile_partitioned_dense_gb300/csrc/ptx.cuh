@@ -656,6 +656,41 @@ __device__ __forceinline__ void tc_mma_mxf8_pair(uint32_t d_tmem, uint64_t a_des
         : "memory");
 }
 
+// D[tmem] (+)= (A scaled) * (B scaled), kind::mxf4nvf4 (packed E2M1 A and B,
+// K = 64): with kNv, scale_vec::4X, four scales per row per MMA (one per 16
+// elements), the four bytes of each TMEM scale cell; else scale_vec::2X, two
+// per row (one per 32 elements), the two bytes from the scale-factor ID on.
+// The scale format (E4M3 or E8M0) is bit 23 of idesc. kPair: the CTA-pair
+// form, issued by one thread of the even CTA.
+template <bool kPair, bool kNv>
+__device__ __forceinline__ void tc_mma_fp4(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                           uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+    if constexpr (kPair && kNv)
+        asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
+                     "tcgen05.mma.cta_group::2.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], [%5], p;"
+                     "\n\t}\n" ::"r"(d_tmem),
+                     "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+                     : "memory");
+    else if constexpr (kPair)
+        asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
+                     "tcgen05.mma.cta_group::2.kind::mxf4nvf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%4], [%5], p;"
+                     "\n\t}\n" ::"r"(d_tmem),
+                     "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+                     : "memory");
+    else if constexpr (kNv)
+        asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
+                     "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], [%5], p;"
+                     "\n\t}\n" ::"r"(d_tmem),
+                     "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+                     : "memory");
+    else
+        asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
+                     "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%4], [%5], p;"
+                     "\n\t}\n" ::"r"(d_tmem),
+                     "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+                     : "memory");
+}
+
 // Instruction descriptor of a block-scaled MMA, kind::mxf8f6f4, both operands
 // K-major, E8M0 scales:
 //   bits 4-5 B scale-factor ID, bits 7-9 A format and 10-12 B format (0 E4M3,
@@ -663,6 +698,11 @@ __device__ __forceinline__ void tc_mma_mxf8_pair(uint32_t d_tmem, uint64_t a_des
 //   M >> 4, bits 29-30 A scale-factor ID.
 __host__ __device__ constexpr uint32_t make_idesc_mxf8(uint32_t m, uint32_t n, uint32_t a_fmt, uint32_t b_fmt) {
     return (a_fmt << 7) | (b_fmt << 10) | ((n >> 3) << 17) | (1u << 23) | ((m >> 4) << 24);
+}
+// kind::mxf4nvf4: both operands E2M1 (format 1) and K-major; the scale format
+// bit is 0 for E4M3 (NVFP4) and 1 for E8M0 (MXFP4).
+__host__ __device__ constexpr uint32_t make_idesc_fp4(uint32_t m, uint32_t n, bool e8m0_scales) {
+    return (1u << 7) | (1u << 10) | ((n >> 3) << 17) | ((e8m0_scales ? 1u : 0u) << 23) | ((m >> 4) << 24);
 }
 __host__ __device__ constexpr uint32_t idesc_mx_sf_ids(uint32_t a_id, uint32_t b_id) {
     return (b_id << 4) | (a_id << 29);

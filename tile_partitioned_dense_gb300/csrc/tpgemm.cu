@@ -90,6 +90,8 @@ struct tpgemm_handle {
     std::atomic<int> ks_clusters[2][2] = {};
     // co-resident CTA pairs of the MX kernel's pair mode, per [out f32]
     std::atomic<int> mx_pairs[2] = {};
+    // the same for its FP4 forms, per [format][out f32]
+    std::atomic<int> fp4_pairs[2][2] = {};
     // Caller-owned workspace (gemm_set_workspace), or null, and the tag of the
     // latest call that may use it.
     void *ws = nullptr;
@@ -432,6 +434,8 @@ bool set_smem_limits() {
     ok = tpg::tiled_set_limits_e5() && ok;
     ok = tpg::stream_set_limits() && ok;
     ok = tpg::mx_set_limits() && ok;
+    ok = tpg::fp4_set_limits_nv() && ok;
+    ok = tpg::fp4_set_limits_mx() && ok;
     return ok;
 }
 
@@ -1193,6 +1197,205 @@ int gemm_mx_query_plan(tpgemm_handle *h, int64_t M, int64_t N, int64_t K, int ou
     if (grid) *grid = pl.grid;
     if (cluster) *cluster = pl.pair ? 2 : 1;
     if (smem_bytes) *smem_bytes = tpg::mx_smem_bytes(pl.tile_n, pl.pair, pl.a_rows);
+    return TPGEMM_OK;
+}
+
+} // extern "C"
+
+// ---------------------------------------------------------------------------
+// Block-scaled FP4 GEMM (gemm_run_fp4): the MX kernel with packed E2M1
+// operands, NVFP4 or MXFP4 scales.
+namespace {
+
+int64_t fp4_block(int format) { return format == TPGEMM_NVFP4 ? 16 : 32; }
+
+// Scale chunks (128 rows x 4 scale columns) per row block: one per 64
+// elements of K (NVFP4) or per 128 (MXFP4).
+int64_t fp4_chunks_per_row_block(int format, int64_t K) {
+    const int64_t span = 4 * fp4_block(format);
+    return (K + span - 1) / span;
+}
+
+int64_t fp4_scale_bytes(int format, int64_t rows, int64_t K) {
+    return ((rows + 127) / 128) * fp4_chunks_per_row_block(format, K) * 512;
+}
+
+int fp4_pairs_for(tpgemm_handle *h, int format, bool f32) {
+    std::atomic<int> &slot = h->fp4_pairs[format == TPGEMM_NVFP4 ? 0 : 1][f32 ? 1 : 0];
+    const int cached = slot.load(std::memory_order_relaxed);
+    if (cached > 0) return cached;
+    const int n = format == TPGEMM_NVFP4 ? tpg::fp4_pair_clusters_nv(f32, h->num_sms)
+                                         : tpg::fp4_pair_clusters_mx(f32, h->num_sms);
+    const int v = n > 0 ? n : h->num_sms / 2;
+    slot.store(v, std::memory_order_relaxed);
+    return v;
+}
+
+// As mx_plan, with 128 x 128 tiles on single CTAs: an FP4 tile's B scales are
+// then whole row blocks of 128, and two 128-column accumulators leave TMEM
+// room for a stage's 32 scale columns.
+MxPlan fp4_plan(tpgemm_handle *h, int format, int64_t M, int64_t N, bool f32) {
+    MxPlan pl;
+    pl.pair = mx_pair(M, N);
+    pl.tile_n = pl.pair ? kMxPairTileN : 128;
+    pl.a_rows = pl.pair ? 128 : (M <= 32 ? 32 : (M <= 64 ? 64 : 128));
+    pl.tile_m = tpg::mx::BM * (pl.pair ? 2 : 1);
+    pl.mt = (M + pl.tile_m - 1) / pl.tile_m;
+    pl.nt = (N + pl.tile_n - 1) / pl.tile_n;
+    const int64_t cap = pl.pair ? fp4_pairs_for(h, format, f32) : h->num_sms;
+    pl.sched = tpg::make_schedule(pl.mt, pl.nt, pl.pair ? kGroupMPair : kGroupM, cap, 1, 0.5);
+    pl.grid = static_cast<int>(pl.sched.workers * (pl.pair ? 2 : 1));
+    return pl;
+}
+
+// One operand's FP4 scales as [row block][chunk][128 words]; a box is `chunks`
+// chunks of `row_blocks` row blocks, and chunks past either end read as zeros.
+int encode_fp4_scales(tpgemm_handle *h, CUtensorMap *map, const void *ptr, int64_t rows, int64_t kc,
+                      uint32_t chunks, uint32_t row_blocks) {
+    cuuint64_t dims[3] = {128, static_cast<cuuint64_t>(kc), static_cast<cuuint64_t>((rows + 127) / 128)};
+    cuuint64_t strides[2] = {512, static_cast<cuuint64_t>(kc * 512)};
+    cuuint32_t box[3] = {128, chunks, row_blocks};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = h->encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, const_cast<void *>(ptr), dims, strides, box, estr,
+                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? TPGEMM_OK : TPGEMM_ERR_CUDA;
+}
+
+} // namespace
+
+extern "C" {
+
+int64_t gemm_fp4_scale_bytes(int format, int64_t rows, int64_t K) {
+    if ((format != TPGEMM_NVFP4 && format != TPGEMM_MXFP4) || rows < 0 || K < 0) return TPGEMM_ERR_INVALID_ARG;
+    return fp4_scale_bytes(format, rows, K);
+}
+
+int gemm_fp4_check_args(int64_t M, int64_t N, int64_t K, int format, const void *A, int64_t lda, const void *SA,
+                        const void *B, int64_t ldb, const void *SB, const void *C, int64_t ldc, const void *D,
+                        int64_t ldd, float beta, int out_dtype) {
+    if (out_dtype != TPGEMM_OUT_BF16 && out_dtype != TPGEMM_OUT_F32) return TPGEMM_ERR_INVALID_ARG;
+    if (format != TPGEMM_NVFP4 && format != TPGEMM_MXFP4) return TPGEMM_ERR_INVALID_ARG;
+    if (M < 0 || N < 0 || K < 0 || K % fp4_block(format) != 0) return TPGEMM_ERR_INVALID_ARG;
+    if (M > kMaxDim || N > kMaxDim || K > kMaxDim) return TPGEMM_ERR_TOO_LARGE;
+    if (M == 0 || N == 0) return TPGEMM_OK;
+    // the kernel addresses scale chunks and row blocks with 32-bit coordinates
+    if (fp4_scale_bytes(format, M, K) / 512 > kMaxDim || fp4_scale_bytes(format, N, K) / 512 > kMaxDim)
+        return TPGEMM_ERR_TOO_LARGE;
+    const int64_t elt = out_dtype == TPGEMM_OUT_F32 ? 4 : 2;
+    const int64_t row_bytes = K / 2;
+    const bool use_c = beta != 0.0f;
+    if (!D || ldd < N) return TPGEMM_ERR_INVALID_ARG;
+    if (K > 0 && (!A || !B || !SA || !SB || lda < row_bytes || ldb < row_bytes)) return TPGEMM_ERR_INVALID_ARG;
+    if (use_c && (!C || ldc < N)) return TPGEMM_ERR_INVALID_ARG;
+    if (ldd > kMaxDim * 8 || (K > 0 && (lda > kMaxDim * 16 || ldb > kMaxDim * 16)) || (use_c && ldc > kMaxDim * 8))
+        return TPGEMM_ERR_TOO_LARGE;
+    if (!aligned16(D) || (M > 1 && (ldd * elt) % 16 != 0)) return TPGEMM_ERR_ALIGNMENT;
+    if (K > 0) {
+        if (!aligned16(A) || !aligned16(B) || !aligned16(SA) || !aligned16(SB)) return TPGEMM_ERR_ALIGNMENT;
+        if ((M > 1 && lda % 16 != 0) || (N > 1 && ldb % 16 != 0)) return TPGEMM_ERR_ALIGNMENT;
+    }
+    if (use_c && (!aligned16(C) || (M > 1 && (ldc * elt) % 16 != 0))) return TPGEMM_ERR_ALIGNMENT;
+    const Range rd = byte_range(D, M, N, ldd, elt);
+    if (K > 0) {
+        const Range rsa{reinterpret_cast<uintptr_t>(SA), reinterpret_cast<uintptr_t>(SA) +
+                                                             static_cast<uintptr_t>(fp4_scale_bytes(format, M, K))};
+        const Range rsb{reinterpret_cast<uintptr_t>(SB), reinterpret_cast<uintptr_t>(SB) +
+                                                             static_cast<uintptr_t>(fp4_scale_bytes(format, N, K))};
+        if (overlaps(rd, byte_range(A, M, row_bytes, lda, 1)) || overlaps(rd, byte_range(B, N, row_bytes, ldb, 1)) ||
+            overlaps(rd, rsa) || overlaps(rd, rsb))
+            return TPGEMM_ERR_OVERLAP;
+    }
+    if (use_c && !(C == D && ldc == ldd) && overlaps(rd, byte_range(C, M, N, ldc, elt))) return TPGEMM_ERR_OVERLAP;
+    return TPGEMM_OK;
+}
+
+int gemm_run_fp4(tpgemm_handle *h, int64_t M, int64_t N, int64_t K, int format, const void *A, int64_t lda,
+                 const void *SA, const void *B, int64_t ldb, const void *SB, const void *C, int64_t ldc, void *D,
+                 int64_t ldd, float alpha, float beta, int out_dtype, void *stream_ptr) {
+    if (!h) return TPGEMM_ERR_INVALID_ARG;
+    const int chk =
+        gemm_fp4_check_args(M, N, K, format, A, lda, SA, B, ldb, SB, C, ldc, D, ldd, beta, out_dtype);
+    if (chk != TPGEMM_OK || M == 0 || N == 0) return chk;
+    const bool f32 = out_dtype == TPGEMM_OUT_F32;
+    const int64_t elt = f32 ? 4 : 2;
+    const bool use_c = beta != 0.0f;
+    DeviceGuard guard(h->device);
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+    if (K == 0) {
+        int64_t blocks = (M * N + 1023) / 1024;
+        if (blocks > 8LL * h->num_sms) blocks = 8LL * h->num_sms;
+        const int32_t m = static_cast<int32_t>(M), n = static_cast<int32_t>(N);
+        const tpg::EpiParams none{};
+        const void *c = use_c ? C : nullptr;
+        return f32 ? launch(tpg::epilogue_only_kernel<true, false>, static_cast<int>(blocks), 256, 0, 1, stream, m, n,
+                            beta, c, ldc, D, ldd, none)
+                   : launch(tpg::epilogue_only_kernel<false, false>, static_cast<int>(blocks), 256, 0, 1, stream, m,
+                            n, beta, c, ldc, D, ldd, none);
+    }
+    const MxPlan pl = fp4_plan(h, format, M, N, f32);
+    const int tile_n = pl.tile_n;
+    const uint32_t chunk = f32 ? 32u : 64u;
+    const int64_t cell = 16 / elt;
+    const int64_t n_tma = N / cell * cell;
+    const uint64_t map_n = static_cast<uint64_t>(n_tma > 0 ? n_tma : N);
+    const int64_t row_bytes = K / 2;
+    const int64_t kc = fp4_chunks_per_row_block(format, K);
+    // chunks per 256-element stage: four of 64 elements (NVFP4), two of 128 (MXFP4)
+    const uint32_t cps = format == TPGEMM_NVFP4 ? 4u : 2u;
+    const CUtensorMapDataType out_dt = f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    CUtensorMap tmA, tmB, tmSA, tmSB, tmC, tmD;
+    if (encode_2d(h, &tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, A, row_bytes, M, tma_stride(M, row_bytes, lda, 1), 128,
+                  static_cast<uint32_t>(pl.a_rows)) ||
+        encode_2d(h, &tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, B, row_bytes, N, tma_stride(N, row_bytes, ldb, 1), 128,
+                  static_cast<uint32_t>(pl.pair ? tile_n / 2 : tile_n)) ||
+        encode_fp4_scales(h, &tmSA, SA, M, kc, cps, 1) ||
+        encode_fp4_scales(h, &tmSB, SB, N, kc, cps, static_cast<uint32_t>(tile_n / 128)) ||
+        encode_2d(h, &tmD, out_dt, D, map_n, M, tma_stride(M, N, ldd, elt), chunk, 128) ||
+        encode_2d(h, &tmC, out_dt, use_c ? C : D, map_n, M,
+                  use_c ? tma_stride(M, N, ldc, elt) : tma_stride(M, N, ldd, elt), chunk, 128))
+        return TPGEMM_ERR_CUDA;
+    tpg::MxParams p{};
+    p.M = static_cast<int32_t>(M);
+    p.N = static_cast<int32_t>(N);
+    p.K = static_cast<int32_t>(K);
+    // a stage is 128 bytes of a row: 256 elements
+    p.kb = static_cast<int32_t>((K + 255) / 256);
+    p.sched = pl.sched;
+    p.n_tma = static_cast<int32_t>(n_tma);
+    p.sfb_rows = static_cast<int32_t>((N + 127) / 128);
+    p.sf_kc = static_cast<int32_t>(kc);
+    p.idesc = tpg::make_idesc_fp4(static_cast<uint32_t>(pl.tile_m), static_cast<uint32_t>(tile_n),
+                                  format == TPGEMM_MXFP4);
+    p.alpha = alpha;
+    p.beta = beta;
+    p.C = use_c ? C : nullptr;
+    p.ldc = ldc;
+    p.D = D;
+    p.ldd = ldd;
+    p.status = h->status;
+    p.timeout_ns = h->timeout_ns;
+    const tpg::MxLaunch l{pl.grid, tile_n, pl.pair, pl.a_rows, f32, stream, &tmA, &tmB, &tmSA, &tmSB, &tmC, &tmD, &p};
+    const cudaError_t e = format == TPGEMM_NVFP4 ? tpg::fp4_launch_nv(l) : tpg::fp4_launch_mx(l);
+    return e == cudaSuccess ? TPGEMM_OK : TPGEMM_ERR_CUDA;
+}
+
+int gemm_fp4_query_plan(tpgemm_handle *h, int format, int64_t M, int64_t N, int64_t K, int out_dtype, int *tile_m,
+                        int *tile_n, int64_t *num_tiles, int *grid, int *cluster, int *smem_bytes) {
+    if (!h || M < 0 || N < 0 || K < 0) return TPGEMM_ERR_INVALID_ARG;
+    if (format != TPGEMM_NVFP4 && format != TPGEMM_MXFP4) return TPGEMM_ERR_INVALID_ARG;
+    if (out_dtype != TPGEMM_OUT_BF16 && out_dtype != TPGEMM_OUT_F32) return TPGEMM_ERR_INVALID_ARG;
+    if (M > kMaxDim || N > kMaxDim || K > kMaxDim) return TPGEMM_ERR_TOO_LARGE;
+    DeviceGuard guard(h->device);
+    const MxPlan pl = fp4_plan(h, format, M, N, out_dtype == TPGEMM_OUT_F32);
+    if (tile_m) *tile_m = pl.tile_m;
+    if (tile_n) *tile_n = pl.tile_n;
+    if (num_tiles) *num_tiles = pl.mt * pl.nt;
+    if (grid) *grid = pl.grid;
+    if (cluster) *cluster = pl.pair ? 2 : 1;
+    if (smem_bytes)
+        *smem_bytes = format == TPGEMM_NVFP4 ? tpg::fp4_smem_bytes_nv(pl.pair, pl.a_rows)
+                                             : tpg::fp4_smem_bytes_mx(pl.pair, pl.a_rows);
     return TPGEMM_OK;
 }
 

@@ -208,16 +208,122 @@ def make_mx_inputs(M: int, N: int, K: int, seed: int, integer: bool = False, fmt
     return padded(A, lda), sa, padded(Bt, ldb), sb
 
 
-def mx_blocked_scales(S) -> "np.ndarray":
-    """Scale codes [R, K/32] (row-major) rearranged into the blocked layout
-    gemm_run_mx takes: 512-byte chunks of 128 rows x 4 scale columns in (row
-    block, column block) order, the scale of row r, column c of a chunk at
-    byte (r % 32) * 16 + (r / 32) * 4 + c. Padding rows and columns hold 127
-    (a scale of 1). A permutation of bytes, nothing else."""
+def mx_blocked_scales(S, pad: int = 127) -> "np.ndarray":
+    """Scale codes [R, K/block] (row-major) rearranged into the blocked layout
+    gemm_run_mx and gemm_run_fp4 take: 512-byte chunks of 128 rows x 4 scale
+    columns in (row block, column block) order, the scale of row r, column c of
+    a chunk at byte (r % 32) * 16 + (r / 32) * 4 + c. Padding rows and columns
+    hold `pad` (127, a scale of 1 in E8M0; 0x38 is 1 in E4M3). A permutation of
+    bytes, nothing else."""
     import numpy as np
     S = np.asarray(S, dtype=np.uint8)
     R, nb = S.shape
     rbs, kc = -(-R // 128), -(-nb // 4)
-    P = np.full((rbs * 128, kc * 4), 127, dtype=np.uint8)
+    P = np.full((rbs * 128, kc * 4), pad, dtype=np.uint8)
     P[:R, :nb] = S
     return np.ascontiguousarray(P.reshape(rbs, 4, 32, kc, 4).transpose(0, 3, 2, 1, 4).reshape(-1))
+
+
+# ---------------------------------------------------------------- FP4 (NVFP4, MXFP4)
+
+FP4_NV, FP4_MX = 0, 1  # the library's TPGEMM_NVFP4 and TPGEMM_MXFP4
+FP4_BLOCK = {FP4_NV: 16, FP4_MX: 32}
+E4M3_ONE = 0x38  # 1.0 as an E4M3 scale code (padding of NVFP4 scale layouts)
+
+
+@dataclasses.dataclass(frozen=True)
+class Fp4Config:
+    name: str
+    fmt: int
+    M: int
+    N: int
+    K: int
+    seed: int
+    description: str
+
+    @property
+    def flops(self) -> int:
+        return 2 * self.M * self.N * self.K
+
+
+FP4_CONFIGS = {
+    "nvfp4_decode": Fp4Config("nvfp4_decode", FP4_NV, 16, 28672, 4096, 15,
+                              "NVFP4 decode projection 16x28672x4096, E4M3 scales per 16, bf16 output"),
+    "nvfp4_m256": Fp4Config("nvfp4_m256", FP4_NV, 256, 28672, 4096, 16,
+                            "NVFP4 GEMM with 256 rows 256x28672x4096, E4M3 scales per 16, bf16 output"),
+    "nvfp4_qkv": Fp4Config("nvfp4_qkv", FP4_NV, 8192, 6144, 4096, 17,
+                           "NVFP4 QKV projection 8192x6144x4096, E4M3 scales per 16, bf16 output"),
+}
+
+# magnitudes of the eight E2M1 codes 0..7 (the sign is bit 3)
+_E2M1_MAG = (0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0)
+
+
+def _e2m1_codes(x: torch.Tensor) -> torch.Tensor:
+    """Nearest E2M1 code of each value (magnitudes clamped to 6; ties go to the
+    smaller magnitude), as uint8 codes 0..15."""
+    grid = torch.tensor(_E2M1_MAG, dtype=torch.float32)
+    mids = (grid[1:] + grid[:-1]) / 2
+    mag = torch.bucketize(x.abs().clamp(max=6.0), mids, right=False).to(torch.uint8)
+    sign = ((x < 0) & (mag != 0)).to(torch.uint8) << 3
+    return mag | sign
+
+
+def _pack_fp4(codes: torch.Tensor) -> torch.Tensor:
+    """[R, K] codes 0..15 -> [R, K/2] bytes, the even element in the low nibble."""
+    return (codes[:, 0::2] | (codes[:, 1::2] << 4)).contiguous()
+
+
+def make_fp4_inputs(M: int, N: int, K: int, seed: int, fmt: int = FP4_NV, integer: bool = False,
+                    lda: int | None = None, ldb: int | None = None):
+    """Seeded FP4 inputs as uint8 CPU tensors: A [M, K/2] and Bt [N, K/2]
+    packed E2M1 codes (B transposed; the even element in the low nibble), SA
+    [M, K/block] and SB [N, K/block] scale codes (E4M3 for NVFP4, E8M0 for
+    MXFP4), row-major; lda / ldb (bytes) > K/2 give padded rows whose padding
+    holds 0xFF.
+
+    integer=True: uniformly random codes (all sixteen, -0 included) with scales
+    of 1/2, 1 and 2, so every partial sum of the product is exact in fp32 (for
+    K up to 7281). Otherwise N(0,1) data quantised the usual way: per block,
+    the scale is the block's largest magnitude over 6 (NVFP4: rounded to
+    E4M3; MXFP4: the power of two at or above it) and each element the nearest
+    E2M1 value of data / scale."""
+    block = FP4_BLOCK[fmt]
+    if K % block:
+        raise ValueError(f"K must be a multiple of {block}")
+    gen = torch.Generator(device="cpu")
+    gen.manual_seed(seed)
+
+    def one(rows):
+        if integer:
+            codes = torch.randint(0, 16, (rows, K), generator=gen).to(torch.uint8)
+            if fmt == FP4_NV:
+                s = torch.tensor([0x30, 0x38, 0x40], dtype=torch.uint8)[
+                    torch.randint(0, 3, (rows, K // block), generator=gen)]
+            else:
+                s = torch.randint(126, 129, (rows, K // block), generator=gen).to(torch.uint8)
+            return _pack_fp4(codes), s
+        x = torch.randn((rows, K), generator=gen)
+        amax = x.view(rows, K // block, block).abs().amax(dim=2).clamp(min=1e-30)
+        if fmt == FP4_NV:
+            sc = (amax / 6.0).clamp(min=2.0 ** -9).to(torch.float8_e4m3fn)  # never a zero scale
+            s = sc.view(torch.uint8).clone()
+            scale = sc.to(torch.float32)
+        else:
+            e = torch.ceil(torch.log2(amax / 6.0)).clamp(-127, 127)
+            s = (e + 127).to(torch.uint8)
+            scale = torch.exp2(e)
+        q = x / scale.repeat_interleave(block, dim=1)
+        return _pack_fp4(_e2m1_codes(q)), s
+
+    A, SA = one(M)
+    Bt, SB = one(N)
+
+    def padded(x, ld):
+        if ld is None or ld == x.shape[1]:
+            return x
+        base = torch.full((x.shape[0], ld), 0xFF, dtype=torch.uint8)
+        base[:, :x.shape[1]] = x
+        return base[:, :x.shape[1]]
+
+    return padded(A, lda), SA, padded(Bt, ldb), SB
