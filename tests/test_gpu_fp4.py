@@ -81,13 +81,15 @@ def _want(fmt, A, SA, Bt, SB, C, alpha, beta, out_dtype, rows=None):
     return D
 
 
-# (M, N, K, lda, ldb), strides in bytes: two pair tiles; ragged everything
-# with K = 96 (part of one stage, a partial scale chunk) and N = 200 on pairs
-# whose second CTA owns rows past M; single CTAs with 128-row A boxes (N <=
-# 128, two row tiles); many pair tiles in both directions, N ragged; a pair
-# whose second CTA has one row, N odd (the column tail goes around the tensor
-# map); M <= 32 and M <= 64 on 32- and 64-row A boxes; 128-row boxes for M in
-# (64, 128]; one tile with a long K.
+# (M, N, K, lda, ldb), strides in bytes: 256 x 192 pair tiles with a ragged
+# last one; ragged everything with K = 96 (part of one stage, a partial scale
+# chunk) and N = 200 on 256 x 256 pairs whose second CTA owns rows past M;
+# single CTAs with 128 x 128 tiles (N <= 128, two row tiles); many 256 x 256
+# pair tiles, N ragged; 256 x 192 pairs whose second CTA has one row, N odd
+# (the column tail goes around the tensor map, and the last tile starts 64
+# rows into a scale row block); M <= 32 and M <= 64 on 128 x 192 tiles with
+# 32- and 64-row A boxes; 128-row boxes for M in (64, 128]; one 128 x 128 tile
+# with a long K.
 SHAPES = [(256, 512, 512, None, None), (300, 200, 96, 64, 48), (200, 100, 320, 176, 160),
           (640, 1000, 1024, None, 528), (129, 577, 160, 96, 80), (16, 1000, 512, None, None),
           (33, 600, 192, None, None), (64, 577, 160, 96, 80), (100, 300, 256, None, None),
@@ -214,11 +216,15 @@ def test_fp4_plan(h):
         p = tpd.gemm_fp4_query_plan(h, fmt, 8192, 6144, 4096)
         assert p["tile_m"] == 256 and p["tile_n"] == 256 and p["num_tiles"] == 32 * 24 and p["cluster"] == 2
         assert p["grid"] % 2 == 0 and sms - 8 <= p["grid"] <= sms
-        p = tpd.gemm_fp4_query_plan(h, fmt, 16, 28672, 4096)  # 128 rows or fewer: single CTAs
-        assert p["tile_m"] == 128 and p["tile_n"] == 128 and p["cluster"] == 1 and p["num_tiles"] == 224
+        p = tpd.gemm_fp4_query_plan(h, fmt, 256, 28672, 4096)  # up to 256 rows: 256 x 192 pairs, 150 tiles
+        assert p["tile_m"] == 256 and p["tile_n"] == 192 and p["cluster"] == 2 and p["num_tiles"] == 150
+        p = tpd.gemm_fp4_query_plan(h, fmt, 16, 28672, 4096)  # 128 rows or fewer: single CTAs, one wave
+        assert p["tile_m"] == 128 and p["tile_n"] == 192 and p["cluster"] == 1 and p["num_tiles"] == 150
         sizes = {p["smem_bytes"]}
         for m in (64, 100):  # 64-row A boxes, then 128-row ones: each its own ring
             p = tpd.gemm_fp4_query_plan(h, fmt, m, 28672, 4096)
-            assert p["tile_n"] == 128 and p["smem_bytes"] not in sizes
+            assert p["tile_n"] == 192 and p["smem_bytes"] not in sizes
             sizes.add(p["smem_bytes"])
+        p = tpd.gemm_fp4_query_plan(h, fmt, 100, 128, 4096)  # N <= 128: 128 x 128 tiles
+        assert p["tile_n"] == 128 and p["num_tiles"] == 1
         assert max(sizes) <= 232448

@@ -39,7 +39,11 @@
 //               quarters, into both CTAs' TMEM in pair mode) and commits them
 //               to the stage's scales-ready barrier. Keeping the copies off the
 //               MMA thread leaves that thread four MMAs, one wait and one
-//               commit per stage.
+//               commit per stage. FP4 stages hold three or four times as
+//               many chunks, so warps 6 and 7 share them: each copies the
+//               chunks of two of the four MMAs and signals its own barrier,
+//               and the MMA thread issues each pair of MMAs once its half of
+//               the scales is in.
 //   warp 1      allocates TMEM (fp32 accumulators of kBN columns, two or, for
 //               pairs, one, and per ring stage 4 scale columns for A and 8 for
 //               B); one lane (of
@@ -67,11 +71,13 @@
 // four bytes of a TMEM cell are the four scales of one MMA, one 512-byte chunk
 // per MMA and 128 rows); MXFP4 every 32 with an E8M0 byte (scale_vec::2X: one
 // chunk serves two MMAs, which take bytes 0-1 and 2-3 of each cell). Tiles are
-// 256 x 256 on CTA pairs or 128 x 128 on one CTA, so a tile's B scales are
-// whole row blocks, and the scale maps are rank 3 ([row block][chunk][128
-// words]): a stage's chunks arrive in one box per operand, and chunks past the
-// end of a row block (K not a multiple of the stage's 256 elements) or past the
-// last row block read as zero scales rather than the next row block's.
+// 256 x 256 or 256 x 192 on CTA pairs, 128 x 192 or 128 x 128 on one CTA; a
+// tile's B scales are the one or two row blocks of 128 it reaches (a 192-wide
+// tile starts 0 or 64 rows into the first). The scale maps are rank 3 ([row
+// block][chunk][128 words]): a stage's chunks arrive in one box per operand,
+// and chunks past the end of a row block (K not a multiple of the stage's 256
+// elements) or past the last row block read as zero scales rather than the
+// next row block's. 192-wide FP4 tiles have one accumulator, as pairs do.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -107,7 +113,6 @@ constexpr int kFmtMxf4 = 2; // packed E2M1, one E8M0 scale per 32 (kind::mxf4nvf
 
 constexpr int BM = 128; // rows per CTA
 constexpr int BK = 128; // K elements (bytes) per stage: four MMAs of K = 32, four scale columns
-constexpr int THREADS = 224; // warps 0-5 as the bf16 kernel, warp 6 copies scales
 constexpr int EPI_THREADS = 128;
 constexpr uint32_t SF_CHUNK = 512;
 constexpr uint32_t EPI_BUF_BYTES = BM * 128;
@@ -122,22 +127,25 @@ template <int kBN, bool kPair, int kARows = 128, int kFmt = kFmtMxf8>
 struct Layout {
     static constexpr bool FP4 = kFmt != kFmtMxf8;
     static_assert(kFmt == kFmtMxf8 || kFmt == kFmtNvf4 || kFmt == kFmtMxf4, "format");
-    static_assert(kPair ? kBN == 256 : (FP4 ? kBN == 128 : (kBN == 128 || kBN == 192)), "tile width");
-    static_assert(kARows == 128 || (!kPair && kBN == (FP4 ? 128 : 192) && (kARows == 64 || kARows == 32)),
-                  "the small-M rings are 1-CTA");
+    static_assert(kPair ? (kBN == 256 || (FP4 && kBN == 192)) : (kBN == 128 || kBN == 192), "tile width");
+    static_assert(kARows == 128 || (!kPair && kBN == 192 && (kARows == 64 || kARows == 32)),
+                  "the small-M rings are 1-CTA, 192 wide");
     static constexpr int CL = kPair ? 2 : 1;
     // FP4: scale chunks per stage and row block (a stage is 256 elements of K:
     // four NVFP4 chunks of 64, two MXFP4 chunks of 128), and row blocks of B's
-    // scales per tile.
+    // scales a tile reaches (a 192-wide tile starts 0 or 64 rows into one and
+    // ends in the next).
     static constexpr int CPS = kFmt == kFmtNvf4 ? 4 : 2;
-    static constexpr int NRB = kBN / 128;
-    // Pair mode: one accumulator of 256 columns (two would fill TMEM and leave
-    // no room for the scales), one epilogue staging buffer and 1.5 KB scale
-    // slots; six stages fit (five with FP4's larger scale slots).
-    static constexpr int ACCS = kPair ? 1 : 2;
-    static constexpr int STAGES = FP4 ? (kPair ? 5 : (kARows == 32 ? 7 : (kARows == 64 ? 6 : 5)))
-                                      : (kPair ? 6 : (kARows == 32 ? 6 : (kARows == 64 ? 5 : (kBN == 192 ? 4 : 5))));
-    static constexpr int EPI_BUFS = kPair ? 1 : 2;
+    static constexpr int NRB = kBN == 128 ? 1 : 2;
+    // One accumulator in pair mode (two of 256 columns would fill TMEM and
+    // leave no room for the scales) and for FP4's 192-wide tiles (two would
+    // leave room for two stages of scales); then one epilogue staging buffer.
+    static constexpr int ACCS = (kPair || (FP4 && kBN == 192)) ? 1 : 2;
+    static constexpr int STAGES =
+        FP4 ? (kPair ? (kBN == 256 ? 5 : 6)
+                     : (kBN == 128 ? 5 : (kARows == 32 ? 6 : (kARows == 64 ? 5 : 4))))
+            : (kPair ? 6 : (kARows == 32 ? 6 : (kARows == 64 ? 5 : (kBN == 192 ? 4 : 5))));
+    static constexpr int EPI_BUFS = ACCS == 1 ? 1 : 2;
     static constexpr uint32_t A_ROWS = kARows; // rows of A's box
     static constexpr uint32_t A_BYTES = A_ROWS * BK;
     static constexpr uint32_t B_ROWS = kBN / CL; // rows of B's transpose this CTA stages
@@ -159,7 +167,14 @@ struct Layout {
     static constexpr uint32_t OFF_EPI = (OFF_SF + STAGES * SF_BYTES + 1023) / 1024 * 1024;
     static constexpr uint32_t OFF_BAR = OFF_EPI + EPI_BUFS * EPI_BUF_BYTES;
     // full, empty, scales ready, tfull, tempty, c, drain, scale-copy drain
-    static constexpr uint32_t NUM_BARS = 3 * STAGES + 2 + 2 + 2 + 2;
+    // FP4 splits a stage's scale copies over two warps, each with its own
+    // scales-ready barrier: the first copies the chunks of MMAs 0 and 1, the
+    // second those of MMAs 2 and 3, and the MMAs of each half start as soon
+    // as their scales are in.
+    static constexpr int COPIERS = FP4 ? 2 : 1;
+    static constexpr int THREADS = (6 + COPIERS) * 32;
+    // full, empty, scales ready (per copier), tfull, tempty, c, drain, scale-copy drain (per copier)
+    static constexpr uint32_t NUM_BARS = (2 + COPIERS) * STAGES + 2 + 2 + 2 + 1 + COPIERS;
     static constexpr uint32_t OFF_MISC = OFF_BAR + NUM_BARS * 8;
     static constexpr uint32_t SMEM_BYTES = OFF_MISC + 16 + 1024;
     static constexpr uint32_t SF_COL0 = ACCS * kBN; // first TMEM column of the scale region
@@ -188,7 +203,7 @@ __device__ __forceinline__ void mx_settle(uint64_t ns) {
 }
 
 template <bool kOutF32, int kBN, bool kPair, int kARows = 128, int kFmt = kFmtMxf8>
-__global__ void __launch_bounds__(THREADS, 1)
+__global__ void __launch_bounds__(Layout<kBN, kPair, kARows, kFmt>::THREADS, 1)
     gemm_mx_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmSB,
                    const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmD,
@@ -204,8 +219,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::OFF_BAR);
     uint64_t *full = bars;
     uint64_t *empty = bars + STAGES;
-    uint64_t *sfready = bars + 2 * STAGES;
-    uint64_t *tfull = bars + 3 * STAGES;
+    uint64_t *sfready = bars + 2 * STAGES; // copier c's barrier of stage s: sfready[c * STAGES + s]
+    uint64_t *tfull = bars + (2 + L::COPIERS) * STAGES;
     uint64_t *tempty = tfull + 2;
     uint64_t *cbar = tempty + 2;
     uint64_t *drain = cbar + 2;
@@ -223,7 +238,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
-            mbar_init(&sfready[s], 1);
+            for (int c = 0; c < L::COPIERS; ++c) mbar_init(&sfready[c * STAGES + s], 1);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&tfull[b], 1);
@@ -232,7 +247,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             mbar_init(&cbar[b], 1);
         }
         mbar_init(drain, 1);
-        mbar_init(sfdrain, 1);
+        for (int c = 0; c < L::COPIERS; ++c) mbar_init(&sfdrain[c], 1);
         *abort_flag = 0u;
         fence_barrier_init();
     }
@@ -377,37 +392,21 @@ __global__ void __launch_bounds__(THREADS, 1)
                 }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + acc * kBN;
-                // Issues the four MMAs of K block kb from the current stage and frees the stage.
+                // FP8: issues the four MMAs of K block kb from the current stage and frees the stage.
                 auto issue = [&](int32_t kb) {
                     const uint32_t sfa_t = tmem_base + L::SF_COL0 + stage * L::SF_TSTRIDE;
+                    const uint32_t sfb_t = sfa_t + 4 + sfb_skip;
                     const uint64_t ad = adesc0 + stage * (L::A_BYTES >> 4);
                     const uint64_t bd = bdesc0 + stage * (L::B_BYTES >> 4);
-                    if constexpr (L::FP4) {
-                        const uint32_t sfb_t = sfa_t + 4 * L::CPS;
 #pragma unroll
-                        for (int kk = 0; kk < 4; ++kk) {
-                            // K = 64 FP4 elements are 32 bytes: +2 in the descriptors' address field.
-                            // NVFP4: chunk kk, all four bytes; MXFP4: chunk kk / 2, bytes 2 (kk % 2) and up.
-                            const uint32_t accumulate = (kb != 0 || kk != 0) ? 1u : 0u;
-                            const uint32_t g = kFmt == kFmtNvf4 ? kk : kk / 2;
-                            const uint32_t id = kFmt == kFmtNvf4 ? 0u : 2u * (kk % 2);
-                            const uint32_t idesc = p.idesc | idesc_mx_sf_ids(id, id);
-                            const uint32_t sfa = sfa_t + 4 * g, sfb = sfb_t + 4 * L::NRB * g;
-                            tc_mma_fp4<kPair, kFmt == kFmtNvf4>(d_tmem, ad + kk * 2, bd + kk * 2, idesc, sfa, sfb,
-                                                              accumulate);
-                        }
-                    } else {
-                        const uint32_t sfb_t = sfa_t + 4 + sfb_skip;
-#pragma unroll
-                        for (int kk = 0; kk < BK / 32; ++kk) {
-                            // K = 32 FP8 elements are 32 bytes: +2 in the descriptors' address field
-                            const uint32_t accumulate = (kb != 0 || kk != 0) ? 1u : 0u;
-                            const uint32_t idesc = p.idesc | idesc_mx_sf_ids(kk, kk);
-                            if constexpr (kPair)
-                                tc_mma_mxf8_pair(d_tmem, ad + kk * 2, bd + kk * 2, idesc, sfa_t, sfb_t, accumulate);
-                            else
-                                tc_mma_mxf8(d_tmem, ad + kk * 2, bd + kk * 2, idesc, sfa_t, sfb_t, accumulate);
-                        }
+                    for (int kk = 0; kk < BK / 32; ++kk) {
+                        // K = 32 FP8 elements are 32 bytes: +2 in the descriptors' address field
+                        const uint32_t accumulate = (kb != 0 || kk != 0) ? 1u : 0u;
+                        const uint32_t idesc = p.idesc | idesc_mx_sf_ids(kk, kk);
+                        if constexpr (kPair)
+                            tc_mma_mxf8_pair(d_tmem, ad + kk * 2, bd + kk * 2, idesc, sfa_t, sfb_t, accumulate);
+                        else
+                            tc_mma_mxf8(d_tmem, ad + kk * 2, bd + kk * 2, idesc, sfa_t, sfb_t, accumulate);
                     }
                     any = true;
                     if constexpr (kPair)
@@ -419,20 +418,63 @@ __global__ void __launch_bounds__(THREADS, 1)
                         phase ^= 1u;
                     }
                 };
-                for (int32_t kb = 0; kb < p.kb;) {
-                    // Wait until the stage's operands have landed and its scales are in
-                    // TMEM, and test the next stage in the same breath: when both are
-                    // ready, one wait serves two K blocks.
-                    const uint32_t nstage = stage + 1 == STAGES ? 0u : stage + 1;
-                    const uint32_t nphase = stage + 1 == STAGES ? phase ^ 1u : phase;
-                    const uint32_t st2 = mbar_try_wait_and_test(ready_a + stage * 8u, phase, ready_a + nstage * 8u, nphase);
-                    if (!(st2 & 1u) && !mbar_wait(&sfready[stage], phase, ctl, kStatusTimeoutMma)) {
-                        ok = false;
-                        break;
+                if constexpr (L::FP4) {
+                    for (int32_t kb = 0; kb < p.kb && ok; ++kb) {
+                        const uint32_t sfa_t = tmem_base + L::SF_COL0 + stage * L::SF_TSTRIDE;
+                        // a 192-wide tile's B scales start (w.n % 128) / 32 columns into each MMA's group
+                        const uint32_t sfb_t = sfa_t + 4 * L::CPS + sfb_skip;
+                        const uint64_t ad = adesc0 + stage * (L::A_BYTES >> 4);
+                        const uint64_t bd = bdesc0 + stage * (L::B_BYTES >> 4);
+#pragma unroll
+                        for (int half = 0; half < 2; ++half) {
+                            // the operands have landed and this half's scales are in TMEM
+                            if (!mbar_wait(&sfready[half * STAGES + stage], phase, ctl, kStatusTimeoutMma)) {
+                                ok = false;
+                                break;
+                            }
+                            tc_fence_after();
+#pragma unroll
+                            for (int k2 = 0; k2 < 2; ++k2) {
+                                // K = 64 FP4 elements are 32 bytes: +2 in the descriptors' address
+                                // field. NVFP4: chunk kk, all four bytes; MXFP4: chunk kk / 2,
+                                // bytes 2 (kk % 2) and up.
+                                const int kk = 2 * half + k2;
+                                const uint32_t accumulate = (kb != 0 || kk != 0) ? 1u : 0u;
+                                const uint32_t g = kFmt == kFmtNvf4 ? kk : kk / 2;
+                                const uint32_t id = kFmt == kFmtNvf4 ? 0u : 2u * (kk % 2);
+                                const uint32_t idesc = p.idesc | idesc_mx_sf_ids(id, id);
+                                tc_mma_fp4<kPair, kFmt == kFmtNvf4>(d_tmem, ad + kk * 2, bd + kk * 2, idesc,
+                                                                  sfa_t + 4 * g, sfb_t + 4 * L::NRB * g, accumulate);
+                            }
+                            any = true;
+                        }
+                        if (!ok) break;
+                        if constexpr (kPair)
+                            tc_commit_pair_mc_addr(empty_a + stage * 8u, 0x3);
+                        else
+                            tc_commit_addr(empty_a + stage * 8u);
+                        if (++stage == STAGES) {
+                            stage = 0;
+                            phase ^= 1u;
+                        }
                     }
-                    tc_fence_after();
-                    issue(kb++);
-                    if ((st2 & 2u) && kb < p.kb) issue(kb++);
+                } else {
+                    for (int32_t kb = 0; kb < p.kb;) {
+                        // Wait until the stage's operands have landed and its scales are in
+                        // TMEM, and test the next stage in the same breath: when both are
+                        // ready, one wait serves two K blocks.
+                        const uint32_t nstage = stage + 1 == STAGES ? 0u : stage + 1;
+                        const uint32_t nphase = stage + 1 == STAGES ? phase ^ 1u : phase;
+                        const uint32_t st2 =
+                            mbar_try_wait_and_test(ready_a + stage * 8u, phase, ready_a + nstage * 8u, nphase);
+                        if (!(st2 & 1u) && !mbar_wait(&sfready[stage], phase, ctl, kStatusTimeoutMma)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        issue(kb++);
+                        if ((st2 & 2u) && kb < p.kb) issue(kb++);
+                    }
                 }
                 if (!ok) break;
                 if constexpr (kPair)
@@ -454,12 +496,14 @@ __global__ void __launch_bounds__(THREADS, 1)
             }
         }
         __syncwarp();
-    } else if (warp == 6) {
+    } else if (warp >= 6) {
         // ------------------------------------------------ scale copies into TMEM (even CTA)
+        const int cw = static_cast<int>(warp) - 6; // copier index
         if (lane == 0 && rank == 0) {
             // a scale chunk: 32 rows of 16 bytes, groups of 8 rows 128 bytes apart
             const uint64_t sdesc0 = make_smem_desc_plain(smem_addr(smem + L::OFF_SF), 512, 128);
             const uint32_t full_a = smem_addr(full);
+            uint64_t *ready = sfready + cw * STAGES;
             uint32_t stage = 0, phase = 0;
             bool ok = true;
             bool any = false;
@@ -479,41 +523,40 @@ __global__ void __launch_bounds__(THREADS, 1)
                     if constexpr (L::FP4) {
                         // A's chunk j to column 4j; B's chunk j of row block r to
                         // 4 CPS + 4 (NRB j + r), so that one MMA's B scales are NRB * 4
-                        // consecutive columns, row r of the tile in column r / 32.
+                        // consecutive columns, row r of the tile in column r / 32. Copier
+                        // cw takes chunks [cw CPS / 2, (cw + 1) CPS / 2): those of MMAs
+                        // 2 cw and 2 cw + 1.
 #pragma unroll
-                        for (int j = 0; j < L::CPS; ++j) {
+                        for (int j = cw * L::CPS / 2; j < (cw + 1) * L::CPS / 2; ++j) {
                             const uint64_t src = sd + ((j * SF_CHUNK) >> 4);
                             if constexpr (kPair)
                                 tc_cp_32x128b_x4_pair(sfa_t + 4 * j, src);
                             else
                                 tc_cp_32x128b_x4(sfa_t + 4 * j, src);
-                        }
 #pragma unroll
-                        for (int r = 0; r < L::NRB; ++r) {
-#pragma unroll
-                            for (int j = 0; j < L::CPS; ++j) {
-                                const uint64_t src = sd + ((((1 + r) * L::CPS + j) * SF_CHUNK) >> 4);
+                            for (int r = 0; r < L::NRB; ++r) {
+                                const uint64_t srcb = sd + ((((1 + r) * L::CPS + j) * SF_CHUNK) >> 4);
                                 const uint32_t dst = sfa_t + 4 * L::CPS + 4 * (L::NRB * j + r);
                                 if constexpr (kPair)
-                                    tc_cp_32x128b_x4_pair(dst, src);
+                                    tc_cp_32x128b_x4_pair(dst, srcb);
                                 else
-                                    tc_cp_32x128b_x4(dst, src);
+                                    tc_cp_32x128b_x4(dst, srcb);
                             }
                         }
                         if constexpr (kPair)
-                            tc_commit_pair_mc(&sfready[stage], 0x1);
+                            tc_commit_pair_mc(&ready[stage], 0x1);
                         else
-                            tc_commit(&sfready[stage]);
+                            tc_commit(&ready[stage]);
                     } else if constexpr (kPair) {
                         tc_cp_32x128b_x4_pair(sfa_t, sd);
                         tc_cp_32x128b_x4_pair(sfa_t + 4, sd + (SF_CHUNK >> 4));
                         tc_cp_32x128b_x4_pair(sfa_t + 8, sd + (2 * SF_CHUNK >> 4));
-                        tc_commit_pair_mc(&sfready[stage], 0x1);
+                        tc_commit_pair_mc(&ready[stage], 0x1);
                     } else {
                         tc_cp_32x128b_x4(sfa_t, sd);
                         tc_cp_32x128b_x4(sfa_t + 4, sd + (SF_CHUNK >> 4));
                         if constexpr (kBN > 128) tc_cp_32x128b_x4(sfa_t + 8, sd + (2 * SF_CHUNK >> 4));
-                        tc_commit(&sfready[stage]);
+                        tc_commit(&ready[stage]);
                     }
                     any = true;
                     if (++stage == STAGES) {
@@ -525,10 +568,11 @@ __global__ void __launch_bounds__(THREADS, 1)
             if (!ok && any) {
                 // Wait for every copy issued so far before TMEM is freed.
                 if constexpr (kPair)
-                    tc_commit_pair_mc(sfdrain, 0x1);
+                    tc_commit_pair_mc(&sfdrain[cw], 0x1);
                 else
-                    tc_commit(sfdrain);
-                if (!mx_drain_wait(sfdrain, 0, p.timeout_ns) && p.status) atomicOr(p.status, kStatusTimeoutDrain);
+                    tc_commit(&sfdrain[cw]);
+                if (!mx_drain_wait(&sfdrain[cw], 0, p.timeout_ns) && p.status)
+                    atomicOr(p.status, kStatusTimeoutDrain);
             }
         }
         __syncwarp();
@@ -569,12 +613,12 @@ __global__ void __launch_bounds__(THREADS, 1)
                 }
             };
             if (nchunks == 0) release();
-            if constexpr (kPair && !kOutF32) {
+            if constexpr (L::ACCS == 1 && !kOutF32) {
                 if (!has_beta && p.n_tma == p.N) {
-                    // One accumulator per pair: the next tile's MMAs wait until this
-                    // one is read. So read all 256 columns first, packed to bf16 in
-                    // registers (alpha applied, one rounding), hand the accumulator
-                    // back, and only then stage and store the chunks.
+                    // One accumulator: the next tile's MMAs wait until this one is
+                    // read. So read all kBN columns first, packed to bf16 in registers
+                    // (alpha applied, one rounding), hand the accumulator back, and
+                    // only then stage and store the chunks.
                     uint32_t packed[kBN / 2];
 #pragma unroll
                     for (int g = 0; g < kBN / 32; ++g) {

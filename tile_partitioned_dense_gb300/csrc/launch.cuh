@@ -78,9 +78,9 @@ struct StreamLaunch {
 
 struct MxLaunch {
     int grid;   // CTAs (twice the pairs in pair mode)
-    int tile_n; // 1-CTA tiles: 128 or 192 (FP8), 128 (FP4); 256 on pairs
-    bool pair;    // 256 x 256 tiles on CTA pairs
-    int a_rows;   // rows of A's box: 128, or 64 / 32 for M <= 64 / 32 on 1-CTA tiles (192-wide FP8, FP4)
+    int tile_n; // 1-CTA tiles: 128 or 192; on pairs 256 (and 192 for FP4)
+    bool pair;    // 256-row tiles on CTA pairs
+    int a_rows;   // rows of A's box: 128, or 64 / 32 for M <= 64 / 32 on 1-CTA 192-wide tiles
     bool f32;
     cudaStream_t stream;
     const CUtensorMap *a, *b, *sa, *sb, *c, *d;
@@ -99,8 +99,8 @@ cudaError_t fp4_launch_nv(const MxLaunch &l);
 cudaError_t fp4_launch_mx(const MxLaunch &l);
 bool fp4_set_limits_nv();
 bool fp4_set_limits_mx();
-int fp4_smem_bytes_nv(bool pair, int a_rows);
-int fp4_smem_bytes_mx(bool pair, int a_rows);
+int fp4_smem_bytes_nv(int tile_n, bool pair, int a_rows);
+int fp4_smem_bytes_mx(int tile_n, bool pair, int a_rows);
 int fp4_pair_clusters_nv(bool f32, int num_sms);
 int fp4_pair_clusters_mx(bool f32, int num_sms);
 

@@ -14,7 +14,7 @@ bool set_limit() {
 }
 template <bool kOutF32, int kBN, bool kPair, int kARows = 128>
 cudaError_t launch_one(const MxLaunch &l) {
-    return launch_ex(mx::gemm_mx_kernel<kOutF32, kBN, kPair, kARows>, l.grid, mx::THREADS,
+    return launch_ex(mx::gemm_mx_kernel<kOutF32, kBN, kPair, kARows>, l.grid, mx::Layout<kBN, kPair, kARows>::THREADS,
                      static_cast<int>(mx::Layout<kBN, kPair, kARows>::SMEM_BYTES), kPair ? 2 : 1, true, l.stream,
                      *l.a, *l.b, *l.sa, *l.sb, *l.c, *l.d, *l.p);
 }
@@ -59,7 +59,7 @@ int mx_smem_bytes(int tile_n, bool pair, int a_rows) {
 int mx_pair_clusters(bool f32, int num_sms) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(2 * (num_sms / 2)), 1, 1);
-    cfg.blockDim = dim3(mx::THREADS, 1, 1);
+    cfg.blockDim = dim3(mx::Layout<256, true>::THREADS, 1, 1);
     cfg.dynamicSmemBytes = mx::Layout<256, true>::SMEM_BYTES;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;

@@ -1231,14 +1231,15 @@ int fp4_pairs_for(tpgemm_handle *h, int format, bool f32) {
     return v;
 }
 
-// As mx_plan, with 128 x 128 tiles on single CTAs: an FP4 tile's B scales are
-// then whole row blocks of 128, and two 128-column accumulators leave TMEM
-// room for a stage's 32 scale columns.
+// As mx_plan. FP4 moves half the bytes of FP8 per MMA, so up to 256 rows the
+// GEMM is bound by reading B, and the tiles are chosen to cover the SMs in
+// whole waves: 256 x 192 on pairs (256 x 256 above 256 rows, where the MMAs'
+// width pays), 128 x 192 on single CTAs (128 x 128 when N <= 128).
 MxPlan fp4_plan(tpgemm_handle *h, int format, int64_t M, int64_t N, bool f32) {
     MxPlan pl;
     pl.pair = mx_pair(M, N);
-    pl.tile_n = pl.pair ? kMxPairTileN : 128;
-    pl.a_rows = pl.pair ? 128 : (M <= 32 ? 32 : (M <= 64 ? 64 : 128));
+    pl.tile_n = pl.pair ? (M <= 256 ? 192 : kMxPairTileN) : (N > 128 ? 192 : 128);
+    pl.a_rows = (!pl.pair && pl.tile_n == 192) ? (M <= 32 ? 32 : (M <= 64 ? 64 : 128)) : 128;
     pl.tile_m = tpg::mx::BM * (pl.pair ? 2 : 1);
     pl.mt = (M + pl.tile_m - 1) / pl.tile_m;
     pl.nt = (N + pl.tile_n - 1) / pl.tile_n;
@@ -1350,7 +1351,7 @@ int gemm_run_fp4(tpgemm_handle *h, int64_t M, int64_t N, int64_t K, int format, 
         encode_2d(h, &tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, B, row_bytes, N, tma_stride(N, row_bytes, ldb, 1), 128,
                   static_cast<uint32_t>(pl.pair ? tile_n / 2 : tile_n)) ||
         encode_fp4_scales(h, &tmSA, SA, M, kc, cps, 1) ||
-        encode_fp4_scales(h, &tmSB, SB, N, kc, cps, static_cast<uint32_t>(tile_n / 128)) ||
+        encode_fp4_scales(h, &tmSB, SB, N, kc, cps, tile_n == 128 ? 1u : 2u) ||
         encode_2d(h, &tmD, out_dt, D, map_n, M, tma_stride(M, N, ldd, elt), chunk, 128) ||
         encode_2d(h, &tmC, out_dt, use_c ? C : D, map_n, M,
                   use_c ? tma_stride(M, N, ldc, elt) : tma_stride(M, N, ldd, elt), chunk, 128))
@@ -1394,8 +1395,8 @@ int gemm_fp4_query_plan(tpgemm_handle *h, int format, int64_t M, int64_t N, int6
     if (grid) *grid = pl.grid;
     if (cluster) *cluster = pl.pair ? 2 : 1;
     if (smem_bytes)
-        *smem_bytes = format == TPGEMM_NVFP4 ? tpg::fp4_smem_bytes_nv(pl.pair, pl.a_rows)
-                                             : tpg::fp4_smem_bytes_mx(pl.pair, pl.a_rows);
+        *smem_bytes = format == TPGEMM_NVFP4 ? tpg::fp4_smem_bytes_nv(pl.tile_n, pl.pair, pl.a_rows)
+                                             : tpg::fp4_smem_bytes_mx(pl.tile_n, pl.pair, pl.a_rows);
     return TPGEMM_OK;
 }
 
