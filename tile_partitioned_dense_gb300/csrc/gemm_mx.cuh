@@ -32,9 +32,11 @@
 //               bytes), both K-major with 128-byte swizzle, plus the K block's
 //               scale chunks: 512 bytes for the CTA's 128 rows of A and one or
 //               two for the tile's rows of B (all of them, in both CTAs of a
-//               pair), copied as they are from the caller's blocked layout.
-//   warp 6      scale copier (even CTA): once a stage has landed, one lane
-//               copies its scale chunks into the stage's TMEM scale columns
+//               pair), copied as they are from the caller's blocked layout. The
+//               scale chunks are issued first and complete on a barrier of
+//               their own, so they reach TMEM while the operands are in flight.
+//   warp 6      scale copier (even CTA): once a stage's scales have landed,
+//               one lane copies its scale chunks into the stage's TMEM scale columns
 //               (tcgen05.cp, 32 lanes x 16 bytes, repeated in all four lane
 //               quarters, into both CTAs' TMEM in pair mode) and commits them
 //               to the stage's scales-ready barrier. Keeping the copies off the
@@ -46,10 +48,10 @@
 //               the scales is in.
 //   warp 1      allocates TMEM (fp32 accumulators of kBN columns, two or, for
 //               pairs, one, and per ring stage 4 scale columns for A and 8 for
-//               B); one lane (of
-//               the even CTA) issues the four K = 32 MMAs of a stage once its
-//               scales are in TMEM, scale byte j of each TMEM cell going with
-//               MMA j; tcgen05.commit frees the stage (in both CTAs).
+//               B); one lane (of the even CTA) issues the four K = 32 MMAs of a
+//               stage once its operands have landed and its scales are in TMEM,
+//               scale byte j of each TMEM cell going with MMA j; tcgen05.commit
+//               frees the stage (in both CTAs).
 //   warps 2-5   epilogue, as in the bf16 kernel: TMEM -> registers -> alpha,
 //               beta*C -> one rounding -> swizzled staging -> TMA store, each
 //               CTA its own 128 rows.
@@ -173,8 +175,9 @@ struct Layout {
     // as their scales are in.
     static constexpr int COPIERS = FP4 ? 2 : 1;
     static constexpr int THREADS = (6 + COPIERS) * 32;
-    // full, empty, scales ready (per copier), tfull, tempty, c, drain, scale-copy drain (per copier)
-    static constexpr uint32_t NUM_BARS = (2 + COPIERS) * STAGES + 2 + 2 + 2 + 1 + COPIERS;
+    // full (operands), empty, scales landed, scales ready (per copier), tfull,
+    // tempty, c, drain, scale-copy drain (per copier)
+    static constexpr uint32_t NUM_BARS = (3 + COPIERS) * STAGES + 2 + 2 + 2 + 1 + COPIERS;
     static constexpr uint32_t OFF_MISC = OFF_BAR + NUM_BARS * 8;
     static constexpr uint32_t SMEM_BYTES = OFF_MISC + 16 + 1024;
     static constexpr uint32_t SF_COL0 = ACCS * kBN; // first TMEM column of the scale region
@@ -219,8 +222,9 @@ __global__ void __launch_bounds__(Layout<kBN, kPair, kARows, kFmt>::THREADS, 1)
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::OFF_BAR);
     uint64_t *full = bars;
     uint64_t *empty = bars + STAGES;
-    uint64_t *sfready = bars + 2 * STAGES; // copier c's barrier of stage s: sfready[c * STAGES + s]
-    uint64_t *tfull = bars + (2 + L::COPIERS) * STAGES;
+    uint64_t *sffull = bars + 2 * STAGES;  // a stage's scale chunks have landed
+    uint64_t *sfready = bars + 3 * STAGES; // copier c's barrier of stage s: sfready[c * STAGES + s]
+    uint64_t *tfull = bars + (3 + L::COPIERS) * STAGES;
     uint64_t *tempty = tfull + 2;
     uint64_t *cbar = tempty + 2;
     uint64_t *drain = cbar + 2;
@@ -238,6 +242,7 @@ __global__ void __launch_bounds__(Layout<kBN, kPair, kARows, kFmt>::THREADS, 1)
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
+            mbar_init(&sffull[s], 1);
             for (int c = 0; c < L::COPIERS; ++c) mbar_init(&sfready[c * STAGES + s], 1);
         }
         for (int b = 0; b < 2; ++b) {
@@ -283,8 +288,11 @@ __global__ void __launch_bounds__(Layout<kBN, kPair, kARows, kFmt>::THREADS, 1)
     if (warp == 0) {
         // ------------------------------------------------ TMA producer (both CTAs)
         if (lane == 0) {
-            // In pair mode both CTAs' loads complete on the even CTA's barrier.
+            // In pair mode both CTAs' loads complete on the even CTA's barriers.
+            // A stage's scale chunks go first, on their own barrier, so that the
+            // copier can move them into TMEM while the operands are in flight.
             const uint32_t full0 = kPair ? map_to_rank(smem_addr(full), 0) : 0u;
+            const uint32_t sffull0 = kPair ? map_to_rank(smem_addr(sffull), 0) : 0u;
             uint32_t stage = 0, phase = 0;
             int64_t issued = 0;
             bool ok = true;
@@ -297,8 +305,8 @@ __global__ void __launch_bounds__(Layout<kBN, kPair, kARows, kFmt>::THREADS, 1)
                 // a 192-wide FP8 tile may reach into the next row block of B's scales
                 const bool two = !L::FP4 && kBN + (w.n % 128) > 128 && rb + 1 < p.sfb_rows;
                 // FP4 scale boxes are whole (zero-filled past the ends), so always complete
-                const uint32_t tx = CL * (L::A_BYTES + L::B_BYTES +
-                                          (L::FP4 ? L::SF_BYTES : SF_CHUNK * (two ? 3u : 2u)));
+                const uint32_t sf_tx = CL * (L::FP4 ? L::SF_BYTES : SF_CHUNK * (two ? 3u : 2u));
+                const uint32_t tx = CL * (L::A_BYTES + L::B_BYTES);
                 const int32_t ca = static_cast<int32_t>(arow * p.sf_kc);
                 const int32_t cb = static_cast<int32_t>(rb * p.sf_kc);
                 for (int32_t kb = 0; kb < p.kb; ++kb) {
@@ -309,39 +317,42 @@ __global__ void __launch_bounds__(Layout<kBN, kPair, kARows, kFmt>::THREADS, 1)
                     uint8_t *adst = smem + L::OFF_A + stage * L::A_BYTES;
                     uint8_t *bdst = smem + L::OFF_B + stage * L::B_BYTES;
                     uint8_t *sf = smem + L::OFF_SF + stage * L::SF_BYTES;
-                    if constexpr (L::FP4) {
-                        // this CTA's row block of A's scales; all of the tile's row blocks of B's
-                        const int32_t sc = kb * L::CPS;
-                        if constexpr (kPair) {
-                            if (rank == 0) mbar_arrive_expect_tx(&full[stage], tx);
-                            const uint32_t fb = full0 + stage * 8u;
-                            tma_load_2d_pair(&tmA, fb, adst, kb * BK, m0);
-                            tma_load_2d_pair(&tmB, fb, bdst, kb * BK, n0);
-                            tma_load_3d_pair(&tmSA, fb, sf, 0, sc, arow);
-                            tma_load_3d_pair(&tmSB, fb, sf + L::CPS * SF_CHUNK, 0, sc, rb);
-                        } else {
+                    if constexpr (kPair) {
+                        if (rank == 0) {
+                            mbar_arrive_expect_tx(&sffull[stage], sf_tx);
                             mbar_arrive_expect_tx(&full[stage], tx);
-                            tma_load_2d(&tmA, &full[stage], adst, kb * BK, m0);
-                            tma_load_2d(&tmB, &full[stage], bdst, kb * BK, n0);
-                            tma_load_3d(&tmSA, &full[stage], sf, 0, sc, arow);
-                            tma_load_3d(&tmSB, &full[stage], sf + L::CPS * SF_CHUNK, 0, sc, rb);
                         }
-                    } else if constexpr (kPair) {
-                        if (rank == 0) mbar_arrive_expect_tx(&full[stage], tx);
-                        const uint32_t fb = full0 + stage * 8u;
+                        const uint32_t sb = sffull0 + stage * 8u, fb = full0 + stage * 8u;
+                        if constexpr (L::FP4) {
+                            // this CTA's row block of A's scales; all of the tile's row blocks of B's
+                            const int32_t sc = kb * L::CPS;
+                            tma_load_3d_pair(&tmSA, sb, sf, 0, sc, arow);
+                            tma_load_3d_pair(&tmSB, sb, sf + L::CPS * SF_CHUNK, 0, sc, rb);
+                        } else {
+                            tma_load_2d_pair(&tmSA, sb, sf, 0, ca + kb);
+                            tma_load_2d_pair(&tmSB, sb, sf + SF_CHUNK, 0, cb + kb);
+                            if (two)
+                                tma_load_2d_pair(&tmSB, sb, sf + 2 * SF_CHUNK, 0,
+                                                 cb + static_cast<int32_t>(p.sf_kc) + kb);
+                        }
                         tma_load_2d_pair(&tmA, fb, adst, kb * BK, m0);
                         tma_load_2d_pair(&tmB, fb, bdst, kb * BK, n0);
-                        tma_load_2d_pair(&tmSA, fb, sf, 0, ca + kb);
-                        tma_load_2d_pair(&tmSB, fb, sf + SF_CHUNK, 0, cb + kb);
-                        if (two) tma_load_2d_pair(&tmSB, fb, sf + 2 * SF_CHUNK, 0, cb + static_cast<int32_t>(p.sf_kc) + kb);
                     } else {
+                        mbar_arrive_expect_tx(&sffull[stage], sf_tx);
                         mbar_arrive_expect_tx(&full[stage], tx);
+                        if constexpr (L::FP4) {
+                            const int32_t sc = kb * L::CPS;
+                            tma_load_3d(&tmSA, &sffull[stage], sf, 0, sc, arow);
+                            tma_load_3d(&tmSB, &sffull[stage], sf + L::CPS * SF_CHUNK, 0, sc, rb);
+                        } else {
+                            tma_load_2d(&tmSA, &sffull[stage], sf, 0, ca + kb);
+                            tma_load_2d(&tmSB, &sffull[stage], sf + SF_CHUNK, 0, cb + kb);
+                            if (two)
+                                tma_load_2d(&tmSB, &sffull[stage], sf + 2 * SF_CHUNK, 0,
+                                            cb + static_cast<int32_t>(p.sf_kc) + kb);
+                        }
                         tma_load_2d(&tmA, &full[stage], adst, kb * BK, m0);
                         tma_load_2d(&tmB, &full[stage], bdst, kb * BK, n0);
-                        tma_load_2d(&tmSA, &full[stage], sf, 0, ca + kb);
-                        tma_load_2d(&tmSB, &full[stage], sf + SF_CHUNK, 0, cb + kb);
-                        if (two)
-                            tma_load_2d(&tmSB, &full[stage], sf + 2 * SF_CHUNK, 0, cb + static_cast<int32_t>(p.sf_kc) + kb);
                     }
                     ++issued;
                     if (++stage == STAGES) {
@@ -362,6 +373,8 @@ __global__ void __launch_bounds__(Layout<kBN, kPair, kARows, kFmt>::THREADS, 1)
                         } else {
                             --s;
                         }
+                        if (!mx_drain_wait(&sffull[s], ph, p.timeout_ns) && p.status)
+                            atomicOr(p.status, kStatusTimeoutDrain);
                         if (!mx_drain_wait(&full[s], ph, p.timeout_ns) && p.status)
                             atomicOr(p.status, kStatusTimeoutDrain);
                     }
@@ -377,7 +390,7 @@ __global__ void __launch_bounds__(Layout<kBN, kPair, kARows, kFmt>::THREADS, 1)
         if (lane == 0 && rank == 0) {
             const uint64_t adesc0 = make_smem_desc_sw128(smem_addr(smem + L::OFF_A), 16, 1024);
             const uint64_t bdesc0 = make_smem_desc_sw128(smem_addr(smem + L::OFF_B), 16, 1024);
-            const uint32_t ready_a = smem_addr(sfready), empty_a = smem_addr(empty);
+            const uint32_t ready_a = smem_addr(sfready), empty_a = smem_addr(empty), full_a = smem_addr(full);
             uint32_t stage = 0, phase = 0;
             uint32_t acc = 0, acc_phase = 0;
             bool ok = true;
@@ -427,8 +440,10 @@ __global__ void __launch_bounds__(Layout<kBN, kPair, kARows, kFmt>::THREADS, 1)
                         const uint64_t bd = bdesc0 + stage * (L::B_BYTES >> 4);
 #pragma unroll
                         for (int half = 0; half < 2; ++half) {
-                            // the operands have landed and this half's scales are in TMEM
-                            if (!mbar_wait(&sfready[half * STAGES + stage], phase, ctl, kStatusTimeoutMma)) {
+                            // this half's scales are in TMEM (and, before the first half, the
+                            // stage's operands have landed)
+                            if (!mbar_wait(&sfready[half * STAGES + stage], phase, ctl, kStatusTimeoutMma) ||
+                                (half == 0 && !mbar_wait(&full[stage], phase, ctl, kStatusTimeoutMma))) {
                                 ok = false;
                                 break;
                             }
@@ -467,13 +482,18 @@ __global__ void __launch_bounds__(Layout<kBN, kPair, kARows, kFmt>::THREADS, 1)
                         const uint32_t nphase = stage + 1 == STAGES ? phase ^ 1u : phase;
                         const uint32_t st2 =
                             mbar_try_wait_and_test(ready_a + stage * 8u, phase, ready_a + nstage * 8u, nphase);
-                        if (!(st2 & 1u) && !mbar_wait(&sfready[stage], phase, ctl, kStatusTimeoutMma)) {
+                        if ((!(st2 & 1u) && !mbar_wait(&sfready[stage], phase, ctl, kStatusTimeoutMma)) ||
+                            !mbar_wait(&full[stage], phase, ctl, kStatusTimeoutMma)) {
                             ok = false;
                             break;
                         }
                         tc_fence_after();
                         issue(kb++);
-                        if ((st2 & 2u) && kb < p.kb) issue(kb++);
+                        // the next stage too, if its scales are in and its operands have landed
+                        if ((st2 & 2u) && kb < p.kb && mbar_try_wait(full_a + stage * 8u, phase)) {
+                            tc_fence_after();
+                            issue(kb++);
+                        }
                     }
                 }
                 if (!ok) break;
@@ -502,7 +522,7 @@ __global__ void __launch_bounds__(Layout<kBN, kPair, kARows, kFmt>::THREADS, 1)
         if (lane == 0 && rank == 0) {
             // a scale chunk: 32 rows of 16 bytes, groups of 8 rows 128 bytes apart
             const uint64_t sdesc0 = make_smem_desc_plain(smem_addr(smem + L::OFF_SF), 512, 128);
-            const uint32_t full_a = smem_addr(full);
+            const uint32_t sffull_a = smem_addr(sffull);
             uint64_t *ready = sfready + cw * STAGES;
             uint32_t stage = 0, phase = 0;
             bool ok = true;
@@ -511,9 +531,10 @@ __global__ void __launch_bounds__(Layout<kBN, kPair, kARows, kFmt>::THREADS, 1)
             for (int64_t t = worker; ok && work_item(p.sched, t, kBN, w); t += workers) {
                 for (int32_t kb = 0; kb < p.kb; ++kb) {
                     // Stage s was last read by MMAs that completed before the producer
-                    // could refill it, so its TMEM scale columns are free once it is full.
-                    if (!mbar_try_wait(full_a + stage * 8u, phase) &&
-                        !mbar_wait(&full[stage], phase, ctl, kStatusTimeoutMma)) {
+                    // could refill it, so its TMEM scale columns are free once its
+                    // scales have landed.
+                    if (!mbar_try_wait(sffull_a + stage * 8u, phase) &&
+                        !mbar_wait(&sffull[stage], phase, ctl, kStatusTimeoutMma)) {
                         ok = false;
                         break;
                     }
@@ -620,15 +641,22 @@ __global__ void __launch_bounds__(Layout<kBN, kPair, kARows, kFmt>::THREADS, 1)
                     // (alpha applied, one rounding), hand the accumulator back, and
                     // only then stage and store the chunks.
                     uint32_t packed[kBN / 2];
+                    // two 32-column loads in flight per wait: the drain's length is
+                    // the loads' latency, one wait per pair of groups
 #pragma unroll
-                    for (int g = 0; g < kBN / 32; ++g) {
-                        uint32_t ra[32];
-                        tmem_ld32(tmem_base + acc * kBN + static_cast<uint32_t>(g * 32) + ((q * 32u) << 16), ra);
+                    for (int g = 0; g < kBN / 32; g += 2) {
+                        uint32_t ra[32], rb[32];
+                        const uint32_t ta = tmem_base + acc * kBN + static_cast<uint32_t>(g * 32) + ((q * 32u) << 16);
+                        tmem_ld32(ta, ra);
+                        tmem_ld32(ta + 32, rb);
                         tc_wait_ld();
 #pragma unroll
-                        for (int e = 0; e < 16; ++e)
+                        for (int e = 0; e < 16; ++e) {
                             packed[g * 16 + e] = pack_bf16x2(p.alpha * __uint_as_float(ra[2 * e]),
                                                              p.alpha * __uint_as_float(ra[2 * e + 1]));
+                            packed[g * 16 + 16 + e] = pack_bf16x2(p.alpha * __uint_as_float(rb[2 * e]),
+                                                                  p.alpha * __uint_as_float(rb[2 * e + 1]));
+                        }
                     }
                     release();
                     // N is a whole number of 16-byte cells here, so every chunk goes
