@@ -57,6 +57,8 @@ def parse_args():
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="budget of the oracle sample")
     ap.add_argument("--no-sustained", action="store_true", help="skip the repetitions and the sustained regions")
     ap.add_argument("--only-mx", action="store_true", help="of the per_config rows, measure the block-scaled (MXFP8, FP4) ones only")
+    ap.add_argument("--only-rows", default=None,
+                    help="comma-separated names of the block-scaled rows to measure (implies --only-mx)")
     return ap.parse_args()
 
 
@@ -373,7 +375,10 @@ def block_scaled_rows(torch, tpd, h, l2, peaks, local, barrier, args, rows):
     second against the HBM copy peak; with torch._scaled_mm on the same
     buffers when this torch offers it, and the oracle's CPU baseline."""
     out = {}
+    keep = set(args.only_rows.split(",")) if args.only_rows else None
     for r in rows:
+        if keep is not None and r["name"] not in keep:
+            continue
         name, cfg, wl = r["name"], r["cfg"], r["make"](r["cfg"], torch, l2)
         plan = r["plan"](cfg)
         steps = r["steps"]
@@ -445,7 +450,7 @@ def fp4_entries(torch, tpd, h, l2, peaks, local, barrier, rank, world, args):
     plan = lambda c: tpd.gemm_fp4_query_plan(h, c.fmt, c.M, c.N, c.K)  # noqa: E731
     rows = [{"name": n, "cfg": FP4_CONFIGS[n], "make": Fp4Workload, "torch": TorchScaledMMFp4, "plan": plan,
              "ratio": 6.0, "hbm": n != "nvfp4_qkv", "steps": 200 if n == "nvfp4_qkv" else 400,
-             "sustained": n == "nvfp4_qkv", "cpu": cpu} for n in FP4_CONFIGS]
+             "sustained": n == "nvfp4_qkv", "cpu": cpu} for n in ["nvfp4_qkv", "nvfp4_m256", "nvfp4_decode"]]
     return block_scaled_rows(torch, tpd, h, l2, peaks, local, barrier, args, rows)
 
 
@@ -935,6 +940,8 @@ def run_ours(args):
     per_config = {}
     launches = args.steps
     torch_rows = {}
+    if args.only_rows:
+        args.only_mx = True
     bf16_extra = not args.no_extra and not args.only_mx
     if bf16_extra:
         if cfg.name != "tiny":
@@ -1012,10 +1019,10 @@ def run_ours(args):
             torch.cuda.empty_cache()
 
     if not args.no_extra:
-        per_config.update(mx_entries(torch, tpd, h, l2, peaks, local, barrier, rank, world, args))
-        launches += 200 + 400 + 400
-        per_config.update(fp4_entries(torch, tpd, h, l2, peaks, local, barrier, rank, world, args))
-        launches += 400 + 400 + 200
+        bs = mx_entries(torch, tpd, h, l2, peaks, local, barrier, rank, world, args)
+        bs.update(fp4_entries(torch, tpd, h, l2, peaks, local, barrier, rank, world, args))
+        per_config.update(bs)
+        launches += sum(e["steps"] for e in bs.values())
 
     if bf16_extra:
         per_config["tp_overlay_chunks"] = chunk_tradeoff(torch, tpd, h)

@@ -1,11 +1,12 @@
 """Builds libtpgemm.so in-tree with nvcc for sm_103a.
 
-Ten translation units compiled in parallel: the host library (tpgemm.cu),
-the streaming-kernel instantiations (stream_inst.cu), the block-scaled (MX)
-kernel's (mx_inst.cu), the tiled-kernel
-instantiations, one per fused-epilogue mode (tiled_inst.cu with
--DTPG_EPI=0..5, 5 being the plain epilogue for alpha == 1), and the grouped
-tiled kernel (-DTPG_GROUPED=1); then one link.
+Twelve translation units compiled in parallel: the host library
+(tpgemm.cu), the streaming-kernel instantiations (stream_inst.cu), the
+block-scaled kernel's MXFP8 ones (mx_inst.cu) and FP4 ones (fp4_inst.cu with
+-DTPG_FP4=1 for NVFP4 and 2 for MXFP4), the tiled-kernel instantiations, one
+per fused-epilogue mode (tiled_inst.cu with -DTPG_EPI=0..5, 5 being the plain
+epilogue for alpha == 1), and the grouped tiled kernel (-DTPG_GROUPED=1);
+then one link.
 """
 from __future__ import annotations
 
