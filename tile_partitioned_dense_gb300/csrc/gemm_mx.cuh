@@ -628,7 +628,7 @@ __global__ void __launch_bounds__(Layout<kBN, kPair, kARows, kFmt>::THREADS, 1)
                 __syncwarp();
                 if (lane == 0) {
                     if constexpr (kPair)
-                        mbar_arrive_cluster(tempty0 + acc_now * 8u);
+                        mbar_arrive_cluster_relaxed(tempty0 + acc_now * 8u); // hands over no memory
                     else
                         mbar_arrive(&tempty[acc_now]);
                 }

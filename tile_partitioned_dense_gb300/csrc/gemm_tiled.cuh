@@ -707,7 +707,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 __syncwarp();
                 if (lane == 0) {
                     if constexpr (kPair)
-                        mbar_arrive_cluster(tempty0 + acc_now * 8u);
+                        mbar_arrive_cluster_relaxed(tempty0 + acc_now * 8u); // hands over no memory
                     else
                         mbar_arrive(&tempty[acc_now]);
                 }
@@ -765,6 +765,23 @@ __global__ void __launch_bounds__(THREADS, 1)
                 }
                 if (c == nchunks - 1) release();
                 uint8_t *rowp = buf + row * 128u;
+                if (!kOutF32 && !kFused && !has_beta && !direct_tile && tail_cell < 0) {
+                    // The common bf16 chunk (no C, no fused ops, no ragged cell):
+                    // a short loop of its own. The general loop below is large
+                    // enough that running it once per tile cost 0.5-0.8 us per
+                    // chunk, measured, against about 0.15 for this one.
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        const uint32_t *src = j < 4 ? &r0[j * 8] : &r1[(j - 4) * 8];
+                        float v[8];
+#pragma unroll
+                        for (int e = 0; e < 8; ++e)
+                            v[e] = kEpi == kEpiUnitAlpha ? __uint_as_float(src[e]) : p.alpha * __uint_as_float(src[e]);
+                        *reinterpret_cast<uint4 *>(rowp + ((j ^ (row & 7u)) << 4)) =
+                            make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]), pack_bf16x2(v[4], v[5]),
+                                       pack_bf16x2(v[6], v[7]));
+                    }
+                } else
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
                     uint4 *cell = reinterpret_cast<uint4 *>(rowp + ((j ^ (row & 7u)) << 4));

@@ -77,6 +77,17 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
                  : "memory");
 }
 
+// The same arrive without release semantics, for a signal that hands over no
+// memory: an epilogue's "accumulator read" signal, given after
+// tcgen05.wait::ld has completed the TMEM loads (so the next MMAs cannot
+// overwrite columns still being read) and tcgen05.fence::before_thread_sync.
+// A cluster-scope release there waited for the thread's earlier memory
+// operations to reach cluster scope, measured at 1-2 us per tile.
+__device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t cluster_addr) {
+    asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
+                 : "memory");
+}
+
 __device__ __forceinline__ bool mbar_try_wait(uint32_t addr, uint32_t parity) {
     uint32_t ok;
     asm volatile(
