@@ -89,11 +89,12 @@ def _want(fmt, A, SA, Bt, SB, C, alpha, beta, out_dtype, rows=None):
 # (the column tail goes around the tensor map, and the last tile starts 64
 # rows into a scale row block); M <= 32 and M <= 64 on 128 x 192 tiles with
 # 32- and 64-row A boxes; 128-row boxes for M in (64, 128]; one 128 x 128 tile
-# with a long K.
+# with a long K; degenerate outputs: one element with K of a single NVFP4
+# block (16) or MXFP4 block (32), and a few rows and columns with K = 64.
 SHAPES = [(256, 512, 512, None, None), (300, 200, 96, 64, 48), (200, 100, 320, 176, 160),
           (640, 1000, 1024, None, 528), (129, 577, 160, 96, 80), (16, 1000, 512, None, None),
           (33, 600, 192, None, None), (64, 577, 160, 96, 80), (100, 300, 256, None, None),
-          (128, 128, 4096, None, None)]
+          (128, 128, 4096, None, None), (1, 1, 32, None, None), (3, 5, 64, None, None)]
 
 
 def _ids(s):
@@ -228,3 +229,11 @@ def test_fp4_plan(h):
         p = tpd.gemm_fp4_query_plan(h, fmt, 100, 128, 4096)  # N <= 128: 128 x 128 tiles
         assert p["tile_n"] == 128 and p["num_tiles"] == 1
         assert max(sizes) <= 232448
+
+
+def test_fp4_single_nvfp4_block(h):
+    """M = N = 1, K = 16: one NVFP4 block, a fraction of a stage, a chunk and a
+    TMA box; integer codes, so the one output is exact."""
+    A, SA, Bt, SB = make_fp4_inputs(1, 1, 16, seed=5, fmt=FP4_NV, integer=True)
+    D, _ = _run_fp4(h, FP4_NV, A, SA, Bt, SB, None, 1.0, 0.0, torch.float32)
+    assert_bit_exact(bits(D), _want(FP4_NV, A, SA, Bt, SB, None, 1.0, 0.0, torch.float32), "1x1x16")
