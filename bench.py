@@ -351,20 +351,22 @@ class Fp4Workload:
 
 
 class TorchScaledMMFp4:
-    """The same NVFP4 workload through torch._scaled_mm (NVIDIA's library
-    kernel), on the same buffers: a comparison row, not this library's path."""
+    """The same FP4 workload through torch._scaled_mm (NVIDIA's library
+    kernel), on the same buffers: a comparison row, not this library's path.
+    NVFP4 scales are E4M3, MXFP4 scales E8M0."""
 
     def __init__(self, wl, torch):
         self.wl = wl
         self.torch = torch
 
     def run(self, tpd, h, i, stream):
+        from workloads import FP4_NV
         torch = self.torch
         s = self.wl.sets[i % self.wl.nsets]
         a = s["A"].view(torch.float4_e2m1fn_x2)
         b = s["B"].view(torch.float4_e2m1fn_x2).t()
-        torch._scaled_mm(a, b, s["SA"].view(torch.float8_e4m3fn), s["SB"].view(torch.float8_e4m3fn),
-                         out_dtype=torch.bfloat16, out=s["D"])
+        sdt = torch.float8_e4m3fn if self.wl.cfg.fmt == FP4_NV else torch.float8_e8m0fnu
+        torch._scaled_mm(a, b, s["SA"].view(sdt), s["SB"].view(sdt), out_dtype=torch.bfloat16, out=s["D"])
         return 0
 
 
@@ -442,15 +444,16 @@ def mx_entries(torch, tpd, h, l2, peaks, local, barrier, rank, world, args):
 
 
 def fp4_entries(torch, tpd, h, l2, peaks, local, barrier, rank, world, args):
-    """The NVFP4 rows: the decode shape and a 256-row one HBM-bound (bytes of
-    B and its scales per second), the QKV shape against the FP4 tensor peak
-    (the measured bf16 peak times the nominal FP4 : bf16 ratio of 6)."""
+    """The FP4 rows: NVFP4 on the decode shape and a 256-row one, HBM-bound
+    (bytes of B and its scales per second), and on the QKV shape against the
+    FP4 tensor peak (the measured bf16 peak times the nominal FP4 : bf16 ratio
+    of 6); MXFP4 on the QKV shape, the same way."""
     from workloads import FP4_CONFIGS
     cpu = fp4_cpu_baseline if rank == 0 and world == 1 and not args.no_cpu_baseline else None
     plan = lambda c: tpd.gemm_fp4_query_plan(h, c.fmt, c.M, c.N, c.K)  # noqa: E731
     rows = [{"name": n, "cfg": FP4_CONFIGS[n], "make": Fp4Workload, "torch": TorchScaledMMFp4, "plan": plan,
-             "ratio": 6.0, "hbm": n != "nvfp4_qkv", "steps": 200 if n == "nvfp4_qkv" else 400,
-             "sustained": n == "nvfp4_qkv", "cpu": cpu} for n in ["nvfp4_qkv", "nvfp4_m256", "nvfp4_decode"]]
+             "ratio": 6.0, "hbm": not n.endswith("_qkv"), "steps": 200 if n.endswith("_qkv") else 400,
+             "sustained": n == "nvfp4_qkv", "cpu": cpu} for n in ["nvfp4_qkv", "nvfp4_m256", "nvfp4_decode", "mxfp4_qkv"]]
     return block_scaled_rows(torch, tpd, h, l2, peaks, local, barrier, args, rows)
 
 

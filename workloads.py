@@ -253,6 +253,8 @@ FP4_CONFIGS = {
                             "NVFP4 GEMM with 256 rows 256x28672x4096, E4M3 scales per 16, bf16 output"),
     "nvfp4_qkv": Fp4Config("nvfp4_qkv", FP4_NV, 8192, 6144, 4096, 17,
                            "NVFP4 QKV projection 8192x6144x4096, E4M3 scales per 16, bf16 output"),
+    "mxfp4_qkv": Fp4Config("mxfp4_qkv", FP4_MX, 8192, 6144, 4096, 18,
+                           "MXFP4 QKV projection 8192x6144x4096, E8M0 scales per 32, bf16 output"),
 }
 
 # magnitudes of the eight E2M1 codes 0..7 (the sign is bit 3)
